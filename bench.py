@@ -1,0 +1,361 @@
+"""Benchmark of the exact-attention hot path on GB300; prints ONE JSON line (rank 0).
+
+Headline workload: causal bf16 prefill, B=4, 32 heads, Nq = Nk = 4096, d = 128 (outputs O bf16 and
+fp32 LSE), measured as prefill TFLOP/s with causal FLOPs counted as half (4*d*Nq*Nk/2 per head).
+The same line carries the decode KV-cache GB/s of the two decode workloads and the varlen append
+workload in ``breakdown``, each with its own roofline, so that one run covers every step of the
+path (prefill tiles, split-K decode + merge, varlen dispatch).
+
+Timing: W untimed warm-up steps, then K steps bracketed by a barrier and a device synchronize,
+CUDA events on the launching stream; every workload's inputs are larger than L2 (129 MB), so no
+flush is needed between steps. ``e2e`` repeats the headline through the public API with pinned
+host buffers, host-to-device copies of the inputs and device-to-host copies of O and LSE inside
+the timed region. ``cpu_baseline`` times the fp64 oracle (as it stands) on a bounded sample.
+
+``--impl reference`` times the oracle itself on the host cores as the reference arm (a bounded
+sample of the headline workload per step). With ``--gpus N`` under torchrun every rank runs an
+independent replica (the path is single-GPU; nothing is exchanged), ``value`` is the work of all
+ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import exact_attention_flashattn_gb300 as bw  # noqa: E402
+from exact_attention_flashattn_gb300 import roofline as rl  # noqa: E402
+from exact_attention_flashattn_gb300 import workloads as wl  # noqa: E402
+
+HEADLINE = "prefill_causal_b4_h32_n4096_d128"
+METRIC = "prefill TFLOP/s and decode KV GB/s, 1×GB300, as fraction of roofline"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ timing helpers
+
+
+def time_steps(fn, steps, warmup, world, stream):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    n0 = bw.launch_count()
+    for i in range(steps):
+        starts[i].record(stream)
+        fn()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    launches = bw.launch_count() - n0
+    barrier(world)
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return per, launches
+
+
+def cpu_baseline_prefill(seconds_budget=12.0):
+    """fp64 oracle on whole heads of the headline workload (bounded: ~10-30 s of CPU work)."""
+    import numpy as np
+    import oracle
+    w = wl.WORKLOADS[HEADLINE]
+    q, k, v = wl.prefill_inputs(1, 2, 2, w.Nq, w.Nk, w.d, torch.bfloat16, seed=w.seed)
+    qs, ks, vs = (x.float().numpy().astype(np.float64) for x in (q, k, v))
+    heads, t = 0, 0.0
+    while t < seconds_budget and heads < 8:
+        h = heads % 2
+        t0 = time.perf_counter()
+        oracle.attention(qs[:, h:h + 1], ks[:, h:h + 1], vs[:, h:h + 1], True, method="tiled", block=128)
+        t += time.perf_counter() - t0
+        heads += 1
+    flops = rl.prefill_flops(1, heads, w.Nq, w.Nk, w.d, True)
+    return {"value": flops / t / 1e12, "unit": "TFLOP/s", "cores": oracle.hardware_threads(), "kind": "oracle",
+            "sample": f"{heads} whole heads (4096 causal rows, d=128) of the headline workload, tiled fp64 oracle, "
+                      f"{t:.1f} s"}
+
+
+# ------------------------------------------------------------------ reference arm
+
+
+def run_reference(args, rank, world):
+    import numpy as np
+    import oracle
+    if rank != 0:
+        return
+    w = wl.WORKLOADS[HEADLINE]
+    q, k, v = wl.prefill_inputs(1, 1, 1, w.Nq, w.Nk, w.d, torch.bfloat16, seed=w.seed)
+    qs, ks, vs = (x.float().numpy().astype(np.float64) for x in (q, k, v))
+    step = lambda: oracle.attention(qs, ks, vs, True, method="tiled", block=128)  # noqa: E731
+    for _ in range(args.warmup):
+        step()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        step()
+        times.append(time.perf_counter() - t0)
+    flops = rl.prefill_flops(1, 1, w.Nq, w.Nk, w.d, True)
+    ms = 1e3 * statistics.mean(times)
+    val = flops / (ms * 1e-3) / 1e12
+    cores = oracle.hardware_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": HEADLINE, "sample": "one whole head (b=0, h=0: 4096 causal rows, d=128) per step",
+                       "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": True},
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": "one whole head of the headline workload per step, tiled fp64 oracle"},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+# ------------------------------------------------------------------ main arm
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="own", choices=["own", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-breakdown", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        run_reference(args, rank, world)
+        return
+
+    rank, world, local = dist_setup(args.gpus)
+    peaks = load_peaks()
+    stream = torch.cuda.current_stream()
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    # ---------------- headline: causal prefill
+    x = wl.make(HEADLINE, device=dev)
+    w = x["w"]
+    q, k, v = x["q"], x["k"], x["v"]
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=dev)
+    step = lambda: bw.attn_fwd(q, k, v, causal=True, out=o, lse=lse)  # noqa: E731
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        per, launches = time_steps(step, args.steps, args.warmup, world, stream)
+    clocks = clk.summary()
+    ms = max_over_ranks(statistics.mean(per), world)
+    flops = rl.prefill_flops(w.B, w.Hq, w.Nq, w.Nk, w.d, True)
+    value = flops * world / (ms * 1e-3) / 1e12
+    achieved = flops / (ms * 1e-3) / 1e12
+    in_bytes = 3 * q.numel() * q.element_size()
+
+    # ---------------- e2e through the public API with pinned host buffers
+    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def e2e_step():
+        dq = hq.to(dev, non_blocking=True)
+        dk = hk.to(dev, non_blocking=True)
+        dv = hv.to(dev, non_blocking=True)
+        oo, ll = bw.attn_fwd(dq, dk, dv, causal=True)
+        ho.copy_(oo, non_blocking=True)
+        hl.copy_(ll, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 10))
+    per_e2e, _ = time_steps(e2e_step, e2e_steps, 3, world, stream)
+    ms_e2e = max_over_ranks(statistics.mean(per_e2e), world)
+    del hq, hk, hv
+    e2e = {"value": flops * world / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+           "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": o.numel() * o.element_size() + lse.numel() * 4}
+    del x, q, k, v, o, lse
+    torch.cuda.empty_cache()
+
+    # ---------------- breakdown: decode and varlen workloads
+    breakdown = {}
+    if not args.no_breakdown:
+        for name in ("decode_gqa_b8_h32x8_n32768_d128", "decode_long_b1_h64x8_n262144_d128"):
+            xd = wl.make(name, device=dev)
+            wd = xd["w"]
+            nk = xd["nk"].to(dev)
+            od = torch.empty_like(xd["q"])
+            ld = torch.empty((wd.B, wd.Hq), dtype=torch.float32, device=dev)
+            wsd = torch.empty(bw.decode_workspace_size(wd.B, wd.Hq, wd.d, wd.num_splits), dtype=torch.uint8,
+                              device=dev)
+            fn = lambda: bw.attn_decode(xd["q"], xd["kcache"], xd["vcache"], nk, wd.num_splits,  # noqa: E731
+                                        workspace=wsd, out=od, lse=ld)
+            perd, _ = time_steps(fn, args.steps, args.warmup, world, stream)
+            msd = max_over_ranks(statistics.mean(perd), world)
+            kvb = rl.decode_kv_bytes([wd.Nk] * wd.B, wd.Hkv, wd.d)
+            gbs = kvb / (msd * 1e-3) / 1e9
+            breakdown[name] = {"metric": "decode KV-cache GB/s", "value": gbs * world, "unit": "GB/s",
+                               "ms_per_step": msd, "num_splits": wd.num_splits,
+                               "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                                            "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                                            "algorithmic_bytes": kvb, "traffic": None,
+                                            "note": "split-K pass + merge, two launches, timed together"}}
+            del xd, od, ld, wsd, nk
+            torch.cuda.empty_cache()
+        xv = wl.make("varlen_append_64seq_h32x8_d128", device=dev)
+        wv = xv["w"]
+        cq, ck = xv["cu_q"].to(dev), xv["cu_k"].to(dev)
+        ov = torch.empty_like(xv["q"])
+        lv = torch.empty((xv["q"].shape[0], wv.Hq), dtype=torch.float32, device=dev)
+        mq, mk = max(xv["nq"]), max(xv["nk"])
+        wsv = torch.empty(bw.varlen_workspace_size(wv.num_seqs, mk, wv.Hq, wv.Hkv, wv.d), dtype=torch.uint8,
+                          device=dev)
+        fn = lambda: bw.attn_varlen(xv["q"], xv["k"], xv["v"], cq, ck, mq, mk, causal=True,  # noqa: E731
+                                    workspace=wsv, out=ov, lse=lv)
+        perv, _ = time_steps(fn, args.steps, args.warmup, world, stream)
+        msv = max_over_ranks(statistics.mean(perv), world)
+        fv = rl.varlen_flops(xv["nq"], xv["nk"], wv.Hq, wv.d, True)
+        bv = rl.varlen_bytes(xv["nq"], xv["nk"], wv.Hq, wv.Hkv, wv.d)
+        t_roof = rl.varlen_roofline_seconds(xv["nq"], xv["nk"], wv.Hq, wv.Hkv, wv.d, True,
+                                            peaks["bf16_tflops"] * 1e12, peaks["hbm_gbs"] * 1e9)
+        breakdown["varlen_append_64seq_h32x8_d128"] = {
+            "metric": "varlen TFLOP/s", "value": fv * world / (msv * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "ms_per_step": msv, "kv_bytes": bv,
+            "roofline": {"bound": "mixed", "achieved_s": msv * 1e-3, "roofline_s": t_roof,
+                         "frac": t_roof / (msv * 1e-3),
+                         "note": "sum over sequences of max(FLOPs/peak_bf16, bytes/peak_hbm) over measured time"}}
+        del xv, ov, lv, wsv
+        torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_prefill()
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": HEADLINE, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+                       "causal": True, "flops_per_step": flops, "flop_convention": "causal counted as half",
+                       "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB of Q/K/V per step), no flush",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                         "peak_source": f"{peaks['source']} bf16 burst"},
+            "e2e": e2e, "gpu_launches": launches, "clocks": clocks, "cpu_baseline": cpu, "breakdown": breakdown,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

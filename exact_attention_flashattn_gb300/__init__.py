@@ -1,1 +1,257 @@
-"""placeholder"""
+"""Exact scaled-dot-product attention on GB300: Python binding of ``libbwattn``.
+
+Every function here only checks and marshals arguments (shapes, dtypes, device pointers,
+the current CUDA stream) and calls the C-ABI in ``libbwattn.so``; all arithmetic runs in the
+library's CUDA kernels. PyTorch supplies device memory and streams. There is no fallback:
+if the library is missing or a call fails, a ``RuntimeError`` is raised.
+
+Calls (see ``include/bwattn.h`` for the full contract):
+
+* ``attn_fwd(q, k, v, causal, scale)``: prefill / cross attention, q [B, Hq, Nq, d],
+  k, v [B, Hkv, Nk, d]; bf16 (tcgen05 kernel) or fp32 (fp32 FMA kernel).
+* ``attn_decode(q, kcache, vcache, nk, num_splits)``: single-query split-K decode,
+  q [B, Hq, d], caches [B, Hkv, cap, d] bf16, nk [B] int32 on the device.
+* ``attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, causal)``:
+  packed sequences, q [total_q, Hq, d], k, v [total_k, Hkv, d] bf16.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "attn_fwd", "attn_decode", "attn_varlen", "decode_workspace_size", "varlen_workspace_size",
+    "get_status", "clear_status", "set_wait_timeout_ns", "test_wait_timeout", "launch_count", "lib",
+    "BwattnError", "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_TIMEOUT",
+]
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
+DTYPE_FP32, DTYPE_BF16 = 0, 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libbwattn.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class BwattnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"libbwattn.so not found at {LIB_PATH}; build it with "
+                "`python -m exact_attention_flashattn_gb300.build` (needs nvcc for sm_103a)")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, ci, cf, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        L.attn_fwd.argtypes = [vp, vp, vp, vp, vp] + [ci] * 7 + [cf, ci, vp]
+        L.attn_fwd.restype = ci
+        L.attn_decode_workspace_size.argtypes = [ci, ci, ci, ci]
+        L.attn_decode_workspace_size.restype = sz
+        L.attn_decode.argtypes = [vp, vp, vp, vp, vp] + [ci] * 6 + [cf, vp, vp, sz, vp]
+        L.attn_decode.restype = ci
+        L.attn_varlen_workspace_size.argtypes = [ci] * 5
+        L.attn_varlen_workspace_size.restype = sz
+        L.attn_varlen.argtypes = [vp] * 7 + [ci] * 9 + [cf, vp, sz, vp]
+        L.attn_varlen.restype = ci
+        L.bwattn_last_cuda_error.argtypes = []
+        L.bwattn_last_cuda_error.restype = ci
+        L.bwattn_status_string.argtypes = [ci]
+        L.bwattn_status_string.restype = ctypes.c_char_p
+        L.bwattn_get_status.argtypes = [vp]
+        L.bwattn_get_status.restype = ci
+        L.bwattn_clear_status.argtypes = [vp]
+        L.bwattn_clear_status.restype = ci
+        L.bwattn_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+        L.bwattn_set_wait_timeout_ns.restype = None
+        L.bwattn_test_wait_timeout.argtypes = [vp]
+        L.bwattn_test_wait_timeout.restype = ci
+        L.bwattn_launch_count.argtypes = []
+        L.bwattn_launch_count.restype = ctypes.c_uint64
+        L.bwattn_version.argtypes = []
+        L.bwattn_version.restype = ci
+        _lib = L
+        return L
+
+
+def status_string(status: int) -> str:
+    try:
+        return lib().bwattn_status_string(int(status)).decode()
+    except Exception:  # pragma: no cover - only when the library itself is missing
+        return "unknown"
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        if rc == ERR_CUDA:
+            err = lib().bwattn_last_cuda_error()
+            raise BwattnError(rc, f"{what} (cudaError {err})")
+        raise BwattnError(rc, what)
+
+
+def _stream(stream=None) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else int(t.data_ptr())
+
+
+def _cuda(t: torch.Tensor, name: str, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _scale(scale, d):
+    return (1.0 / math.sqrt(d)) if scale is None else float(scale)
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = True, scale: float | None = None,
+             out: torch.Tensor | None = None, lse: torch.Tensor | bool | None = True, stream=None):
+    """Prefill / cross attention. q [B, Hq, Nq, d]; k, v [B, Hkv, Nk, d] -> (o, lse or None)."""
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D [B, H, N, d]")
+    B, Hq, Nq, d = q.shape
+    Bk, Hkv, Nk, dk = k.shape
+    if Bk != B or dk != d or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k and v must be [B, Hkv, Nk, d] with q's B and d")
+    if q.dtype == torch.bfloat16:
+        dt = DTYPE_BF16
+    elif q.dtype == torch.float32:
+        dt = DTYPE_FP32
+    else:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _cuda(t, n, q.dtype)
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda(out, "out", q.dtype)
+    lse_t = None
+    if lse is True:
+        lse_t = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    elif isinstance(lse, torch.Tensor):
+        lse_t = lse
+        _cuda(lse_t, "lse", torch.float32)
+    rc = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse_t), B, Hq, Hkv, Nq, Nk, d, int(bool(causal)),
+                        _scale(scale, d), dt, _stream(stream))
+    _check(rc, "attn_fwd")
+    return out, lse_t
+
+
+def decode_workspace_size(B: int, Hq: int, d: int, num_splits: int) -> int:
+    return int(lib().attn_decode_workspace_size(B, Hq, d, num_splits))
+
+
+def attn_decode(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Tensor, nk: torch.Tensor, num_splits: int,
+                scale: float | None = None, workspace: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                lse: torch.Tensor | bool | None = True, stream=None):
+    """Single-query decode. q [B, Hq, d]; caches [B, Hkv, cap, d]; nk [B] int32 (device)."""
+    if q.dim() != 3 or kcache.dim() != 4:
+        raise ValueError("q must be [B, Hq, d] and caches [B, Hkv, cap, d]")
+    B, Hq, d = q.shape
+    Bk, Hkv, cap, dk = kcache.shape
+    if Bk != B or dk != d or tuple(vcache.shape) != tuple(kcache.shape):
+        raise ValueError("kcache and vcache must be [B, Hkv, cap, d] with q's B and d")
+    for t, n in ((q, "q"), (kcache, "kcache"), (vcache, "vcache")):
+        _cuda(t, n, torch.bfloat16)
+    _cuda(nk, "nk", torch.int32)
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda(out, "out", torch.bfloat16)
+    lse_t = None
+    if lse is True:
+        lse_t = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    elif isinstance(lse, torch.Tensor):
+        lse_t = lse
+        _cuda(lse_t, "lse", torch.float32)
+    need = decode_workspace_size(B, Hq, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _cuda(workspace, "workspace")
+    rc = lib().attn_decode(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(out), _ptr(nk), B, Hq, Hkv, cap, d,
+                           int(num_splits), _scale(scale, d), _ptr(lse_t), _ptr(workspace),
+                           workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "attn_decode")
+    return out, lse_t
+
+
+def varlen_workspace_size(num_seqs: int, max_seqlen_k: int, Hq: int, Hkv: int, d: int) -> int:
+    return int(lib().attn_varlen_workspace_size(num_seqs, max_seqlen_k, Hq, Hkv, d))
+
+
+def attn_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q: torch.Tensor,
+                cu_seqlens_k: torch.Tensor, max_seqlen_q: int, max_seqlen_k: int, causal: bool = True,
+                scale: float | None = None, workspace: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                lse: torch.Tensor | bool | None = True, stream=None):
+    """Packed varlen. q [total_q, Hq, d]; k, v [total_k, Hkv, d]; cu_seqlens int32 [num_seqs + 1] (device)."""
+    if q.dim() != 3 or k.dim() != 3:
+        raise ValueError("q must be [total_q, Hq, d] and k, v [total_k, Hkv, d]")
+    tq, Hq, d = q.shape
+    tk, Hkv, dk = k.shape
+    if dk != d or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k and v must be [total_k, Hkv, d] with q's d")
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _cuda(t, n, torch.bfloat16)
+    _cuda(cu_seqlens_q, "cu_seqlens_q", torch.int32)
+    _cuda(cu_seqlens_k, "cu_seqlens_k", torch.int32)
+    num_seqs = cu_seqlens_q.numel() - 1
+    if cu_seqlens_k.numel() != num_seqs + 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must have the same length")
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda(out, "out", torch.bfloat16)
+    lse_t = None
+    if lse is True:
+        lse_t = torch.empty((tq, Hq), dtype=torch.float32, device=q.device)
+    elif isinstance(lse, torch.Tensor):
+        lse_t = lse
+        _cuda(lse_t, "lse", torch.float32)
+    need = varlen_workspace_size(num_seqs, int(max_seqlen_k), Hq, Hkv, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _cuda(workspace, "workspace")
+    rc = lib().attn_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse_t), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+                           num_seqs, tq, tk, int(max_seqlen_q), int(max_seqlen_k), Hq, Hkv, d, int(bool(causal)),
+                           _scale(scale, d), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                           _stream(stream))
+    _check(rc, "attn_varlen")
+    return out, lse_t
+
+
+def get_status(stream=None) -> int:
+    """Synchronises the stream; BWATTN_ERR_TIMEOUT if a kernel gave up a wait, else OK."""
+    return int(lib().bwattn_get_status(_stream(stream)))
+
+
+def clear_status(stream=None) -> None:
+    _check(lib().bwattn_clear_status(_stream(stream)), "bwattn_clear_status")
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    lib().bwattn_set_wait_timeout_ns(int(ns))
+
+
+def test_wait_timeout(stream=None) -> None:
+    _check(lib().bwattn_test_wait_timeout(_stream(stream)), "bwattn_test_wait_timeout")
+
+
+def launch_count() -> int:
+    return int(lib().bwattn_launch_count())

@@ -1,0 +1,398 @@
+// C-ABI of libbwattn: argument validation, TMA tensor-map encoding, workspace layout and
+// kernel dispatch. See include/bwattn.h for the contract of every entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "../../include/bwattn.h"
+#include "kernels.h"
+
+namespace {
+
+__device__ unsigned int g_status_word;
+
+thread_local int t_last_cuda_error = 0;
+std::atomic<uint64_t> g_launches{0};
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned int* g_status_ptr[kMaxDevices] = {};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int cuda_fail(cudaError_t e) {
+  t_last_cuda_error = static_cast<int>(e);
+  return BWATTN_ERR_CUDA;
+}
+
+// Device address of the status word on the current device (looked up once per device).
+cudaError_t status_ptr(unsigned int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_status_word);
+    if (e != cudaSuccess) return e;
+    g_status_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  *out = g_status_ptr[dev];
+  return cudaSuccess;
+}
+
+cudaError_t encoder(EncodeTiledFn* out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorSymbolNotFound;
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  *out = g_encode;
+  return cudaSuccess;
+}
+
+// 3-D bf16 map {d, dim1, dim2} with row strides in elements, box {64, box1, box2},
+// 128-byte swizzle, zero fill out of bounds.
+cudaError_t make_map(CUtensorMap* m, const void* base, int d, int64_t dim1, int64_t dim2, int64_t stride1_elems,
+                     int64_t stride2_elems, int box1, int box2) {
+  EncodeTiledFn enc = nullptr;
+  cudaError_t e = encoder(&enc);
+  if (e != cudaSuccess) return e;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(dim1),
+                              static_cast<cuuint64_t>(dim2)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(stride1_elems) * 2,
+                                 static_cast<cuuint64_t>(stride2_elems) * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box1), static_cast<cuuint32_t>(box2)};
+  const cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+bool good_scale(float s) { return isfinite(s) && s > 0.f; }
+
+constexpr int kSmallRowsLimit = 32;  // varlen: n_q * g at or below this takes the split-K path
+constexpr int kVarlenKeysPerSplit = 2048;
+constexpr int kVarlenMaxSplits = 64;
+
+int varlen_splits(int max_seqlen_k) {
+  int s = (max_seqlen_k + kVarlenKeysPerSplit - 1) / kVarlenKeysPerSplit;
+  if (s < 1) s = 1;
+  if (s > kVarlenMaxSplits) s = kVarlenMaxSplits;
+  return s;
+}
+
+}  // namespace
+
+extern "C" {
+
+int bwattn_version(void) { return 100; }
+
+int bwattn_last_cuda_error(void) { return t_last_cuda_error; }
+
+uint64_t bwattn_launch_count(void) { return g_launches.load(); }
+
+void bwattn_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 1); }
+
+const char* bwattn_status_string(int status) {
+  switch (status) {
+    case BWATTN_OK:
+      return "ok";
+    case BWATTN_ERR_INVALID_ARG:
+      return "invalid argument";
+    case BWATTN_ERR_UNSUPPORTED:
+      return "unsupported configuration";
+    case BWATTN_ERR_CUDA:
+      return "CUDA error";
+    case BWATTN_ERR_TIMEOUT:
+      return "a kernel gave up an internal wait";
+    default:
+      return "unknown status";
+  }
+}
+
+int bwattn_get_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  unsigned int* p = nullptr;
+  if ((e = status_ptr(&p)) != cudaSuccess) return cuda_fail(e);
+  unsigned int v = 0;
+  if ((e = cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost)) != cudaSuccess) return cuda_fail(e);
+  return (v & bw::kStatusTimeoutBit) ? BWATTN_ERR_TIMEOUT : BWATTN_OK;
+}
+
+int bwattn_clear_status(void* stream) {
+  unsigned int* p = nullptr;
+  cudaError_t e = status_ptr(&p);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaMemsetAsync(p, 0, sizeof(unsigned int), static_cast<cudaStream_t>(stream))) != cudaSuccess)
+    return cuda_fail(e);
+  return BWATTN_OK;
+}
+
+int bwattn_test_wait_timeout(void* stream) {
+  unsigned int* p = nullptr;
+  cudaError_t e = status_ptr(&p);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = bw::launch_wait_timeout_probe(g_timeout_ns.load(), p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  g_launches.fetch_add(1);
+  return BWATTN_OK;
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+             int Nk, int d, int causal, float scale, int dtype, void* stream) {
+  if (B < 0 || Nq < 0 || Nk < 0 || Hq <= 0 || Hkv <= 0 || d <= 0) return BWATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || !good_scale(scale) || (causal != 0 && causal != 1)) return BWATTN_ERR_INVALID_ARG;
+  if (B > 65535 || Hq > 65535) return BWATTN_ERR_INVALID_ARG;
+  if (dtype != BWATTN_DTYPE_FP32 && dtype != BWATTN_DTYPE_BF16) return BWATTN_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return BWATTN_ERR_UNSUPPORTED;
+  if (B == 0 || Nq == 0) return BWATTN_OK;
+  if (!q || !o || ((!k || !v) && Nk > 0)) return BWATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(o) || (Nk > 0 && (!aligned16(k) || !aligned16(v)))) return BWATTN_ERR_INVALID_ARG;
+  if (lse && !aligned4(lse)) return BWATTN_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const float sl2 = scale * bw::kLog2e;
+  cudaError_t e;
+  if (dtype == BWATTN_DTYPE_FP32) {
+    bw::Fp32FwdArgs a{static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),
+                      static_cast<float*>(o), lse, B, Hq, Hkv, Nq, Nk, d, causal, sl2};
+    if ((e = bw::launch_prefill_fp32(a, st)) != cudaSuccess) return cuda_fail(e);
+    g_launches.fetch_add(1);
+    return BWATTN_OK;
+  }
+  bw::TcFwdArgs a{};
+  const int nk_map = Nk > 0 ? Nk : 1;
+  const void* kp = Nk > 0 ? k : q;
+  const void* vp = Nk > 0 ? v : q;
+  if ((e = make_map(&a.tm_q, q, d, Nq, static_cast<int64_t>(B) * Hq, d, static_cast<int64_t>(Nq) * d, 128, 1)) !=
+      cudaSuccess)
+    return cuda_fail(e);
+  const int64_t kv_heads_map = Nk > 0 ? static_cast<int64_t>(B) * Hkv : static_cast<int64_t>(B) * Hq;
+  const int nk_rows = Nk > 0 ? nk_map : Nq;
+  if ((e = make_map(&a.tm_k, kp, d, nk_rows, kv_heads_map, d, static_cast<int64_t>(nk_rows) * d, 128, 1)) !=
+      cudaSuccess)
+    return cuda_fail(e);
+  if ((e = make_map(&a.tm_v, vp, d, nk_rows, kv_heads_map, d, static_cast<int64_t>(nk_rows) * d, 128, 1)) !=
+      cudaSuccess)
+    return cuda_fail(e);
+  a.o = static_cast<uint16_t*>(o);
+  a.lse = lse;
+  a.cu_q = a.cu_k = nullptr;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.d = d;
+  a.causal = causal;
+  a.num_seqs = B;
+  a.small_rows_limit = 0;
+  a.max_pairs = (Nq + 255) / 256;
+  a.scale_log2 = sl2;
+  a.timeout_ns = g_timeout_ns.load();
+  unsigned int* sp = nullptr;
+  if ((e = status_ptr(&sp)) != cudaSuccess) return cuda_fail(e);
+  if ((e = bw::launch_prefill_tc(a, sp, st)) != cudaSuccess) return cuda_fail(e);
+  g_launches.fetch_add(1);
+  return BWATTN_OK;
+}
+
+size_t attn_decode_workspace_size(int B, int Hq, int d, int num_splits) {
+  if (B <= 0 || Hq <= 0 || d <= 0 || num_splits <= 0) return 0;
+  // units x rows = B x Hq (rows_max = g per (sequence, KV head))
+  return bw::splitk_ws_bytes(B, num_splits, Hq, d);
+}
+
+int attn_decode(const void* q, const void* kcache, const void* vcache, void* o, const int32_t* nk, int B, int Hq,
+                int Hkv, int nk_cap, int d, int num_splits, float scale, float* lse, void* workspace,
+                size_t workspace_bytes, void* stream) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || nk_cap < 0 || d <= 0) return BWATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || !good_scale(scale) || num_splits < 1 || num_splits > 1024) return BWATTN_ERR_INVALID_ARG;
+  if (B > 65535) return BWATTN_ERR_INVALID_ARG;
+  const int g = Hq / Hkv;
+  if (d != 128 || g > 32 || Hkv > 32767) return BWATTN_ERR_UNSUPPORTED;
+  if (B == 0) return BWATTN_OK;
+  if (!q || !kcache || !vcache || !o || !nk || !workspace) return BWATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) || !aligned16(workspace) ||
+      !aligned4(nk) || (lse && !aligned4(lse)))
+    return BWATTN_ERR_INVALID_ARG;
+  // workspace: units = B * Hkv, rows_max = g
+  const size_t need = bw::splitk_ws_bytes(B * Hkv, num_splits, g, d);
+  if (workspace_bytes < need) return BWATTN_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const float sl2 = scale * bw::kLog2e;
+  bw::SplitKArgs a{};
+  a.q = static_cast<const uint16_t*>(q);
+  a.k = static_cast<const uint16_t*>(kcache);
+  a.v = static_cast<const uint16_t*>(vcache);
+  a.ws = static_cast<float*>(workspace);
+  a.nk = nk;
+  a.cu_q = a.cu_k = nullptr;
+  a.num_seqs = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.g = g;
+  a.kv_seq_stride = static_cast<int64_t>(Hkv) * nk_cap * d;
+  a.kv_head_stride = static_cast<int64_t>(nk_cap) * d;
+  a.kv_key_stride = d;
+  a.kv_cap = nk_cap;
+  a.total_q = a.total_k = 0;
+  a.num_splits = num_splits;
+  a.rows_max = g;
+  a.row_groups = (g + 15) / 16;
+  a.causal = 0;
+  a.small_rows_limit = g;
+  a.ws_o_offset = bw::splitk_o_offset(B * Hkv, num_splits, g);
+  a.scale_log2 = sl2;
+  cudaError_t e;
+  if ((e = bw::launch_splitk(a, st)) != cudaSuccess) return cuda_fail(e);
+  g_launches.fetch_add(1);
+  bw::MergeArgs m{};
+  m.ws = a.ws;
+  m.o = static_cast<uint16_t*>(o);
+  m.lse = lse;
+  m.cu_q = m.cu_k = nullptr;
+  m.nk = nk;
+  m.num_seqs = B;
+  m.Hq = Hq;
+  m.Hkv = Hkv;
+  m.g = g;
+  m.num_splits = num_splits;
+  m.rows_max = g;
+  m.small_rows_limit = g;
+  m.total_q = B;
+  m.ws_o_offset = a.ws_o_offset;
+  if ((e = bw::launch_merge(m, st)) != cudaSuccess) return cuda_fail(e);
+  g_launches.fetch_add(1);
+  return BWATTN_OK;
+}
+
+size_t attn_varlen_workspace_size(int num_seqs, int max_seqlen_k, int Hq, int Hkv, int d) {
+  if (num_seqs <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || max_seqlen_k < 0) return 0;
+  return bw::splitk_ws_bytes(num_seqs * Hkv, varlen_splits(max_seqlen_k), kSmallRowsLimit, d);
+}
+
+int attn_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens_q,
+                const int32_t* cu_seqlens_k, int num_seqs, int total_q, int total_k, int max_seqlen_q,
+                int max_seqlen_k, int Hq, int Hkv, int d, int causal, float scale, void* workspace,
+                size_t workspace_bytes, void* stream) {
+  if (num_seqs < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0) return BWATTN_ERR_INVALID_ARG;
+  if (Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0 || !good_scale(scale) || (causal != 0 && causal != 1))
+    return BWATTN_ERR_INVALID_ARG;
+  if (num_seqs > 65535 || Hq > 65535) return BWATTN_ERR_INVALID_ARG;
+  const int g = Hq / Hkv;
+  if (d != 128 || g > kSmallRowsLimit) return BWATTN_ERR_UNSUPPORTED;
+  if (num_seqs == 0 || total_q == 0 || max_seqlen_q == 0) return BWATTN_OK;
+  if (!q || !o || !cu_seqlens_q || !cu_seqlens_k || !workspace || (total_k > 0 && (!k || !v)))
+    return BWATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(o) || !aligned16(workspace) || (total_k > 0 && (!aligned16(k) || !aligned16(v))) ||
+      !aligned4(cu_seqlens_q) || !aligned4(cu_seqlens_k) || (lse && !aligned4(lse)))
+    return BWATTN_ERR_INVALID_ARG;
+  const int splits = varlen_splits(max_seqlen_k);
+  const int units = num_seqs * Hkv;
+  if (workspace_bytes < bw::splitk_ws_bytes(units, splits, kSmallRowsLimit, d)) return BWATTN_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const float sl2 = scale * bw::kLog2e;
+  cudaError_t e;
+  // 1) sequences with many queries: tcgen05 prefill kernel over the packed layout
+  if (static_cast<int64_t>(max_seqlen_q) * g > kSmallRowsLimit) {
+    bw::TcFwdArgs a{};
+    // with no keys at all the K/V maps are never used; they point at q so they stay valid
+    const void* kp = total_k > 0 ? k : q;
+    const void* vp = total_k > 0 ? v : q;
+    const int hk_map = total_k > 0 ? Hkv : Hq;
+    const int tk_map = total_k > 0 ? total_k : total_q;
+    if ((e = make_map(&a.tm_q, q, d, Hq, total_q, d, static_cast<int64_t>(Hq) * d, 1, 128)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((e = make_map(&a.tm_k, kp, d, hk_map, tk_map, d, static_cast<int64_t>(hk_map) * d, 1, 128)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((e = make_map(&a.tm_v, vp, d, hk_map, tk_map, d, static_cast<int64_t>(hk_map) * d, 1, 128)) != cudaSuccess)
+      return cuda_fail(e);
+    a.o = static_cast<uint16_t*>(o);
+    a.lse = lse;
+    a.cu_q = cu_seqlens_q;
+    a.cu_k = cu_seqlens_k;
+    a.B = num_seqs;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.Nq = total_q;
+    a.Nk = total_k;
+    a.d = d;
+    a.causal = causal;
+    a.num_seqs = num_seqs;
+    a.small_rows_limit = kSmallRowsLimit;
+    a.max_pairs = (max_seqlen_q + 255) / 256;
+    a.scale_log2 = sl2;
+    a.timeout_ns = g_timeout_ns.load();
+    unsigned int* sp = nullptr;
+    if ((e = status_ptr(&sp)) != cudaSuccess) return cuda_fail(e);
+    if ((e = bw::launch_prefill_tc(a, sp, st)) != cudaSuccess) return cuda_fail(e);
+    g_launches.fetch_add(1);
+  }
+  // 2) sequences with few queries: split-K kernel with the (query, head) rows packed, then merge
+  bw::SplitKArgs s{};
+  s.q = static_cast<const uint16_t*>(q);
+  s.k = static_cast<const uint16_t*>(k);
+  s.v = static_cast<const uint16_t*>(v);
+  s.ws = static_cast<float*>(workspace);
+  s.nk = nullptr;
+  s.cu_q = cu_seqlens_q;
+  s.cu_k = cu_seqlens_k;
+  s.num_seqs = num_seqs;
+  s.Hq = Hq;
+  s.Hkv = Hkv;
+  s.g = g;
+  s.kv_seq_stride = 0;
+  s.kv_head_stride = d;
+  s.kv_key_stride = static_cast<int64_t>(Hkv) * d;
+  s.kv_cap = 0;
+  s.total_q = total_q;
+  s.total_k = total_k;
+  s.num_splits = splits;
+  s.rows_max = kSmallRowsLimit;
+  s.row_groups = kSmallRowsLimit / 16;
+  s.causal = causal;
+  s.small_rows_limit = kSmallRowsLimit;
+  s.ws_o_offset = bw::splitk_o_offset(units, splits, kSmallRowsLimit);
+  s.scale_log2 = sl2;
+  if ((e = bw::launch_splitk(s, st)) != cudaSuccess) return cuda_fail(e);
+  g_launches.fetch_add(1);
+  bw::MergeArgs m{};
+  m.ws = s.ws;
+  m.o = static_cast<uint16_t*>(o);
+  m.lse = lse;
+  m.cu_q = cu_seqlens_q;
+  m.cu_k = cu_seqlens_k;
+  m.nk = nullptr;
+  m.num_seqs = num_seqs;
+  m.Hq = Hq;
+  m.Hkv = Hkv;
+  m.g = g;
+  m.num_splits = splits;
+  m.rows_max = kSmallRowsLimit;
+  m.small_rows_limit = kSmallRowsLimit;
+  m.total_q = total_q;
+  m.ws_o_offset = s.ws_o_offset;
+  if ((e = bw::launch_merge(m, st)) != cudaSuccess) return cuda_fail(e);
+  g_launches.fetch_add(1);
+  return BWATTN_OK;
+}
+
+}  // extern "C"

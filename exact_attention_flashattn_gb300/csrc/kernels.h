@@ -1,0 +1,96 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace bw {
+
+constexpr float kLog2e = 1.4426950408889634f;
+// Bit of the device status word (owned by the C-ABI layer, passed to kernels as a pointer)
+// that records a wait some kernel gave up.
+constexpr unsigned int kStatusTimeoutBit = 1u;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// ---- fp32 FMA prefill (any B, heads, lengths; d in {64, 128}) ----
+struct Fp32FwdArgs {
+  const float* q;
+  const float* k;
+  const float* v;
+  float* o;
+  float* lse;
+  int B, Hq, Hkv, Nq, Nk, d, causal;
+  float scale_log2;  // scale * log2(e)
+};
+cudaError_t launch_prefill_fp32(const Fp32FwdArgs& a, cudaStream_t stream);
+
+// ---- split-K pass over the KV axis (decode and small-n_q varlen sequences) ----
+// A "unit" is (sequence, KV head, row group); its rows are the (query, head) pairs
+// r = i * g + hh of that sequence's queries and the group's query heads, 16 per row group.
+struct SplitKArgs {
+  const uint16_t* q;  // bf16 bits; token-major [tokens, Hq, D]
+  const uint16_t* k;  // bf16 bits
+  const uint16_t* v;
+  float* ws;          // partials: (m, l) then o, see splitk_ws_layout()
+  const int32_t* nk;  // dense decode: [B] valid keys per sequence (device)
+  const int32_t* cu_q;  // varlen: [num_seqs + 1] (device), else null
+  const int32_t* cu_k;
+  int num_seqs, Hq, Hkv, g;
+  int64_t kv_seq_stride;  // dense: elements between sequences' caches (Hkv * cap * D)
+  int64_t kv_head_stride;  // elements between KV heads at the same key (dense: cap * D, varlen: D)
+  int64_t kv_key_stride;   // elements between consecutive keys (dense: D, varlen: Hkv * D)
+  int kv_cap;         // dense: cache capacity (nk[b] is clamped to it)
+  int total_q, total_k;  // varlen: rows of the packed tensors (cu_seqlens are clamped to them)
+  int num_splits;
+  int rows_max;       // workspace rows per (sequence, KV head)
+  int row_groups;     // ceil(rows_max / 16)
+  int causal;         // varlen: causal aligned to each sequence's end
+  int small_rows_limit;  // varlen: a sequence takes this path iff n_q * g <= this
+  size_t ws_o_offset;    // splitk_o_offset(num_seqs * Hkv, num_splits, rows_max)
+  float scale_log2;
+};
+cudaError_t launch_splitk(const SplitKArgs& a, cudaStream_t stream);
+
+struct MergeArgs {
+  const float* ws;
+  uint16_t* o;  // bf16 bits, token-major [tokens, Hq, D]
+  float* lse;   // [tokens, Hq] or null
+  const int32_t* cu_q;  // varlen or null (dense: one token per sequence)
+  const int32_t* cu_k;
+  const int32_t* nk;
+  int num_seqs, Hq, Hkv, g, num_splits, rows_max, small_rows_limit;
+  int total_q;  // varlen: rows of the packed q / o (cu_seqlens_q is clamped to it)
+  size_t ws_o_offset;
+};
+cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
+
+// ---- tcgen05 prefill (bf16, d in {64, 128}) ----
+struct TcFwdArgs {
+  CUtensorMap tm_q, tm_k, tm_v;  // 3-D maps, box {64, 1 or 128, ...}, 128-byte swizzle
+  uint16_t* o;
+  float* lse;
+  const int32_t* cu_q;  // varlen (packed) mode if non-null
+  const int32_t* cu_k;
+  int B, Hq, Hkv, Nq, Nk, d, causal;  // packed mode: Nq, Nk = total rows of q and k
+  int num_seqs;
+  int small_rows_limit;  // varlen: sequences with n_q * g <= this are skipped here
+  int max_pairs;         // grid.x: pairs of 128-row query tiles per (sequence, head)
+  float scale_log2;
+  uint64_t timeout_ns;
+};
+cudaError_t launch_prefill_tc(const TcFwdArgs& a, unsigned int* status, cudaStream_t stream);
+
+// Timeout self-test: one CTA waits on a barrier that is never arrived at.
+cudaError_t launch_wait_timeout_probe(uint64_t timeout_ns, unsigned int* status, cudaStream_t stream);
+
+// Float offset of the o[] block of the split-K workspace (after the (m, l) pairs, 256-byte aligned).
+inline size_t splitk_o_offset(int units, int num_splits, int rows_max) {
+  return (static_cast<size_t>(units) * num_splits * rows_max * 2 + 63) & ~static_cast<size_t>(63);
+}
+inline size_t splitk_ws_bytes(int units, int num_splits, int rows_max, int d) {
+  return (splitk_o_offset(units, num_splits, rows_max) + static_cast<size_t>(units) * num_splits * rows_max * d) *
+         sizeof(float);
+}
+
+}  // namespace bw

@@ -1,0 +1,382 @@
+// Split-K attention over the KV axis for few query rows (single-query decode, and the
+// short-query sequences of a packed varlen batch), plus the merge of the per-split partial
+// states.
+//
+// Method ("Attention from the kernel's side", Prefill and decode are different problems;
+// "Attention kernels", Concept and Maths): the keys of one (sequence, KV head) are cut into
+// num_splits slices; each CTA folds its slice into partial states (m, l, o) with the
+// online-softmax recurrence and writes them out; a second kernel merges the partials with
+// m = max_s m_s, l = sum_s l_s e^{m_s - m}, o = sum_s o_s e^{m_s - m}, and divides.
+//
+// Layout of the work: a CTA owns one slice for up to 16 "rows", a row being one (query,
+// query head) pair of the GQA group that shares the KV head ("Attention Computation in
+// Practice", GQA in the kernel), so every K/V byte the CTA reads serves all those rows.
+// The two contractions per 16 keys are warp-level bf16 tensor-core MMAs (m16n8k16, fp32
+// accumulate): S = Q K^T with the rows as M, then O += P V with the keys as K. Cache reads
+// are 16-byte vector loads straight into registers. To make them line up with the MMA
+// fragment layout without shared memory, the head-dim index is permuted identically on Q
+// and K (a permutation of the contraction index leaves the dot product unchanged), and the
+// output-channel index of the P V product is permuted and undone at the write.
+#include <math.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace bw {
+
+namespace {
+
+constexpr int D = 128;
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kRowsPerGroup = 16;
+constexpr int kKeysPerStep = 16;
+
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t word(const uint4& v, int w) {
+  return w == 0 ? v.x : (w == 1 ? v.y : (w == 2 ? v.z : v.w));
+}
+
+// Output channel held by MMA column position p (0..7) of output n-tile nu (0..15).
+__device__ __forceinline__ int dv_of(int nu, int p) { return (nu < 8) ? (8 * p + nu) : (64 + 8 * p + (nu - 8)); }
+
+struct UnitGeom {
+  int tok0;     // first query token of the sequence
+  int nq;       // queries of the sequence
+  int nk;       // keys of the sequence
+  int64_t kv0;  // element offset of key 0 of this KV head
+  bool active;
+};
+
+__device__ __forceinline__ UnitGeom unit_geom(const SplitKArgs& a, int seq, int hkv) {
+  UnitGeom u;
+  if (a.cu_q) {
+    // lengths come from device arrays: clamp them to the packed tensors so no access leaves them
+    u.tok0 = min(max(a.cu_q[seq], 0), a.total_q);
+    u.nq = min(max(a.cu_q[seq + 1] - u.tok0, 0), a.total_q - u.tok0);
+    const int k0 = min(max(a.cu_k[seq], 0), a.total_k);
+    u.nk = min(max(a.cu_k[seq + 1] - k0, 0), a.total_k - k0);
+    u.kv0 = static_cast<int64_t>(k0) * a.kv_key_stride + static_cast<int64_t>(hkv) * a.kv_head_stride;
+    u.active = u.nq > 0 && u.nq * a.g <= a.small_rows_limit;
+  } else {
+    u.tok0 = seq;
+    u.nq = 1;
+    u.nk = min(max(a.nk[seq], 0), a.kv_cap);
+    u.kv0 = static_cast<int64_t>(seq) * a.kv_seq_stride + static_cast<int64_t>(hkv) * a.kv_head_stride;
+    u.active = true;
+  }
+  return u;
+}
+
+// Workspace: for unit (seq, hkv), split s, row r: ml[2] then o[D] are stored as
+//   ml: ws[((unit * S + s) * rows_max + r) * 2 + {0, 1}]
+//   o : ws[ws_o_offset + ((unit * S + s) * rows_max + r) * D + c]
+__device__ __forceinline__ size_t ws_ml_index(const SplitKArgs& a, int unit, int s, int r) {
+  return ((static_cast<size_t>(unit) * a.num_splits + s) * a.rows_max + r) * 2;
+}
+
+__global__ void __launch_bounds__(kThreads, 3) splitk_kernel(SplitKArgs a) {
+  const int split = blockIdx.x;
+  const int hkv = blockIdx.y % a.Hkv;
+  const int grp = blockIdx.y / a.Hkv;
+  const int seq = blockIdx.z;
+  const UnitGeom u = unit_geom(a, seq, hkv);
+  if (!u.active) return;
+  const int R = u.nq * a.g;
+  const int row0 = grp * kRowsPerGroup;
+  if (row0 >= R) return;
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t = lane & 3, gr = lane >> 2;
+
+  // Key slice of this split: whole 16-key steps.
+  const int per = (u.nk + a.num_splits - 1) / a.num_splits;
+  const int chunk = (per + kKeysPerStep - 1) / kKeysPerStep * kKeysPerStep;
+  const int kbeg = min(u.nk, split * chunk);
+  const int kend = min(u.nk, kbeg + chunk);
+
+  // Rows gr and gr + 8 of this group: (query i, head hh) and their key limits.
+  int lim[2];
+  uint32_t qa[8][4];
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    const int r = row0 + gr + 8 * rr;
+    const bool ok = r < R;
+    const int i = ok ? r / a.g : 0;
+    const int hh = ok ? r % a.g : 0;
+    lim[rr] = a.causal ? min(kend, u.nk - u.nq + i + 1) : kend;
+    if (!ok) lim[rr] = kend;
+    const uint16_t* qrow = a.q + (static_cast<int64_t>(u.tok0 + i) * a.Hq + hkv * a.g + hh) * D;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      uint4 c = make_uint4(0, 0, 0, 0);
+      if (ok) c = *reinterpret_cast<const uint4*>(qrow + 8 * (t + 4 * s));
+      // k-step 2s uses words 0,1 of chunk t+4s; k-step 2s+1 words 2,3 (same permutation as K)
+      qa[2 * s][rr] = c.x;
+      qa[2 * s][rr + 2] = c.y;
+      qa[2 * s + 1][rr] = c.z;
+      qa[2 * s + 1][rr + 2] = c.w;
+    }
+  }
+  // lowest key limit over the CTA's rows: steps ending at or below it need no mask
+  int min_lim = kend;
+  if (a.causal) min_lim = min(kend, u.nk - u.nq + row0 / a.g + 1);
+
+  float oacc[16][4];
+#pragma unroll
+  for (int nu = 0; nu < 16; ++nu) oacc[nu][0] = oacc[nu][1] = oacc[nu][2] = oacc[nu][3] = 0.f;
+  float m_run[2] = {-INFINITY, -INFINITY};
+  float l_part[2] = {0.f, 0.f};
+
+  const uint16_t* kbase = a.k + u.kv0;
+  const uint16_t* vbase = a.v + u.kv0;
+  const int64_t ks = a.kv_key_stride;
+
+  for (int kb = kbeg + warp * kKeysPerStep; kb < kend; kb += kWarps * kKeysPerStep) {
+    // ---- loads: K rows kb + nt*8 + gr (chunks t + 4s); V rows kb + {2t, 2t+1, 2t+8, 2t+9}
+    uint4 kk[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int key = kb + nt * 8 + gr;
+      const uint16_t* kr = kbase + static_cast<int64_t>(key) * ks;
+#pragma unroll
+      for (int s = 0; s < 4; ++s)
+        kk[nt][s] = (key < kend) ? ld_stream(kr + 8 * (t + 4 * s)) : make_uint4(0, 0, 0, 0);
+    }
+    uint4 va[4], vb[4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const int key = kb + 2 * t + (x & 1) + 8 * (x >> 1);
+      const uint16_t* vr = vbase + static_cast<int64_t>(key) * ks;
+      va[x] = (key < kend) ? ld_stream(vr + 8 * gr) : make_uint4(0, 0, 0, 0);
+      vb[x] = (key < kend) ? ld_stream(vr + 64 + 8 * gr) : make_uint4(0, 0, 0, 0);
+    }
+    // ---- S = Q K^T for 16 keys: two n8 tiles, 8 k16 steps over the head dim
+    float sacc[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+#pragma unroll
+      for (int kst = 0; kst < 8; ++kst) {
+        const uint4& c = kk[nt][kst >> 1];
+        const uint32_t b0 = (kst & 1) ? c.z : c.x;
+        const uint32_t b1 = (kst & 1) ? c.w : c.y;
+        mma_bf16(sacc[nt], qa[kst], b0, b1);
+      }
+    }
+    // ---- scale (log2 units), mask, row max over the quad
+    const bool need_mask = kb + kKeysPerStep > min_lim;
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int rr = c >> 1;
+        float s = sacc[nt][c] * a.scale_log2;
+        if (need_mask) {
+          const int key = kb + nt * 8 + 2 * t + (c & 1);
+          if (key >= lim[rr]) s = -INFINITY;
+        }
+        sacc[nt][c] = s;
+        mx[rr] = fmaxf(mx[rr], s);
+      }
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
+      mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
+    }
+    // ---- online-softmax update; O is rescaled only when some row's max grew
+    float mnew[2], muse[2];
+    bool grow = false;
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      mnew[rr] = fmaxf(m_run[rr], mx[rr]);
+      grow |= mnew[rr] > m_run[rr];
+      muse[rr] = (mnew[rr] == -INFINITY) ? 0.f : mnew[rr];
+    }
+    if (__any_sync(0xffffffffu, grow)) {
+      float al[2];
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        al[rr] = (m_run[rr] == -INFINITY) ? 0.f : ex2(m_run[rr] - muse[rr]);
+        l_part[rr] *= al[rr];
+      }
+#pragma unroll
+      for (int nu = 0; nu < 16; ++nu) {
+        oacc[nu][0] *= al[0];
+        oacc[nu][1] *= al[0];
+        oacc[nu][2] *= al[1];
+        oacc[nu][3] *= al[1];
+      }
+    }
+    m_run[0] = mnew[0];
+    m_run[1] = mnew[1];
+    uint32_t pa[4];
+    {
+      float p[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          p[nt][c] = ex2(sacc[nt][c] - muse[c >> 1]);
+          l_part[c >> 1] += p[nt][c];
+        }
+      // A fragment of P (rows x 16 keys): k positions 2t,2t+1 from tile 0, 2t+8,2t+9 from tile 1
+      pa[0] = pack_bf16x2(p[0][0], p[0][1]);
+      pa[1] = pack_bf16x2(p[0][2], p[0][3]);
+      pa[2] = pack_bf16x2(p[1][0], p[1][1]);
+      pa[3] = pack_bf16x2(p[1][2], p[1][3]);
+    }
+    // ---- O += P V over 16 output n-tiles
+#pragma unroll
+    for (int nu = 0; nu < 16; ++nu) {
+      const int e = nu & 7;
+      const int w = e >> 1;
+      const uint32_t sel = (e & 1) ? 0x7632u : 0x5410u;
+      const uint32_t w0 = word((nu < 8) ? va[0] : vb[0], w), w1 = word((nu < 8) ? va[1] : vb[1], w);
+      const uint32_t w2 = word((nu < 8) ? va[2] : vb[2], w), w3 = word((nu < 8) ? va[3] : vb[3], w);
+      mma_bf16(oacc[nu], pa, __byte_perm(w0, w1, sel), __byte_perm(w2, w3, sel));
+    }
+  }
+
+  // ---- combine the warps' states in shared memory, write this split's partials
+  __shared__ float sm_m[kWarps][kRowsPerGroup];
+  __shared__ float sm_l[kWarps][kRowsPerGroup];
+  __shared__ float sm_o[kWarps][kRowsPerGroup][D + 4];
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    float l = l_part[rr];
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    if (t == 0) {
+      sm_m[warp][gr + 8 * rr] = m_run[rr];
+      sm_l[warp][gr + 8 * rr] = l;
+    }
+  }
+#pragma unroll
+  for (int nu = 0; nu < 16; ++nu) {
+    sm_o[warp][gr][dv_of(nu, 2 * t)] = oacc[nu][0];
+    sm_o[warp][gr][dv_of(nu, 2 * t + 1)] = oacc[nu][1];
+    sm_o[warp][gr + 8][dv_of(nu, 2 * t)] = oacc[nu][2];
+    sm_o[warp][gr + 8][dv_of(nu, 2 * t + 1)] = oacc[nu][3];
+  }
+  __syncthreads();
+  const int unit = seq * a.Hkv + hkv;
+  const int nrows = min(kRowsPerGroup, R - row0);
+  float* ws_o = a.ws + a.ws_o_offset;
+  // thread -> (row, channel quad): 16 rows x 32 quads = 512 items, 4 per thread
+  for (int it = threadIdx.x; it < kRowsPerGroup * (D / 4); it += kThreads) {
+    const int r = it / (D / 4);
+    const int c4 = it % (D / 4);
+    if (r >= nrows) continue;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w)
+      if (sm_l[w][r] > 0.f) M = fmaxf(M, sm_m[w][r]);
+    float L = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      if (!(sm_l[w][r] > 0.f)) continue;
+      const float f = ex2(sm_m[w][r] - M);
+      L += f * sm_l[w][r];
+      o.x += f * sm_o[w][r][4 * c4 + 0];
+      o.y += f * sm_o[w][r][4 * c4 + 1];
+      o.z += f * sm_o[w][r][4 * c4 + 2];
+      o.w += f * sm_o[w][r][4 * c4 + 3];
+    }
+    const size_t mi = ws_ml_index(a, unit, split, row0 + r);
+    *reinterpret_cast<float4*>(ws_o + (mi / 2) * D + 4 * c4) = o;
+    if (c4 == 0) {
+      a.ws[mi] = (L > 0.f) ? M : -INFINITY;
+      a.ws[mi + 1] = L;
+    }
+  }
+}
+
+// One warp per output row: merge the num_splits partials of (unit, row).
+__global__ void __launch_bounds__(256) merge_kernel(MergeArgs a) {
+  const int warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int units = a.num_seqs * a.Hkv;
+  if (warp_global >= units * a.rows_max) return;
+  const int unit = warp_global / a.rows_max;
+  const int r = warp_global % a.rows_max;
+  const int seq = unit / a.Hkv, hkv = unit % a.Hkv;
+  int tok0, nq;
+  if (a.cu_q) {
+    tok0 = min(max(a.cu_q[seq], 0), a.total_q);
+    nq = min(max(a.cu_q[seq + 1] - tok0, 0), a.total_q - tok0);
+    if (nq <= 0 || nq * a.g > a.small_rows_limit) return;
+  } else {
+    tok0 = seq;
+    nq = 1;
+  }
+  if (r >= nq * a.g) return;
+  const int i = r / a.g, hh = r % a.g;
+  const int S = a.num_splits;
+  const float* ml = a.ws + (static_cast<size_t>(unit) * S * a.rows_max + r) * 2;  // split stride rows_max*2
+  const float* wo = a.ws + a.ws_o_offset + (static_cast<size_t>(unit) * S * a.rows_max + r) * D;
+  const size_t ml_stride = static_cast<size_t>(a.rows_max) * 2;
+  const size_t o_stride = static_cast<size_t>(a.rows_max) * D;
+
+  float M = -INFINITY;
+  for (int s = lane; s < S; s += 32) {
+    const float ls = ml[s * ml_stride + 1];
+    if (ls > 0.f) M = fmaxf(M, ml[s * ml_stride]);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float L = 0.f;
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < S; ++s) {
+    const float ls = ml[s * ml_stride + 1];
+    if (!(ls > 0.f)) continue;
+    const float f = ex2(ml[s * ml_stride] - M);
+    L += f * ls;
+    const float4 x = *reinterpret_cast<const float4*>(wo + s * o_stride + 4 * lane);
+    o.x += f * x.x;
+    o.y += f * x.y;
+    o.z += f * x.z;
+    o.w += f * x.w;
+  }
+  const float inv = (L > 0.f) ? 1.f / L : 0.f;
+  const int64_t orow = (static_cast<int64_t>(tok0 + i) * a.Hq + hkv * a.g + hh);
+  uint2 packed;
+  packed.x = pack_bf16x2(o.x * inv, o.y * inv);
+  packed.y = pack_bf16x2(o.z * inv, o.w * inv);
+  *reinterpret_cast<uint2*>(a.o + orow * D + 4 * lane) = packed;
+  if (a.lse && lane == 0) a.lse[orow] = (L > 0.f) ? (M + log2f(L)) * kLn2 : -INFINITY;
+}
+
+}  // namespace
+
+cudaError_t launch_splitk(const SplitKArgs& a, cudaStream_t stream) {
+  dim3 grid(a.num_splits, a.Hkv * a.row_groups, a.num_seqs);
+  splitk_kernel<<<grid, kThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
+  const long warps = static_cast<long>(a.num_seqs) * a.Hkv * a.rows_max;
+  const long blocks = (warps * 32 + 255) / 256;
+  merge_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace bw

@@ -1,0 +1,183 @@
+/*
+ * libbwattn: exact scaled-dot-product attention on one GB300 (sm_103a).
+ *
+ *   O = softmax(Q K^T * scale) V,  scale normally 1/sqrt(d)
+ *
+ * computed with the online-softmax recurrence (a running max m, running sum l and an
+ * unnormalised output o, rescaled by exp(m - m_new) tile by tile), so that the score matrix
+ * never reaches device memory. Sources, by page title and section:
+ *   - "Attention from the kernel's side: FlashAttention, online softmax and fused dequant":
+ *     "The online softmax" (the recurrence), "FlashAttention: what never touches memory"
+ *     (Q tile resident, K/V tiles streamed, O written once), "Prefill and decode are
+ *     different problems" (GQA reuse, flash-decoding split over the KV axis).
+ *   - "Attention kernels" (llm-inference-explained): "Maths" (the recurrence and the merge
+ *     rule for two partial states (m, l, o)), "Concept" (split-K decode).
+ *   - "Attention Computation in Practice": section 5, "The four attention kernels you
+ *     actually use" (prefill, decode, append/mixed with cu_seqlens, cross attention),
+ *     "GQA in the kernel" (query head h reads KV head h / (Hq / Hkv)), "Masking variants"
+ *     (causal j <= i and the skip / full / diagonal rule per block pair).
+ *
+ * Conventions shared by every call:
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller, contiguous in the layout
+ *     given, 16-byte aligned. The library never allocates, frees or synchronises.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*; NULL = the
+ *     legacy default stream) and returns a status code. Argument checks happen on the host
+ *     before any CUDA call, so a rejected call has no side effect.
+ *   - Causal masking with Nq != Nk is aligned to the end: query i sees key j iff
+ *     j <= i + (Nk - Nq). A query that sees no key gets O = 0 and LSE = -inf.
+ *   - LSE (log-sum-exp) is the natural log of sum_j exp(scale * q.k_j) over the visible keys,
+ *     written as fp32. Passing lse = NULL skips it.
+ *   - Inputs are bf16 (IEEE bfloat16) unless a dtype argument says otherwise; arithmetic is
+ *     fp32 (tensor cores with fp32 accumulation for bf16 inputs, fp32 FMA for fp32 inputs).
+ *   - The library keeps no state across calls except a device status word that records a
+ *     timed-out internal wait (see bwattn_get_status); it is thread-safe.
+ */
+#ifndef BWATTN_H
+#define BWATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---- */
+#define BWATTN_OK 0
+#define BWATTN_ERR_INVALID_ARG 1 /* null pointer, size out of range, Hq % Hkv != 0, misaligned pointer, workspace too small */
+#define BWATTN_ERR_UNSUPPORTED 2 /* valid arguments outside what the kernels implement (dtype / head dim / group size) */
+#define BWATTN_ERR_CUDA 3        /* a CUDA runtime call or kernel launch failed; see bwattn_last_cuda_error() */
+#define BWATTN_ERR_TIMEOUT 4     /* a kernel gave up an internal wait; reported by bwattn_get_status() */
+
+/* ---- dtypes ---- */
+#define BWATTN_DTYPE_FP32 0
+#define BWATTN_DTYPE_BF16 1
+
+/*
+ * attn_fwd: prefill / cross attention over dense batches.
+ * ("Attention Computation in Practice", section 5, kernel classes 1 and 4;
+ *  "Attention from the kernel's side", "FlashAttention: what never touches memory".)
+ *
+ *   q, o : [B, Hq, Nq, d]        (dtype; o has the same dtype as q)
+ *   k, v : [B, Hkv, Nk, d]       (dtype)
+ *   lse  : [B, Hq, Nq] fp32, may be NULL
+ *   causal: 0 = no mask (cross attention), 1 = causal aligned to the end
+ *   scale: multiplies q.k before the softmax; must be finite and > 0
+ *   dtype: BWATTN_DTYPE_BF16 (tcgen05 tensor-core kernel, d in {64, 128}) or
+ *          BWATTN_DTYPE_FP32 (fp32 FMA kernel, d in {64, 128})
+ * Query head h reads KV head h / (Hq / Hkv). Nq = 0 or B = 0 is a valid no-op; Nk = 0 gives
+ * O = 0 and LSE = -inf. Errors: INVALID_ARG for null / misaligned pointers, negative sizes,
+ * Hq % Hkv != 0, bad scale; UNSUPPORTED for other d or dtype.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+             int Nk, int d, int causal, float scale, int dtype, void* stream);
+
+/*
+ * attn_decode_workspace_size: bytes of caller-provided workspace attn_decode needs for the
+ * per-split partial states (m, l, o[d]) in fp32.
+ */
+size_t attn_decode_workspace_size(int B, int Hq, int d, int num_splits);
+
+/*
+ * attn_decode: single-query decode against a contiguous KV cache, split over the KV axis
+ * (flash-decoding), partial states merged with the two-state merge rule.
+ * ("Attention from the kernel's side", "Prefill and decode are different problems";
+ *  "Attention kernels", "Maths", second display; "Attention Computation in Practice",
+ *  section 5, kernel class 2 and "PagedAttention's kernel difference", contiguous form.)
+ *
+ *   q, o     : [B, Hq, d] bf16 (the one new query of each sequence)
+ *   kcache,
+ *   vcache   : [B, Hkv, nk_cap, d] bf16
+ *   nk       : [B] int32 DEVICE array, valid keys per sequence, 0 <= nk[b] <= nk_cap;
+ *              every valid key is visible (the new token's K/V are already in the cache)
+ *   num_splits: KV slices per (sequence, KV head), 1..1024; slices past nk[b] are empty
+ *   scale    : finite, > 0
+ *   lse      : [B, Hq] fp32, may be NULL
+ *   workspace: device buffer of at least attn_decode_workspace_size(B, Hq, d, num_splits)
+ *              bytes; contents on entry are ignored, on exit undefined. Must not be shared
+ *              by calls that may overlap on the GPU.
+ * The g = Hq / Hkv query heads of a group are packed against each K/V tile, so every cache
+ * byte is read once. Supported: d = 128, 1 <= g <= 32. Errors as for attn_fwd, plus
+ * INVALID_ARG when the workspace is NULL or too small.
+ */
+int attn_decode(const void* q, const void* kcache, const void* vcache, void* o, const int32_t* nk, int B, int Hq,
+                int Hkv, int nk_cap, int d, int num_splits, float scale, float* lse, void* workspace,
+                size_t workspace_bytes, void* stream);
+
+/*
+ * attn_varlen_workspace_size: bytes of workspace attn_varlen needs, from the host-side
+ * bounds it is given.
+ */
+size_t attn_varlen_workspace_size(int num_seqs, int max_seqlen_k, int Hq, int Hkv, int d);
+
+/*
+ * attn_varlen: packed batches of sequences with different lengths (append / mixed:
+ * speculative verify, chunked prefill), described by prefix sums of the lengths.
+ * ("Attention Computation in Practice", section 5, kernel class 3, "varlen kernels with
+ *  cu_seqlens".)
+ *
+ *   q, o         : [total_q, Hq, d] bf16, sequence s owns rows cu_seqlens_q[s] .. cu_seqlens_q[s+1]-1
+ *   k, v         : [total_k, Hkv, d] bf16, sequence s owns rows cu_seqlens_k[s] .. cu_seqlens_k[s+1]-1
+ *   total_q,
+ *   total_k      : host-side row counts of the packed tensors (= cu_seqlens_*[num_seqs]); they
+ *                  bound every tensor-core load, so no copy ever reads past the buffers
+ *   lse          : [total_q, Hq] fp32, may be NULL
+ *   cu_seqlens_q,
+ *   cu_seqlens_k : [num_seqs + 1] int32 DEVICE arrays, non-decreasing, [0] = 0
+ *   max_seqlen_q,
+ *   max_seqlen_k : host-side upper bounds of the per-sequence lengths (grid sizing); a
+ *                  sequence longer than its bound is not processed correctly
+ *   causal       : 1 = causal aligned to each sequence's end, 0 = none
+ *   workspace    : device buffer of at least attn_varlen_workspace_size(...) bytes
+ * Sequences whose n_q * (Hq / Hkv) <= 32 run on the split-K decode kernel (all query heads
+ * of a KV group packed in one tile); the others run on the tcgen05 prefill kernel.
+ * Supported: d = 128. Errors as for attn_decode.
+ */
+int attn_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens_q,
+                const int32_t* cu_seqlens_k, int num_seqs, int total_q, int total_k, int max_seqlen_q,
+                int max_seqlen_k, int Hq, int Hkv, int d, int causal, float scale, void* workspace,
+                size_t workspace_bytes, void* stream);
+
+/* ---- status and diagnostics ---- */
+
+/* The cudaError_t of the last failing CUDA call made by this thread inside the library (0 if none). */
+int bwattn_last_cuda_error(void);
+
+/* Short text for a status code (static storage). */
+const char* bwattn_status_string(int status);
+
+/*
+ * bwattn_get_status: synchronises `stream`, then returns BWATTN_ERR_TIMEOUT if any kernel of
+ * this library on the current device gave up an internal wait since the last
+ * bwattn_clear_status(), else BWATTN_OK (or BWATTN_ERR_CUDA if the synchronisation failed).
+ * A kernel that gives up a wait writes no further output and leaves the context usable.
+ */
+int bwattn_get_status(void* stream);
+
+/* bwattn_clear_status: resets the device status word (ordered on `stream`). */
+int bwattn_clear_status(void* stream);
+
+/*
+ * bwattn_set_wait_timeout_ns: the bound on any single internal wait of a kernel (default
+ * 2e9 ns); applies to launches made after the call, from any thread.
+ */
+void bwattn_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * bwattn_test_wait_timeout: launches a one-CTA kernel that waits on a barrier nothing ever
+ * arrives at, bounded by the current wait timeout, so a test can check that a timed-out wait
+ * returns BWATTN_ERR_TIMEOUT through bwattn_get_status() with the context still usable.
+ */
+int bwattn_test_wait_timeout(void* stream);
+
+/* Number of kernels this library has launched successfully in this process (all threads). */
+uint64_t bwattn_launch_count(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int bwattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BWATTN_H */

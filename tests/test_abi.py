@@ -1,0 +1,120 @@
+"""The C-ABI library loads, exports every symbol include/bwattn.h declares, and rejects bad
+arguments on the host before any CUDA call (so these run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_attention_flashattn_gb300 as bw
+from exact_attention_flashattn_gb300 import build as bw_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bwattn.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    bw_build.build()
+    return bw.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:[A-Za-z_][\w\s\*]*?)\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "defined")))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("attn_fwd", "attn_decode", "attn_varlen", "attn_decode_workspace_size", "attn_varlen_workspace_size",
+              "bwattn_get_status", "bwattn_clear_status", "bwattn_last_cuda_error", "bwattn_status_string",
+              "bwattn_set_wait_timeout_ns", "bwattn_test_wait_timeout", "bwattn_launch_count", "bwattn_version"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for n in declared_functions():
+        assert hasattr(L, n), n
+
+
+def test_version_and_strings(L):
+    assert L.bwattn_version() >= 100
+    assert bw.status_string(bw.OK) == "ok"
+    assert "invalid" in bw.status_string(bw.ERR_INVALID_ARG)
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation fails before any CUDA call
+
+
+def fwd(L, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, B=1, Hq=2, Hkv=1, Nq=8, Nk=8, d=128, causal=1, scale=0.1,
+             dtype=bw.DTYPE_BF16, stream=None)
+    a.update(kw)
+    return L.attn_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Hq"], a["Hkv"], a["Nq"], a["Nk"], a["d"],
+                      a["causal"], a["scale"], a["dtype"], a["stream"])
+
+
+def test_fwd_argument_errors(L):
+    assert fwd(L, q=None) == bw.ERR_INVALID_ARG
+    assert fwd(L, o=None) == bw.ERR_INVALID_ARG
+    assert fwd(L, Hq=3, Hkv=2) == bw.ERR_INVALID_ARG
+    assert fwd(L, Nq=-1) == bw.ERR_INVALID_ARG
+    assert fwd(L, scale=0.0) == bw.ERR_INVALID_ARG
+    assert fwd(L, scale=float("nan")) == bw.ERR_INVALID_ARG
+    assert fwd(L, causal=2) == bw.ERR_INVALID_ARG
+    assert fwd(L, q=FAKE + 8) == bw.ERR_INVALID_ARG  # misaligned
+    assert fwd(L, lse=FAKE + 2) == bw.ERR_INVALID_ARG
+    assert fwd(L, d=96) == bw.ERR_UNSUPPORTED
+    assert fwd(L, dtype=7) == bw.ERR_UNSUPPORTED
+    # empty work is a valid no-op that touches nothing
+    assert fwd(L, B=0, q=None, k=None, v=None, o=None) == bw.OK
+    assert fwd(L, Nq=0, q=None, k=None, v=None, o=None) == bw.OK
+
+
+def dec(L, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, nk=FAKE, B=2, Hq=8, Hkv=2, cap=64, d=128, S=4, scale=0.1, lse=None,
+             ws=FAKE, wsb=1 << 30, stream=None)
+    a.update(kw)
+    return L.attn_decode(a["q"], a["k"], a["v"], a["o"], a["nk"], a["B"], a["Hq"], a["Hkv"], a["cap"], a["d"], a["S"],
+                         a["scale"], a["lse"], a["ws"], a["wsb"], a["stream"])
+
+
+def test_decode_argument_errors(L):
+    need = L.attn_decode_workspace_size(2, 8, 128, 4)
+    assert need >= 2 * 8 * 4 * 130 * 4
+    assert dec(L, nk=None) == bw.ERR_INVALID_ARG
+    assert dec(L, ws=None) == bw.ERR_INVALID_ARG
+    assert dec(L, wsb=need - 1) == bw.ERR_INVALID_ARG
+    assert dec(L, S=0) == bw.ERR_INVALID_ARG
+    assert dec(L, S=1025) == bw.ERR_INVALID_ARG
+    assert dec(L, Hq=8, Hkv=3) == bw.ERR_INVALID_ARG
+    assert dec(L, d=64) == bw.ERR_UNSUPPORTED
+    assert dec(L, Hq=66, Hkv=1) == bw.ERR_UNSUPPORTED
+    assert dec(L, nk=FAKE + 2) == bw.ERR_INVALID_ARG
+    assert dec(L, B=0, q=None) == bw.OK
+
+
+def test_varlen_argument_errors(L):
+    def var(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, cq=FAKE, ck=FAKE, n=3, tq=10, tk=30, mq=8, mk=16, Hq=8,
+                 Hkv=2, d=128, causal=1, scale=0.1, ws=FAKE, wsb=1 << 30, stream=None)
+        a.update(kw)
+        return L.attn_varlen(a["q"], a["k"], a["v"], a["o"], a["lse"], a["cq"], a["ck"], a["n"], a["tq"], a["tk"],
+                             a["mq"], a["mk"], a["Hq"], a["Hkv"], a["d"], a["causal"], a["scale"], a["ws"], a["wsb"],
+                             a["stream"])
+    assert var(cq=None) == bw.ERR_INVALID_ARG
+    assert var(ws=None) == bw.ERR_INVALID_ARG
+    assert var(wsb=16) == bw.ERR_INVALID_ARG
+    assert var(Hq=8, Hkv=3) == bw.ERR_INVALID_ARG
+    assert var(d=64) == bw.ERR_UNSUPPORTED
+    assert var(n=0) == bw.OK
+    assert L.attn_varlen_workspace_size(3, 16, 8, 2, 128) > 0
+
+
+def test_python_binding_rejects_host_tensors():
+    import torch
+    q = torch.zeros(1, 1, 8, 64)
+    with pytest.raises(ValueError):
+        bw.attn_fwd(q, q, q)

@@ -1,0 +1,263 @@
+"""GPU parity: every call of the C-ABI library against the fp64 oracle on the same seeded inputs.
+
+Tolerances (written here, applied element by element):
+* fp32 inputs (fp32 FMA kernel): max |O_gpu - O_oracle| <= 1e-4;
+* bf16 inputs (tensor cores, fp32 accumulation, the oracle fed the same bf16 values): max abs
+  error <= 2e-2 and mean abs error <= 2e-3; LSE max abs error <= 2e-3;
+* masking is bit-exact: K/V at masked positions set to large finite values leave every output
+  bit unchanged.
+Small cases span several tiles and a ragged tail; the workloads' full sizes run in the same
+launch configuration as the benchmark and are checked on sampled rows the oracle computes one
+by one.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_flashattn_gb300 as bw
+import oracle
+from exact_attention_flashattn_gb300 import build as bw_build
+from exact_attention_flashattn_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16_MAX, TOL_BF16_MEAN, TOL_LSE = 2e-2, 2e-3, 2e-3
+TOL_FP32_MAX = 1e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    bw_build.build()
+    bw.lib()
+    torch.cuda.init()
+    yield
+
+
+def f64(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def check_bf16(o_gpu, o_ref, lse_gpu=None, lse_ref=None, what=""):
+    err = np.abs(f64(o_gpu) - o_ref)
+    assert np.all(np.isfinite(err)), what
+    assert err.max() <= TOL_BF16_MAX, (what, err.max())
+    assert err.mean() <= TOL_BF16_MEAN, (what, err.mean())
+    if lse_gpu is not None:
+        lg, lr = f64(lse_gpu), lse_ref
+        same_inf = np.isneginf(lg) == np.isneginf(lr)
+        assert np.all(same_inf), what
+        fin = np.isfinite(lr)
+        if fin.any():
+            assert np.abs(lg[fin] - lr[fin]).max() <= TOL_LSE, (what, np.abs(lg[fin] - lr[fin]).max())
+
+
+# ------------------------------------------------------------------ fp32 prefill
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d,causal", [
+    (1, 1, 1, 512, 512, 64, True),     # the single-head workload
+    (2, 4, 2, 200, 333, 64, True),     # ragged, GQA, bottom-right causal
+    (1, 2, 1, 77, 500, 128, False),    # cross attention, d = 128
+    (1, 1, 1, 130, 60, 128, True),     # more queries than keys: leading rows see nothing
+])
+def test_fp32_prefill(B, Hq, Hkv, Nq, Nk, d, causal):
+    q, k, v = wl.prefill_inputs(B, Hq, Hkv, Nq, Nk, d, torch.float32, seed=7 + Nq)
+    o_ref, lse_ref = oracle.attention(f64(q), f64(k), f64(v), causal, method="tiled", block=128)
+    o, lse = bw.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal)
+    torch.cuda.synchronize()
+    err = np.abs(f64(o) - o_ref)
+    assert err.max() <= TOL_FP32_MAX, err.max()
+    lg = f64(lse)
+    assert np.all(np.isneginf(lg) == np.isneginf(lse_ref))
+    fin = np.isfinite(lse_ref)
+    assert np.abs(lg[fin] - lse_ref[fin]).max() <= TOL_FP32_MAX
+
+
+def test_single_head_workload_fp32():
+    x = wl.make("single_head_fp32_512x64")
+    w = x["w"]
+    o_ref, _ = oracle.attention(f64(x["q"]), f64(x["k"]), f64(x["v"]), True, scale=1.0 / 8, method="tiled",
+                                block=w.extra["key_tile"])
+    o, _ = bw.attn_fwd(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), causal=True, scale=1.0 / 8)
+    torch.cuda.synchronize()
+    assert np.abs(f64(o) - o_ref).max() <= TOL_FP32_MAX
+
+
+# ------------------------------------------------------------------ bf16 tensor-core prefill
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d,causal", [
+    (1, 1, 1, 128, 128, 128, True),    # one tile
+    (2, 4, 2, 640, 640, 128, True),    # 5 query tiles (3 CTA pairs), GQA
+    (1, 2, 2, 300, 700, 128, False),   # ragged cross attention
+    (1, 2, 1, 333, 1000, 128, True),   # ragged, bottom-right causal
+    (1, 2, 2, 200, 90, 128, True),     # more queries than keys
+    (2, 2, 1, 384, 384, 64, True),     # head dim 64
+    (1, 1, 1, 1, 1, 128, True),        # one query, one key
+])
+def test_bf16_prefill(B, Hq, Hkv, Nq, Nk, d, causal):
+    q, k, v = wl.prefill_inputs(B, Hq, Hkv, Nq, Nk, d, torch.bfloat16, seed=11 + Nq + Nk)
+    o_ref, lse_ref = oracle.attention(f64(q), f64(k), f64(v), causal, method="tiled", block=128)
+    o, lse = bw.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal)
+    torch.cuda.synchronize()
+    check_bf16(o, o_ref, lse, lse_ref, what=(B, Hq, Hkv, Nq, Nk, d, causal))
+
+
+def test_bf16_prefill_no_keys():
+    q, k, v = wl.prefill_inputs(1, 2, 2, 64, 0, 128, torch.bfloat16, seed=5)
+    o, lse = bw.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=False)
+    torch.cuda.synchronize()
+    assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
+
+
+def test_bf16_prefill_mask_is_exact_and_deterministic():
+    # rows i < 256 never see keys j >= 256: large finite K/V there must not change one bit
+    q, k, v = wl.prefill_inputs(1, 2, 2, 512, 512, 128, torch.bfloat16, seed=21)
+    q, k, v = q.cuda(), k.cuda(), v.cuda()
+    o1, l1 = bw.attn_fwd(q, k, v, causal=True)
+    o2, l2 = bw.attn_fwd(q, k, v, causal=True)
+    k2, v2 = k.clone(), v.clone()
+    k2[:, :, 256:] = 3.0e4
+    v2[:, :, 256:] = -3.0e4
+    o3, l3 = bw.attn_fwd(q, k2, v2, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert torch.equal(o1[:, :, :256], o3[:, :, :256]) and torch.equal(l1[:, :, :256], l3[:, :, :256])
+
+
+def test_prefill_workload_full_size_sampled_rows():
+    x = wl.make("prefill_causal_b4_h32_n4096_d128", device="cuda")
+    w = x["w"]
+    o, lse = bw.attn_fwd(x["q"], x["k"], x["v"], causal=True)
+    torch.cuda.synchronize()
+    g = torch.Generator().manual_seed(99)
+    rows = [(0, 0, 0), (w.B - 1, w.Hq - 1, w.Nq - 1), (1, 5, 127), (2, 9, 128), (3, 31, 4095)]
+    rows += [(int(torch.randint(0, w.B, (1,), generator=g)), int(torch.randint(0, w.Hq, (1,), generator=g)),
+              int(torch.randint(0, w.Nq, (1,), generator=g))) for _ in range(40)]
+    errs = []
+    for b, h, i in rows:
+        qi = f64(x["q"][b, h, i])[None, None, None]
+        ki = f64(x["k"][b, h, :i + 1])[None, None]
+        vi = f64(x["v"][b, h, :i + 1])[None, None]
+        o_ref, lse_ref = oracle.attention(qi, ki, vi, False, method="naive")
+        e = np.abs(f64(o[b, h, i]) - o_ref[0, 0, 0])
+        errs.append(e)
+        assert e.max() <= TOL_BF16_MAX, (b, h, i, e.max())
+        assert abs(float(lse[b, h, i]) - lse_ref[0, 0, 0]) <= TOL_LSE
+    assert np.mean(np.concatenate(errs)) <= TOL_BF16_MEAN
+    # every row is finite
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+
+
+# ------------------------------------------------------------------ split-K decode + merge
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,cap,nk,S", [
+    (3, 8, 2, 300, [300, 17, 0], 4),     # g = 4, ragged lengths, an empty sequence
+    (2, 8, 8, 1000, [1000, 999], 7),     # g = 1
+    (1, 16, 2, 513, [513], 64),          # g = 8, splits with fewer than 16 keys, empty splits
+    (2, 16, 1, 400, [400, 250], 3),      # g = 16
+    (1, 32, 1, 200, [200], 1),           # g = 32: two row groups, one split
+])
+def test_decode(B, Hq, Hkv, cap, nk, S):
+    q, kc, vc, nkt = wl.decode_inputs(B, Hq, Hkv, cap, 128, torch.bfloat16, seed=31 + cap, nk=nk)
+    o_ref, lse_ref = oracle.decode(f64(q), f64(kc), f64(vc), nkt.numpy(), method="splitk", workers=S)
+    o, lse = bw.attn_decode(q.cuda(), kc.cuda(), vc.cuda(), nkt.cuda(), num_splits=S)
+    torch.cuda.synchronize()
+    check_bf16(o, o_ref, lse, lse_ref, what=(B, Hq, Hkv, cap, nk, S))
+
+
+def test_decode_ignores_cache_tail_exactly():
+    q, kc, vc, nkt = wl.decode_inputs(2, 8, 2, 700, 128, torch.bfloat16, seed=41, nk=[650, 333])
+    q, kc, vc, nkt = q.cuda(), kc.cuda(), vc.cuda(), nkt.cuda()
+    o1, l1 = bw.attn_decode(q, kc, vc, nkt, num_splits=5)
+    kc2, vc2 = kc.clone(), vc.clone()
+    kc2[0, :, 650:] = 3.0e4
+    vc2[0, :, 650:] = float("nan")  # never read: outside the valid length
+    kc2[1, :, 333:] = float("inf")
+    o2, l2 = bw.attn_decode(q, kc2, vc2, nkt, num_splits=5)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("name", ["decode_gqa_b8_h32x8_n32768_d128", "decode_long_b1_h64x8_n262144_d128"])
+def test_decode_workloads_full_size(name):
+    x = wl.make(name, device="cuda")
+    w = x["w"]
+    o, lse = bw.attn_decode(x["q"], x["kcache"], x["vcache"], x["nk"].cuda(), num_splits=w.num_splits)
+    torch.cuda.synchronize()
+    # the oracle takes every query head of up to two sequences
+    for b in sorted({0, w.B - 1}):
+        o_ref, lse_ref = oracle.decode(f64(x["q"][b:b + 1]), f64(x["kcache"][b:b + 1]), f64(x["vcache"][b:b + 1]),
+                                       [w.Nk], method="splitk", workers=w.num_splits)
+        check_bf16(o[b:b + 1], o_ref, lse[b:b + 1], lse_ref, what=(name, b))
+
+
+# ------------------------------------------------------------------ varlen
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_varlen_small(causal):
+    nq = [1, 4, 8, 200, 300, 3, 129]
+    nk = [50, 700, 8, 200, 1000, 2100, 129]
+    q, k, v, cq, ck = wl.varlen_inputs(nq, nk, 8, 2, 128, torch.bfloat16, seed=51)
+    o_ref, lse_ref = oracle.varlen(f64(q), f64(k), f64(v), cq.numpy(), ck.numpy(), causal, method="tiled", block=128)
+    o, lse = bw.attn_varlen(q.cuda(), k.cuda(), v.cuda(), cq.cuda(), ck.cuda(), max(nq), max(nk), causal=causal)
+    torch.cuda.synchronize()
+    check_bf16(o, o_ref, lse, lse_ref, what=("varlen", causal))
+
+
+def test_varlen_workload_full_size_sampled_rows():
+    x = wl.make("varlen_append_64seq_h32x8_d128", device="cuda")
+    w = x["w"]
+    nq, nk = x["nq"], x["nk"]
+    cq, ck = x["cu_q"].tolist(), x["cu_k"].tolist()
+    o, lse = bw.attn_varlen(x["q"], x["k"], x["v"], x["cu_q"].cuda(), x["cu_k"].cuda(), max(nq), max(nk), causal=True)
+    torch.cuda.synchronize()
+    g = w.Hq // w.Hkv
+    errs = []
+    for s in range(w.num_seqs):
+        for i in sorted({0, nq[s] - 1, nq[s] // 2}):
+            for h in (0, 13, w.Hq - 1):
+                vis = nk[s] - nq[s] + i + 1
+                qi = f64(x["q"][cq[s] + i, h])[None, None, None]
+                ki = f64(x["k"][ck[s]:ck[s] + vis, h // g])[None, None]
+                vi = f64(x["v"][ck[s]:ck[s] + vis, h // g])[None, None]
+                o_ref, lse_ref = oracle.attention(qi, ki, vi, False, method="naive")
+                e = np.abs(f64(o[cq[s] + i, h]) - o_ref[0, 0, 0])
+                errs.append(e)
+                assert e.max() <= TOL_BF16_MAX, (s, i, h, e.max())
+                assert abs(float(lse[cq[s] + i, h]) - lse_ref[0, 0, 0]) <= TOL_LSE
+    assert np.mean(np.concatenate(errs)) <= TOL_BF16_MEAN
+    assert torch.isfinite(o).all()
+
+
+# ------------------------------------------------------------------ status and failure detection
+
+
+def test_timed_out_wait_is_reported_and_context_survives():
+    bw.clear_status()
+    assert bw.get_status() == bw.OK
+    bw.set_wait_timeout_ns(50_000_000)  # 50 ms
+    try:
+        bw.test_wait_timeout()
+        assert bw.get_status() == bw.ERR_TIMEOUT
+    finally:
+        bw.set_wait_timeout_ns(2_000_000_000)
+    bw.clear_status()
+    assert bw.get_status() == bw.OK
+    # the context is still usable: a normal call runs and reports no timeout
+    q, k, v = wl.prefill_inputs(1, 1, 1, 128, 128, 128, torch.bfloat16, seed=3)
+    o, _ = bw.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True)
+    assert bw.get_status() == bw.OK
+    assert torch.isfinite(o).all()
+
+
+def test_launch_count_counts_kernels():
+    n0 = bw.launch_count()
+    q, kc, vc, nkt = wl.decode_inputs(1, 8, 2, 64, 128, torch.bfloat16, seed=2)
+    bw.attn_decode(q.cuda(), kc.cuda(), vc.cuda(), nkt.cuda(), num_splits=2)
+    torch.cuda.synchronize()
+    assert bw.launch_count() - n0 == 2  # split-K pass + merge
