@@ -38,8 +38,28 @@ from exact_attention_flashattn_gb300 import roofline as rl  # noqa: E402
 from exact_attention_flashattn_gb300 import workloads as wl  # noqa: E402
 
 HEADLINE = "prefill_causal_b4_h32_n4096_d128"
+
+# DRAM traffic of the dominant kernel from the committed ncu capture, per full launch, valid
+# only while the kernel source is the profiled one (checked by hash); otherwise reported null.
+PROFILED_TRAFFIC = {
+    "kernel_source": "exact_attention_flashattn_gb300/csrc/prefill_tc.cu",
+    "sha256": "4732e02d949746ed129f5d7ca189ef60539cdbddad31cea747c2eb728b076977",
+    # (201.78 MB read + 54.04 MB written) at B=2 (profiles/prefill_tc_b2_h32_n4096_d128.md),
+    # scaled x2 to the B=4 launch: traffic grows with the number of (batch, head) units
+    "bytes_per_launch": 511645184,
+}
 METRIC = "prefill TFLOP/s and decode KV GB/s, 1×GB300, as fraction of roofline"
 L2_BYTES = 129 * 1024 * 1024
+
+
+def profiled_traffic():
+    import hashlib
+    p = os.path.join(ROOT, PROFILED_TRAFFIC["kernel_source"])
+    if PROFILED_TRAFFIC["sha256"] is None or not os.path.exists(p):
+        return None
+    with open(p, "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()
+    return PROFILED_TRAFFIC["bytes_per_launch"] if digest == PROFILED_TRAFFIC["sha256"] else None
 
 
 def load_peaks():
@@ -102,7 +122,7 @@ class ClockSampler:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except Exception:
@@ -166,16 +186,16 @@ def time_steps(fn, steps, warmup, world, stream):
     return per, launches
 
 
-def cpu_baseline_prefill(seconds_budget=12.0):
+def cpu_baseline_prefill(seconds_budget=15.0):
     """fp64 oracle on whole heads of the headline workload (bounded: ~10-30 s of CPU work)."""
     import numpy as np
     import oracle
     w = wl.WORKLOADS[HEADLINE]
-    q, k, v = wl.prefill_inputs(1, 2, 2, w.Nq, w.Nk, w.d, torch.bfloat16, seed=w.seed)
+    q, k, v = wl.prefill_inputs(1, 4, 4, w.Nq, w.Nk, w.d, torch.bfloat16, seed=w.seed)
     qs, ks, vs = (x.float().numpy().astype(np.float64) for x in (q, k, v))
     heads, t = 0, 0.0
-    while t < seconds_budget and heads < 8:
-        h = heads % 2
+    while t < seconds_budget and heads < w.B * w.Hq:
+        h = heads % 4
         t0 = time.perf_counter()
         oracle.attention(qs[:, h:h + 1], ks[:, h:h + 1], vs[:, h:h + 1], True, method="tiled", block=128)
         t += time.perf_counter() - t0
@@ -220,17 +240,65 @@ def run_reference(args, rank, world):
     print(json.dumps(line))
 
 
+# ------------------------------------------------------------------ single-part runs (profiling aid)
+
+
+def run_case(args, world, stream, dev, peaks):
+    out = {"case": args.case}
+    if args.case == "prefill":
+        w = wl.WORKLOADS[HEADLINE]
+        B = args.batch or w.B
+        q, k, v = wl.prefill_inputs(B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, torch.bfloat16, w.seed, device=dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, w.Hq, w.Nq), dtype=torch.float32, device=dev)
+        per, n = time_steps(lambda: bw.attn_fwd(q, k, v, causal=True, out=o, lse=lse), args.steps, args.warmup,
+                            world, stream)
+        ms = statistics.mean(per)
+        out.update({"B": B, "ms": ms, "tflops": rl.prefill_flops(B, w.Hq, w.Nq, w.Nk, w.d, True) / ms / 1e9,
+                    "launches": n})
+    elif args.case == "decode":
+        for name in ("decode_gqa_b8_h32x8_n32768_d128", "decode_long_b1_h64x8_n262144_d128"):
+            x = wl.make(name, device=dev)
+            wd = x["w"]
+            nk = x["nk"].to(dev)
+            ws = torch.empty(bw.decode_workspace_size(wd.B, wd.Hq, wd.d, wd.num_splits), dtype=torch.uint8,
+                             device=dev)
+            per, n = time_steps(lambda: bw.attn_decode(x["q"], x["kcache"], x["vcache"], nk, wd.num_splits,
+                                                       workspace=ws), args.steps, args.warmup, world, stream)
+            ms = statistics.mean(per)
+            out[name] = {"ms": ms, "GB/s": rl.decode_kv_bytes([wd.Nk] * wd.B, wd.Hkv, wd.d) / ms / 1e6,
+                         "launches": n}
+            del x, ws
+            torch.cuda.empty_cache()
+    else:
+        x = wl.make("varlen_append_64seq_h32x8_d128", device=dev)
+        cq, ck = x["cu_q"].to(dev), x["cu_k"].to(dev)
+        mq, mk = max(x["nq"]), max(x["nk"])
+        wv = x["w"]
+        ws = torch.empty(bw.varlen_workspace_size(wv.num_seqs, mk, wv.Hq, wv.Hkv, wv.d), dtype=torch.uint8,
+                         device=dev)
+        per, n = time_steps(lambda: bw.attn_varlen(x["q"], x["k"], x["v"], cq, ck, mq, mk, causal=True,
+                                                   workspace=ws), args.steps, args.warmup, world, stream)
+        ms = statistics.mean(per)
+        out.update({"ms": ms, "tflops": rl.varlen_flops(x["nq"], x["nk"], wv.Hq, wv.d, True) / ms / 1e9,
+                    "launches": n})
+    print(json.dumps(out))
+
+
 # ------------------------------------------------------------------ main arm
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="own", choices=["own", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-breakdown", action="store_true")
+    ap.add_argument("--case", default="all", choices=["all", "prefill", "decode", "varlen"],
+                    help="profiling aid: run one part only (no e2e, no CPU baseline)")
+    ap.add_argument("--batch", type=int, default=0, help="profiling aid: override the prefill batch size")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -244,6 +312,10 @@ def main():
     peaks = load_peaks()
     stream = torch.cuda.current_stream()
     dev = torch.device("cuda", torch.cuda.current_device())
+
+    if args.case != "all":
+        run_case(args, world, stream, dev, peaks)
+        return
 
     # ---------------- headline: causal prefill
     x = wl.make(HEADLINE, device=dev)
@@ -347,7 +419,7 @@ def main():
                        "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB of Q/K/V per step), no flush",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                         "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                         "frac": achieved / peaks["bf16_tflops"], "traffic": profiled_traffic(),
                          "peak_source": f"{peaks['source']} bf16 burst"},
             "e2e": e2e, "gpu_launches": launches, "clocks": clocks, "cpu_baseline": cpu, "breakdown": breakdown,
         }
