@@ -100,6 +100,11 @@ int varlen_splits(int max_seqlen_k) {
 
 }  // namespace
 
+namespace bw {
+void record_cuda_error(cudaError_t e) { t_last_cuda_error = static_cast<int>(e); }
+void count_launch() { g_launches.fetch_add(1); }
+}  // namespace bw
+
 extern "C" {
 
 int bwattn_version(void) { return 100; }

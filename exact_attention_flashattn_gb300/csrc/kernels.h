@@ -84,6 +84,11 @@ cudaError_t launch_prefill_tc(const TcFwdArgs& a, unsigned int* status, cudaStre
 // Timeout self-test: one CTA waits on a barrier that is never arrived at.
 cudaError_t launch_wait_timeout_probe(uint64_t timeout_ns, unsigned int* status, cudaStream_t stream);
 
+// Bookkeeping shared by every entry point (defined in api.cu): record a failed CUDA call for
+// bwattn_last_cuda_error(), count a successful launch for bwattn_launch_count().
+void record_cuda_error(cudaError_t e);
+void count_launch();
+
 // Float offset of the o[] block of the split-K workspace (after the (m, l) pairs, 256-byte aligned).
 inline size_t splitk_o_offset(int units, int num_splits, int rows_max) {
   return (static_cast<size_t>(units) * num_splits * rows_max * 2 + 63) & ~static_cast<size_t>(63);

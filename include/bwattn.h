@@ -105,6 +105,32 @@ int attn_decode(const void* q, const void* kcache, const void* vcache, void* o, 
                 size_t workspace_bytes, void* stream);
 
 /*
+ * attn_decode_static: the same single-query split-K decode as attn_decode, for callers that
+ * cannot allocate device memory. The pages have no counterpart to this entry point; it exists
+ * for deployment. Some callers cannot call cudaMalloc or hand the library a workspace: a
+ * plugin or inference-engine host that gives a kernel only its input and output buffers, code
+ * whose device memory is entirely owned by another allocator, or a latency-critical loop that
+ * cannot afford cudaMalloc's implicit device-wide synchronisation. This call takes the same
+ * arguments as attn_decode minus the workspace, and keeps its per-split partial states in a
+ * fixed array of BWATTN_DECODE_STATIC_SCRATCH_BYTES inside the library, which every GPU that
+ * loads the library holds until the process exits. It allocates nothing.
+ *   - Limit: the partials must fit the array, i.e.
+ *     attn_decode_workspace_size(B, Hq, d, num_splits) <= BWATTN_DECODE_STATIC_SCRATCH_BYTES
+ *     (about B * Hq * num_splits <= 16,000 at d = 128); larger calls return
+ *     BWATTN_ERR_UNSUPPORTED without launching anything.
+ *   - The first call on each device looks up the array's device address (once per device,
+ *     with that device current); make that first call before any stream capture.
+ *   - Every call on a device shares the one array, and the array keeps the last call's
+ *     contents. Nothing in it needs to start at zero (each call writes every partial it later
+ *     reads), but calls that overlap on the GPU (other streams, other host threads) race on it:
+ *     order them, e.g. on one stream.
+ * Errors otherwise as for attn_decode.
+ */
+#define BWATTN_DECODE_STATIC_SCRATCH_BYTES (8u * 1024u * 1024u)
+int attn_decode_static(const void* q, const void* kcache, const void* vcache, void* o, const int32_t* nk, int B,
+                       int Hq, int Hkv, int nk_cap, int d, int num_splits, float scale, float* lse, void* stream);
+
+/*
  * attn_varlen_workspace_size: bytes of workspace attn_varlen needs, from the host-side
  * bounds it is given.
  */

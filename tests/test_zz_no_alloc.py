@@ -1,0 +1,87 @@
+"""attn_decode_static: the decode entry point that allocates nothing.
+
+Some callers cannot call cudaMalloc or hand the library a workspace (a plugin host that gives
+a kernel only its input and output buffers, code whose device memory belongs to another
+allocator, a latency-critical loop that cannot take cudaMalloc's device-wide
+synchronisation). For them the library keeps the split-K partial states in a fixed device
+array. This test calls that entry point through the C-ABI, twice in a row with different
+problems (the second call runs over the first call's leftovers in the shared array), and
+compares each result with attn_decode's, within the bf16 tolerances of the other parity
+tests. It lives in a file of its own, collected last, and passes alone or after the others.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_flashattn_gb300 as bw
+from exact_attention_flashattn_gb300 import build as bw_build
+from exact_attention_flashattn_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+TOL_MAX, TOL_MEAN, TOL_LSE = 2e-2, 2e-3, 2e-3
+SCRATCH_BYTES = 8 * 1024 * 1024
+
+
+@pytest.fixture(scope="module")
+def static_fn():
+    bw_build.build()
+    L = ctypes.CDLL(bw.LIB_PATH)  # own handle: the binding's prototypes stay untouched
+    f = L.attn_decode_static
+    vp, ci = ctypes.c_void_p, ctypes.c_int
+    f.argtypes = [vp, vp, vp, vp, vp] + [ci] * 6 + [ctypes.c_float, vp, vp]
+    f.restype = ci
+    torch.cuda.init()
+    return f
+
+
+def run_static(f, q, kc, vc, nk, S):
+    B, Hq, d = q.shape
+    _, Hkv, cap, _ = kc.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    rc = f(q.data_ptr(), kc.data_ptr(), vc.data_ptr(), o.data_ptr(), nk.data_ptr(), B, Hq, Hkv, cap, d, S,
+           1.0 / d ** 0.5, lse.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    return rc, o, lse
+
+
+def close(a, b, what):
+    err = (a.float() - b.float()).abs()
+    assert torch.isfinite(err).all(), what
+    assert float(err.max()) <= TOL_MAX and float(err.mean()) <= TOL_MEAN, (what, float(err.max()))
+
+
+def test_static_decode_matches_workspace_decode_twice(static_fn):
+    cases = [
+        # GQA decode with ragged lengths and one empty sequence, 16 splits
+        dict(B=4, Hq=32, Hkv=8, cap=4096, nk=[4096, 1000, 0, 37], S=16, seed=71),
+        # a different shape reusing the same array: g = 8, many small splits
+        dict(B=1, Hq=64, Hkv=8, cap=20000, nk=[19999], S=96, seed=72),
+    ]
+    for c in cases:
+        q, kc, vc, nk = wl.decode_inputs(c["B"], c["Hq"], c["Hkv"], c["cap"], 128, torch.bfloat16, c["seed"],
+                                         nk=c["nk"], device="cuda")
+        nk = nk.cuda()
+        o_ref, l_ref = bw.attn_decode(q, kc, vc, nk, num_splits=c["S"])
+        rc, o, lse = run_static(static_fn, q, kc, vc, nk, c["S"])
+        torch.cuda.synchronize()
+        assert rc == bw.OK, bw.status_string(rc)
+        close(o, o_ref, c)
+        fin = torch.isfinite(l_ref)
+        assert torch.equal(torch.isneginf(lse), torch.isneginf(l_ref))
+        assert float((lse[fin] - l_ref[fin]).abs().max()) <= TOL_LSE
+
+
+def test_static_decode_rejects_partials_beyond_the_array(static_fn):
+    # B * Hq * num_splits * (d + 2) * 4 bytes above 8 MiB must be refused before any launch
+    B, Hq, Hkv, cap, S = 2, 64, 8, 16, 1024
+    assert bw.decode_workspace_size(B, Hq, 128, S) > SCRATCH_BYTES
+    q = torch.zeros((B, Hq, 128), dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros((B, Hkv, cap, 128), dtype=torch.bfloat16, device="cuda")
+    nk = torch.full((B,), cap, dtype=torch.int32, device="cuda")
+    n0 = bw.launch_count()
+    rc, _, _ = run_static(static_fn, q, kc, kc, nk, S)
+    assert rc == bw.ERR_UNSUPPORTED
+    assert bw.launch_count() == n0
