@@ -15,6 +15,13 @@ namespace {
 
 __device__ unsigned int g_status_word;
 
+// Item counters of the persistent prefill kernel: one pair per launch, taken round-robin from
+// this ring, so launches in flight on different streams never share a pair; a launch leaves
+// its pair zeroed when it completes.
+constexpr int kSchedSlots = 4096;
+__device__ unsigned int g_sched_counters[2 * kSchedSlots];
+std::atomic<uint32_t> g_sched_next{0};
+
 thread_local int t_last_cuda_error = 0;
 std::atomic<uint64_t> g_launches{0};
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
@@ -22,6 +29,7 @@ std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 unsigned int* g_status_ptr[kMaxDevices] = {};
+unsigned int* g_sched_ptr[kMaxDevices] = {};
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -47,6 +55,27 @@ cudaError_t status_ptr(unsigned int** out) {
     g_status_ptr[dev] = static_cast<unsigned int*>(p);
   }
   *out = g_status_ptr[dev];
+  return cudaSuccess;
+}
+
+// A fresh pair of item counters on the current device for one launch of the prefill kernel.
+cudaError_t sched_ptr(unsigned int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  unsigned int* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_sched_ptr[dev]) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_sched_counters);
+      if (e != cudaSuccess) return e;
+      g_sched_ptr[dev] = static_cast<unsigned int*>(p);
+    }
+    base = g_sched_ptr[dev];
+  }
+  *out = base + 2 * (g_sched_next.fetch_add(1) % kSchedSlots);
   return cudaSuccess;
 }
 
@@ -213,8 +242,10 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   a.scale_log2 = sl2;
   a.timeout_ns = g_timeout_ns.load();
   unsigned int* sp = nullptr;
+  unsigned int* sc = nullptr;
   if ((e = status_ptr(&sp)) != cudaSuccess) return cuda_fail(e);
-  if ((e = bw::launch_prefill_tc(a, sp, st)) != cudaSuccess) return cuda_fail(e);
+  if ((e = sched_ptr(&sc)) != cudaSuccess) return cuda_fail(e);
+  if ((e = bw::launch_prefill_tc(a, sp, sc, st)) != cudaSuccess) return cuda_fail(e);
   g_launches.fetch_add(1);
   return BWATTN_OK;
 }
@@ -347,8 +378,10 @@ int attn_varlen(const void* q, const void* k, const void* v, void* o, float* lse
     a.scale_log2 = sl2;
     a.timeout_ns = g_timeout_ns.load();
     unsigned int* sp = nullptr;
+    unsigned int* sc = nullptr;
     if ((e = status_ptr(&sp)) != cudaSuccess) return cuda_fail(e);
-    if ((e = bw::launch_prefill_tc(a, sp, st)) != cudaSuccess) return cuda_fail(e);
+    if ((e = sched_ptr(&sc)) != cudaSuccess) return cuda_fail(e);
+    if ((e = bw::launch_prefill_tc(a, sp, sc, st)) != cudaSuccess) return cuda_fail(e);
     g_launches.fetch_add(1);
   }
   // 2) sequences with few queries: split-K kernel with the (query, head) rows packed, then merge

@@ -79,7 +79,9 @@ struct TcFwdArgs {
   float scale_log2;
   uint64_t timeout_ns;
 };
-cudaError_t launch_prefill_tc(const TcFwdArgs& a, unsigned int* status, cudaStream_t stream);
+// `sched`: two zeroed device counters (next item, CTAs finished) owned by this launch alone;
+// the kernel leaves them zeroed again when it completes.
+cudaError_t launch_prefill_tc(const TcFwdArgs& a, unsigned int* status, unsigned int* sched, cudaStream_t stream);
 
 // Timeout self-test: one CTA waits on a barrier that is never arrived at.
 cudaError_t launch_wait_timeout_probe(uint64_t timeout_ns, unsigned int* status, cudaStream_t stream);

@@ -6,20 +6,29 @@
 // exist only on chip, each row keeps a running max m and sum l, the unnormalised output o is
 // rescaled by exp(m - m_new) when the max grows, and O = o / l is written once.
 //
-// GB300 mapping (one CTA = two 128-row query tiles of one (sequence, head); 10 warps):
-//   warp 8      TMA producer: loads both Q tiles once, then K_j, V_j tiles (128 keys x d,
-//               128-byte swizzle) into a ring of shared-memory slots guarded by mbarriers.
+// GB300 mapping. A work item is two 128-row query tiles of one (sequence, head). The kernel is
+// persistent: one CTA per SM takes items from a list in order through an atomic counter
+// (dynamic, so long and short items balance). The list is cut into bands of 16 (sequence,
+// head) units and, inside a band, ordered longest first: the items in flight at any time
+// then belong to one or two bands, whose K/V (a few tens of MB) stay in L2 while every query
+// tile of those heads reads them. 10 warps per CTA:
+//   warp 8      TMA producer: takes the next item and hands it to the other roles through a
+//               small shared-memory queue; per item, both Q tiles once (after the previous item's last
+//               S MMA freed them), then K_j, V_j tiles (128 keys x d, 128-byte swizzle) into a
+//               ring of shared-memory slots guarded by full/empty mbarriers; the ring runs on
+//               across items.
 //   warp 9      MMA issuer (one thread): S_w = Q_w K_j^T into TMEM (fp32, 128 columns per
-//               tile), then O_w += P_w V_j with P read from TMEM (bf16, aliased onto S_w)
-//               and V from shared memory. Issue order S0(j+1) after PV0(j), S1(j+1) after
-//               PV1(j) lets softmax of one tile overlap the tensor core work of the other.
-//   warps 0-3,  softmax warpgroups, one per query tile, thread = row = TMEM lane: read the
-//   4-7         S row, apply the causal mask on diagonal tiles only ("Attention Computation
-//               in Practice", Masking variants: skip / full / diagonal), update m and l in
-//               registers (exp2 with log2(e) folded into the scale), write P as bf16 into
-//               TMEM, and rescale O in TMEM when the running max grew by more than 2^8
-//               (a lazily updated reference max: l and o always share it, so the final o / l
-//               is unchanged). Tiles entirely above the diagonal are never loaded.
+//               tile), then O_w += P_w V_j with P read from TMEM (bf16, aliased onto S_w) and V
+//               from shared memory. Issue order S0(j+1) after PV0(j), S1(j+1) after PV1(j): the
+//               softmax of one tile overlaps tensor work on the other.
+//   warps 0-3,  softmax warpgroups, one per query tile, thread = row = TMEM lane: read the S
+//   4-7         row, apply the causal mask on diagonal tiles only ("Attention Computation in
+//               Practice", Masking variants: skip / full / diagonal), update m and l in
+//               registers (exp2 with log2(e) folded into the scale), write P as bf16 into TMEM,
+//               rescale O in TMEM when the running max grew by more than 2^8 (a lazily updated
+//               reference max: l and o always share it, so the final o / l is unchanged), and
+//               at the end of the item write O = o / l and the LSE. Tiles entirely above the
+//               diagonal are never loaded.
 // Every wait is bounded; a timed-out wait sets the device status word, the CTA stops
 // producing output, waits for its own copies and MMAs and frees its TMEM.
 #include <math.h>
@@ -37,6 +46,9 @@ constexpr int kThreads = 320;
 constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
+constexpr int kBandUnits = 16;             // (sequence, head) units per band of the item list
+constexpr int kItemSlots = 2;              // depth of the item queue from producer to consumers
+constexpr int kItemConsumers = 1 + 8;      // MMA thread + one lane of each softmax warp
 
 template <int D>
 struct Cfg {
@@ -51,18 +63,22 @@ struct Cfg {
 };
 
 struct Barriers {
-  uint64_t q_full;
+  uint64_t q_full, q_empty;
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_full[2];
+  uint64_t o_empty[2];
   uint64_t mma_done;
   uint64_t kv_full[6];
   uint64_t kv_empty[6];
+  uint64_t item_full[kItemSlots];
+  uint64_t item_empty[kItemSlots];
+  int item_q[kItemSlots];  // item index, or -1 when the list is exhausted
   uint32_t tmem_base;
   int abort;
 };
 
-struct Work {
+struct Item {
   bool active;
   int nq, nk;
   int q_lo[2];  // first row (within the sequence) of each query tile
@@ -75,11 +91,20 @@ struct Work {
   int64_t out_row_stride;
 };
 
-__device__ __forceinline__ Work make_work(const TcFwdArgs& a) {
-  Work w;
-  const int pair = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);  // long tiles first
-  const int h = blockIdx.y;
-  const int s = blockIdx.z;
+// Item numbering: bands of kBandUnits (sequence, head) units; inside a band all units of the
+// last query-tile pair come first, then those of the pair before, and so on (with a causal
+// mask later pairs see more keys).
+__device__ __forceinline__ Item make_item(const TcFwdArgs& a, int idx) {
+  Item w;
+  const int units = a.num_seqs * a.Hq;
+  const int per_band = kBandUnits * a.max_pairs;
+  const int band = idx / per_band;
+  const int within = idx % per_band;
+  const int band_units = min(kBandUnits, units - band * kBandUnits);
+  const int pair = a.max_pairs - 1 - within / band_units;
+  const int unit = band * kBandUnits + within % band_units;
+  const int s = unit / a.Hq;
+  const int h = unit % a.Hq;
   const int g = a.Hq / a.Hkv;
   const int hkv = h / g;
   w.packed = a.cu_q != nullptr;
@@ -128,7 +153,17 @@ __device__ __forceinline__ Work make_work(const TcFwdArgs& a) {
   return w;
 }
 
-__device__ __forceinline__ void tma_tile(const CUtensorMap* map, const Work& w, uint8_t* dst, uint64_t* bar,
+// Consumer side of the item queue: the k-th item this CTA runs (-1: no more items).
+__device__ __forceinline__ int next_item(Barriers* bar, int k, bool arrive, uint64_t tmo, const volatile int* abort,
+                                         bool* ok) {
+  const int slot = k % kItemSlots;
+  *ok = mbar_wait(&bar->item_full[slot], (k / kItemSlots) & 1, tmo, abort);
+  const int idx = *ok ? *reinterpret_cast<volatile int*>(&bar->item_q[slot]) : -1;
+  if (arrive && *ok) mbar_arrive(&bar->item_empty[slot]);
+  return idx;
+}
+
+__device__ __forceinline__ void tma_tile(const CUtensorMap* map, const Item& w, uint8_t* dst, uint64_t* bar,
                                          int half, int row0, bool is_q) {
   const int c0 = half * 64;
   if (w.packed) {
@@ -140,31 +175,35 @@ __device__ __forceinline__ void tma_tile(const CUtensorMap* map, const Work& w, 
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ TcFwdArgs a,
-                                                                 unsigned int* status) {
+                                                                 unsigned int* status, unsigned int* sched) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem;                         // [2][halves][128 rows][128 B]
-  uint8_t* sRing = smem + 2 * C::kQBytes;     // [stages][halves][128 rows][128 B]
+  uint8_t* sQ = smem;                      // [2][halves][128 rows][128 B]
+  uint8_t* sRing = smem + 2 * C::kQBytes;  // [stages][halves][128 rows][128 B]
   Barriers* bar = reinterpret_cast<Barriers*>(smem + C::kBarOffset);
-
-  const Work w = make_work(a);
-  if (!w.active) return;  // uniform over the CTA, before any barrier or TMEM use
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int total_items = a.max_pairs * a.num_seqs * a.Hq;
 
   if (threadIdx.x == 0) {
     mbar_init(&bar->q_full, 1);
+    mbar_init(&bar->q_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar->s_full[i], 1);
       mbar_init(&bar->p_full[i], kBM);
       mbar_init(&bar->o_full[i], 1);
+      mbar_init(&bar->o_empty[i], kBM);
     }
     mbar_init(&bar->mma_done, 1);
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&bar->kv_full[i], 1);
       mbar_init(&bar->kv_empty[i], 1);
+    }
+    for (int i = 0; i < kItemSlots; ++i) {
+      mbar_init(&bar->item_full[i], 1);
+      mbar_init(&bar->item_empty[i], kItemConsumers);
     }
     bar->abort = 0;
     fence_mbar_init();
@@ -186,32 +225,46 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       prefetch_tmap(&a.tm_q);
       prefetch_tmap(&a.tm_k);
       prefetch_tmap(&a.tm_v);
-      mbar_arrive_expect_tx(&bar->q_full, 2 * C::kQBytes);
-      for (int t = 0; t < 2; ++t)
-        for (int hf = 0; hf < C::kHalves; ++hf)
-          tma_tile(&a.tm_q, w, sQ + t * C::kQBytes + hf * (kBM * 128), &bar->q_full, hf, w.q_lo[t], true);
-      const int nloads = 2 * w.nt_all;
-      int issued = 0;
-      for (int i = 0; i < nloads; ++i) {
-        const int slot = i % C::kStages;
-        const int round = i / C::kStages;
-        if (round > 0 && !mbar_wait(&bar->kv_empty[slot], (round - 1) & 1, tmo, abort)) {
-          raise_timeout(abort, status);
-          break;
+      int nload = 0;  // K/V tiles issued by this CTA, over all items
+      int items = 0;  // active items started by this CTA
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        // take the next active item from the list and hand it to the consumers
+        int idx;
+        Item w;
+        do {
+          idx = static_cast<int>(atomicAdd(&sched[0], 1u));
+          if (idx < total_items) w = make_item(a, idx);
+        } while (idx < total_items && !w.active);
+        if (idx >= total_items) idx = -1;
+        const int qs = k % kItemSlots;
+        if (k >= kItemSlots && !(ok = mbar_wait(&bar->item_empty[qs], ((k / kItemSlots) - 1) & 1, tmo, abort))) break;
+        bar->item_q[qs] = idx;
+        mbar_arrive(&bar->item_full[qs]);
+        if (idx < 0) break;
+        // Q buffers are free once every S MMA of the previous item has completed
+        if (items > 0 && !(ok = mbar_wait(&bar->q_empty, (items - 1) & 1, tmo, abort))) break;
+        mbar_arrive_expect_tx(&bar->q_full, 2 * C::kQBytes);
+        for (int t = 0; t < 2; ++t)
+          for (int hf = 0; hf < C::kHalves; ++hf)
+            tma_tile(&a.tm_q, w, sQ + t * C::kQBytes + hf * (kBM * 128), &bar->q_full, hf, w.q_lo[t], true);
+        ++items;
+        for (int i = 0; i < 2 * w.nt_all; ++i, ++nload) {
+          const int slot = nload % C::kStages;
+          const int round = nload / C::kStages;
+          if (round > 0 && !(ok = mbar_wait(&bar->kv_empty[slot], (round - 1) & 1, tmo, abort))) break;
+          mbar_arrive_expect_tx(&bar->kv_full[slot], C::kTileBytes);
+          for (int hf = 0; hf < C::kHalves; ++hf)
+            tma_tile((i & 1) ? &a.tm_v : &a.tm_k, w, sRing + slot * C::kTileBytes + hf * (kBN * 128),
+                     &bar->kv_full[slot], hf, (i >> 1) * kBN, false);
         }
-        const bool is_v = i & 1;
-        const int j = i >> 1;
-        mbar_arrive_expect_tx(&bar->kv_full[slot], C::kTileBytes);
-        for (int hf = 0; hf < C::kHalves; ++hf)
-          tma_tile(is_v ? &a.tm_v : &a.tm_k, w, sRing + slot * C::kTileBytes + hf * (kBN * 128),
-                   &bar->kv_full[slot], hf, j * kBN, false);
-        issued = i + 1;
       }
+      if (!ok) raise_timeout(abort, status);
       // every copy this CTA issued must have landed before the CTA may exit (bounded, and
       // not cut short by the abort flag)
       const int no_abort = 0;
-      mbar_wait(&bar->q_full, 0, tmo, &no_abort);
-      for (int i = max(0, issued - C::kStages); i < issued; ++i)
+      if (items > 0) mbar_wait(&bar->q_full, (items - 1) & 1, tmo, &no_abort);
+      for (int i = max(0, nload - C::kStages); i < nload; ++i)
         mbar_wait(&bar->kv_full[i % C::kStages], (i / C::kStages) & 1, tmo, &no_abort);
     }
   } else if (warp == kMmaWarp) {
@@ -219,62 +272,95 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, D, 0, 1);
-      const uint32_t sQ_addr = smem_u32(sQ);
-      const uint32_t sRing_addr = smem_u32(sRing);
-      const uint32_t colS[2] = {C::kColS0, C::kColS1};
-      const uint32_t colO[2] = {C::kColO0, C::kColO1};
-      bool ok = mbar_wait(&bar->q_full, 0, tmo, abort);
-      tc_fence_after();
+      // descriptor halves: K-major Q and K tiles (8-row groups 1024 B apart), MN-major V tiles
+      // (8-key groups 1024 B apart, the two 64-column halves kBN * 128 B apart)
+      const uint32_t hi = sdesc_hi(1024);
+      const uint32_t q_lo0 = sdesc_lo(smem_u32(sQ), 16);
+      const uint32_t q_lo1 = sdesc_lo(smem_u32(sQ) + C::kQBytes, 16);
+      const uint32_t k_lo = sdesc_lo(smem_u32(sRing), 16);
+      const uint32_t v_lo = sdesc_lo(smem_u32(sRing), kBN * 128);
+      const uint32_t slot_step = C::kTileBytes >> 4;
+      const uint32_t tS0 = tbase + C::kColS0, tS1 = tbase + C::kColS1;
+      const uint32_t tO0 = tbase + C::kColO0, tO1 = tbase + C::kColO1;
+      int nload = 0;      // K/V tiles consumed, over all items
+      int items = 0;      // active items
+      int pt0 = 0, pt1 = 0;  // p_full completions consumed per query tile
+      int ou0 = 0, ou1 = 0;  // items whose O accumulator of tile 0 / 1 was used
+      int s_left = 0;     // S MMAs still to issue in the current item
+      bool ok = true;
 
       auto wait_load = [&](int i) -> bool {
         const bool r = mbar_wait(&bar->kv_full[i % C::kStages], (i / C::kStages) & 1, tmo, abort);
         tc_fence_after();
         return r;
       };
-      auto issue_s = [&](int t, int j) {
-        const uint32_t kslot = sRing_addr + ((2 * j) % C::kStages) * C::kTileBytes;
-        const uint32_t qaddr = sQ_addr + t * C::kQBytes;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-          umma_ss(tbase + colS[t], sdesc_sw128(qaddr + off, 16, 1024), sdesc_sw128(kslot + off, 16, 1024),
-                  idesc_qk, kk > 0);
-        }
+      auto issue_s = [&](int t, int i) {  // S_t = Q_t K^T, K in load slot of load i
+        const uint32_t kl = k_lo + (i % C::kStages) * slot_step;
+        if constexpr (D == 128)
+          umma_ss_k128(t ? tS1 : tS0, t ? q_lo1 : q_lo0, hi, kl, hi, idesc_qk, 0);
+        else
+          umma_ss_k64(t ? tS1 : tS0, t ? q_lo1 : q_lo0, hi, kl, hi, idesc_qk, 0);
         umma_commit(&bar->s_full[t]);
+        if (--s_left == 0) umma_commit(&bar->q_empty);  // last read of the Q tiles issued
       };
-      auto issue_pv = [&](int t, int j) {
-        const uint32_t vslot = sRing_addr + ((2 * j + 1) % C::kStages) * C::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          umma_ts(tbase + colO[t], tbase + colS[t] + kk * 8, sdesc_sw128(vslot + kk * 16 * 128, kBN * 128, 1024),
-                  idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-        }
+      auto issue_pv = [&](int t, int i, bool accumulate) {  // O_t += P_t V, V in load slot of load i
+        umma_ts_k128(t ? tO1 : tO0, t ? tS1 : tS0, v_lo + (i % C::kStages) * slot_step, hi, idesc_pv,
+                     accumulate ? 1u : 0u);
       };
 
-      const int nt = w.nt_all;
-      if (ok && nt > 0) {
-        ok = wait_load(0);
-        if (ok) {
-          if (w.nt[0] > 0) issue_s(0, 0);
-          if (w.nt[1] > 0) issue_s(1, 0);
-          umma_commit(&bar->kv_empty[0]);
+      for (int k = 0; ok; ++k) {
+        const int idx = next_item(bar, k, true, tmo, abort, &ok);
+        if (!ok || idx < 0) break;
+        const Item w = make_item(a, idx);
+        if (!(ok = mbar_wait(&bar->q_full, items & 1, tmo, abort))) break;
+        tc_fence_after();
+        ++items;
+        const int nt = w.nt_all, nt0 = w.nt[0], nt1 = w.nt[1];
+        const int base = nload;
+        s_left = nt0 + nt1;
+        if (s_left == 0) umma_commit(&bar->q_empty);
+        if (nt > 0) {
+          if (!(ok = wait_load(base))) break;
+          if (nt0 > 0) issue_s(0, base);
+          if (nt1 > 0) issue_s(1, base);
+          umma_commit(&bar->kv_empty[base % C::kStages]);
         }
-      }
-      for (int j = 0; ok && j < nt; ++j) {
-        if (!(ok = wait_load(2 * j + 1))) break;
-        for (int t = 0; t < 2; ++t) {
-          if (j < w.nt[t]) {
-            if (!(ok = mbar_wait(&bar->p_full[t], j & 1, tmo, abort))) break;
+        for (int j = 0; j < nt; ++j) {
+          const int iv = base + 2 * j + 1, ik = base + 2 * j + 2;
+          if (!(ok = wait_load(iv))) break;
+          // tile 0: P0 V_j, then S0 for the next K tile
+          if (j < nt0) {
+            // the first P.V of an item overwrites O: the previous item's epilogue must be done
+            if (j == 0 && ou0 > 0 && !(ok = mbar_wait(&bar->o_empty[0], (ou0 - 1) & 1, tmo, abort))) break;
+            if (!(ok = mbar_wait(&bar->p_full[0], pt0 & 1, tmo, abort))) break;
+            ++pt0;
             tc_fence_after();
-            issue_pv(t, j);
-            if (j == w.nt[t] - 1) umma_commit(&bar->o_full[t]);
+            issue_pv(0, iv, j > 0);
+            if (j == nt0 - 1) {
+              umma_commit(&bar->o_full[0]);
+              ++ou0;
+            }
           }
-          if (t == 0 && j + 1 < nt && !(ok = wait_load(2 * (j + 1)))) break;
-          if (j + 1 < w.nt[t]) issue_s(t, j + 1);
+          if (j + 1 < nt && !(ok = wait_load(ik))) break;
+          if (j + 1 < nt0) issue_s(0, ik);
+          // tile 1
+          if (j < nt1) {
+            if (j == 0 && ou1 > 0 && !(ok = mbar_wait(&bar->o_empty[1], (ou1 - 1) & 1, tmo, abort))) break;
+            if (!(ok = mbar_wait(&bar->p_full[1], pt1 & 1, tmo, abort))) break;
+            ++pt1;
+            tc_fence_after();
+            issue_pv(1, iv, j > 0);
+            if (j == nt1 - 1) {
+              umma_commit(&bar->o_full[1]);
+              ++ou1;
+            }
+          }
+          if (j + 1 < nt1) issue_s(1, ik);
+          if (j + 1 < nt) umma_commit(&bar->kv_empty[ik % C::kStages]);
+          umma_commit(&bar->kv_empty[iv % C::kStages]);
         }
         if (!ok) break;
-        if (j + 1 < nt) umma_commit(&bar->kv_empty[(2 * (j + 1)) % C::kStages]);
-        umma_commit(&bar->kv_empty[(2 * j + 1) % C::kStages]);
+        nload += 2 * nt;
       }
       if (!ok) raise_timeout(abort, status);
       // all MMAs issued by this thread complete before TMEM is released
@@ -284,104 +370,121 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     }
   } else {
     // ------------------------------------------------------------ softmax warpgroups
-    const int t = warp >> 2;          // query tile of this warpgroup
+    const int t = warp >> 2;                 // query tile of this warpgroup
     const int row = (warp & 3) * 32 + lane;  // = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tbase + lane_base + (t ? C::kColS1 : C::kColS0);
     const uint32_t tO = tbase + lane_base + (t ? C::kColO1 : C::kColO0);
-    const int q_row = w.q_lo[t] + row;
-    const bool row_ok = q_row < w.nq;
-    int lim = a.causal ? min(w.nk, q_row + (w.nk - w.nq) + 1) : w.nk;
     const float sl2 = a.scale_log2;
-    float m_ref = -INFINITY, l = 0.f;
+    int stiles = 0;  // s_full completions consumed, over all items
+    int oused = 0;   // items whose O accumulator was used
     bool ok = true;
-    const int ntile = w.nt[t];
-    for (int j = 0; j < ntile; ++j) {
-      ok = mbar_wait(&bar->s_full[t], j & 1, tmo, abort);
+    for (int k = 0; ok; ++k) {
+      const int idx = next_item(bar, k, false, tmo, abort, &ok);
       ok = __all_sync(0xffffffffu, ok);
+      __syncwarp();
+      if (lane == 0 && ok) mbar_arrive(&bar->item_empty[k % kItemSlots]);
+      if (!ok || idx < 0) break;
+      const Item w = make_item(a, idx);
+      const int q_row = w.q_lo[t] + row;
+      const bool row_ok = q_row < w.nq;
+      const int lim = a.causal ? min(w.nk, q_row + (w.nk - w.nq) + 1) : w.nk;
+      const int ntile = w.nt[t];
+      float m_ref = -INFINITY, l = 0.f;
+      for (int j = 0; j < ntile; ++j) {
+        ok = mbar_wait(&bar->s_full[t], stiles & 1, tmo, abort);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        ++stiles;
+        tc_fence_after();
+        uint32_t s0[32], s1[32], s2[32], s3[32];
+        tmem_ld32(tS, s0);
+        tmem_ld32(tS + 32, s1);
+        tmem_ld32(tS + 64, s2);
+        tmem_ld32(tS + 96, s3);
+        tmem_wait_ld();
+        tmem_reg_fence(s0);
+        tmem_reg_fence(s1);
+        tmem_reg_fence(s2);
+        tmem_reg_fence(s3);
+        const int kv0 = j * kBN;
+        if (kv0 + kBN > lim) {
+          const uint32_t ninf = __float_as_uint(-INFINITY);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            if (kv0 + e >= lim) s0[e] = ninf;
+            if (kv0 + 32 + e >= lim) s1[e] = ninf;
+            if (kv0 + 64 + e >= lim) s2[e] = ninf;
+            if (kv0 + 96 + e >= lim) s3[e] = ninf;
+          }
+        }
+        // row max: four chains of 3-input max (a single 128-long chain is pure latency)
+        float mx0 = __uint_as_float(s0[0]), mx1 = __uint_as_float(s1[0]);
+        float mx2 = __uint_as_float(s2[0]), mx3 = __uint_as_float(s3[0]);
+#pragma unroll
+        for (int e = 1; e < 31; e += 2) {
+          mx0 = max3f(mx0, __uint_as_float(s0[e]), __uint_as_float(s0[e + 1]));
+          mx1 = max3f(mx1, __uint_as_float(s1[e]), __uint_as_float(s1[e + 1]));
+          mx2 = max3f(mx2, __uint_as_float(s2[e]), __uint_as_float(s2[e + 1]));
+          mx3 = max3f(mx3, __uint_as_float(s3[e]), __uint_as_float(s3[e + 1]));
+        }
+        mx0 = max3f(mx0, __uint_as_float(s0[31]), __uint_as_float(s1[31]));
+        mx2 = max3f(mx2, __uint_as_float(s2[31]), __uint_as_float(s3[31]));
+        const float mt = max3f(mx0, mx1, fmaxf(mx2, mx3));
+        const float m_new = fmaxf(m_ref, mt * sl2);
+        float alpha_o = 1.f;
+        if (m_new > m_ref + kRescaleThreshold) {
+          const float alpha = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - m_new);
+          l *= alpha;
+          if (j > 0) alpha_o = alpha;
+          m_ref = m_new;
+        }
+        const float nm = (m_ref == -INFINITY) ? 0.f : -m_ref;
+        // p = 2^(s * scale * log2e - m) as bf16 pairs; keys 32c..32c+31 -> P columns 16c..16c+15,
+        // stored a quarter at a time; the sum runs as 8 independent chains
+        float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        auto exp_quarter = [&](const uint32_t (&sc)[32], uint32_t col) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = ex2(fmaf(__uint_as_float(sc[2 * e]), sl2, nm));
+            const float p1 = ex2(fmaf(__uint_as_float(sc[2 * e + 1]), sl2, nm));
+            ls[(2 * e) & 7] += p0;
+            ls[(2 * e + 1) & 7] += p1;
+            pk[e] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(tS + col, pk);
+        };
+        exp_quarter(s0, 0);
+        exp_quarter(s1, 16);
+        exp_quarter(s2, 32);
+        exp_quarter(s3, 48);
+        l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+        if (__any_sync(0xffffffffu, alpha_o != 1.f)) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(tO + c * 32, ov);
+            tmem_wait_ld();
+            tmem_reg_fence(ov);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha_o);
+            tmem_st32(tO + c * 32, ov);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bar->p_full[t]);
+      }
       if (!ok) break;
-      tc_fence_after();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_reg_fence(sr[c]);
-      const int kv0 = j * kBN;
-      if (kv0 + kBN > lim) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (kv0 + c * 32 + e >= lim) sr[c][e] = __float_as_uint(-INFINITY);
+      // ---- epilogue: O = o / l (bf16), LSE = (m + log2 l) * ln 2
+      if (ntile > 0) {
+        ok = mbar_wait(&bar->o_full[t], oused & 1, tmo, abort);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        ++oused;
+        tc_fence_after();
       }
-      float mt = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int e = 0; e < 32; ++e) mt = fmaxf(mt, __uint_as_float(sr[c][e]));
-      const float m_new = fmaxf(m_ref, mt * sl2);
-      float alpha_o = 1.f;
-      if (m_new > m_ref + kRescaleThreshold) {
-        const float alpha = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - m_new);
-        l *= alpha;
-        if (j > 0) alpha_o = alpha;
-        m_ref = m_new;
-      }
-      const float muse = (m_ref == -INFINITY) ? 0.f : m_ref;
-      float lsum = 0.f;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2(fmaf(__uint_as_float(sr[c][2 * e]), sl2, -muse));
-          const float p1 = ex2(fmaf(__uint_as_float(sr[c][2 * e + 1]), sl2, -muse));
-          lsum += p0 + p1;
-          pk[e] = pack_bf16x2(p0, p1);
-        }
-        // P chunk c (32 keys) -> 16 columns of the S region
-#pragma unroll
-        for (int e = 0; e < 16; ++e) sr[c][e] = pk[e];
-      }
-      l += lsum;
-      {
-        uint32_t p01[32], p23[32];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          p01[e] = sr[0][e];
-          p01[16 + e] = sr[1][e];
-          p23[e] = sr[2][e];
-          p23[16 + e] = sr[3][e];
-        }
-        tmem_st32(tS, p01);
-        tmem_st32(tS + 32, p23);
-      }
-      if (__any_sync(0xffffffffu, alpha_o != 1.f)) {
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t ov[32];
-          tmem_ld32(tO + c * 32, ov);
-          tmem_wait_ld();
-          tmem_reg_fence(ov);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha_o);
-          tmem_st32(tO + c * 32, ov);
-        }
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bar->p_full[t]);
-    }
-    // ---- epilogue: O = o / l (bf16), LSE = (m + log2 l) * ln 2
-    if (ok && ntile > 0) {
-      ok = mbar_wait(&bar->o_full[t], 0, tmo, abort);
-      ok = __all_sync(0xffffffffu, ok);
-      tc_fence_after();
-    }
-    if (!ok) {
-      if (lane == 0) raise_timeout(abort, status);
-    } else {
       const float inv = (l > 0.f) ? 1.f / l : 0.f;
       uint16_t* orow = a.o + (w.out_row0 + static_cast<int64_t>(q_row) * w.out_row_stride) * D;
 #pragma unroll
@@ -408,10 +511,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           }
         }
       }
+      if (ntile > 0) {
+        // O has been read: the next item's first P.V may overwrite it
+        tc_fence_before();
+        mbar_arrive(&bar->o_empty[t]);
+      }
       if (row_ok && a.lse)
         a.lse[w.out_row0 + static_cast<int64_t>(q_row) * w.out_row_stride] =
             (l > 0.f) ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
     }
+    if (!ok && lane == 0) raise_timeout(abort, status);
     tc_fence_before();
   }
   __syncthreads();
@@ -419,6 +528,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tbase, C::kTmemCols);
+  }
+  // The last CTA to leave resets the item counter for the next launch that uses this slot:
+  // every CTA has made its final fetch before it counts itself out.
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(&sched[1], 1u) == gridDim.x - 1) {
+      atomicExch(&sched[0], 0u);
+      atomicExch(&sched[1], 0u);
+    }
   }
 }
 
@@ -438,22 +556,33 @@ __global__ void wait_timeout_probe_kernel(uint64_t timeout_ns, unsigned int* sta
   __syncthreads();
 }
 
+int g_num_sms[64] = {};
+
 template <int D>
-cudaError_t launch_d(const TcFwdArgs& a, unsigned int* status, cudaStream_t stream) {
+cudaError_t launch_d(const TcFwdArgs& a, unsigned int* status, unsigned int* sched, cudaStream_t stream) {
   using C = Cfg<D>;
   cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(C::kSmemBytes));
   if (e != cudaSuccess) return e;
-  dim3 grid(a.max_pairs, a.Hq, a.cu_q ? a.num_seqs : a.B);
-  prefill_tc_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(a, status);
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  int sms = (dev >= 0 && dev < 64) ? g_num_sms[dev] : 0;
+  if (sms == 0) {
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) g_num_sms[dev] = sms;
+  }
+  const long items = static_cast<long>(a.max_pairs) * a.num_seqs * a.Hq;
+  const int grid = static_cast<int>(items < sms ? items : sms);
+  if (grid <= 0) return cudaSuccess;
+  prefill_tc_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(a, status, sched);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_prefill_tc(const TcFwdArgs& a, unsigned int* status, cudaStream_t stream) {
-  if (a.d == 64) return launch_d<64>(a, status, stream);
-  return launch_d<128>(a, status, stream);
+cudaError_t launch_prefill_tc(const TcFwdArgs& a, unsigned int* status, unsigned int* sched, cudaStream_t stream) {
+  if (a.d == 64) return launch_d<64>(a, status, sched, stream);
+  return launch_d<128>(a, status, sched, stream);
 }
 
 cudaError_t launch_wait_timeout_probe(uint64_t timeout_ns, unsigned int* status, cudaStream_t stream) {

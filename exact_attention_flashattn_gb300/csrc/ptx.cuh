@@ -134,6 +134,99 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       : "memory");
 }
 
+// Descriptor halves for sdesc_sw128: the low word carries the start address (>> 4) and the
+// leading-dimension offset; the high word the stride offset, version and swizzle mode. Within
+// one swizzle-aligned tile, moving the start address only changes the low word.
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo_bytes) {
+  return ((saddr & 0x3FFFFu) >> 4) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+__device__ __forceinline__ uint32_t sdesc_hi(uint32_t sbo_bytes) {
+  return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+
+// Eight K=16 steps of D[tmem] (+)= A[smem] B[smem] over a 128-element-deep contraction held as
+// two 128-byte swizzle atoms (K-major, 128 rows per atom): the start address advances by 32 B
+// inside an atom and by one atom (`atom_bytes`) after four steps. acc0 = 0 overwrites D.
+__device__ __forceinline__ void umma_ss_k128(uint32_t d_tmem, uint32_t alo, uint32_t ahi, uint32_t blo, uint32_t bhi,
+                                             uint32_t idesc, uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 da, db;\n\t.reg .b32 xa, xb;\n\t"
+      "setp.ne.b32 p0, %6, 0;\n\tsetp.eq.u32 p1, 0, 0;\n\t"
+      "mov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p0;\n\t"
+      "add.u32 xa, %1, 2;\n\tadd.u32 xb, %3, 2;\n\tmov.b64 da, {xa, %2};\n\tmov.b64 db, {xb, %4};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p1;\n\t"
+      "add.u32 xa, %1, 4;\n\tadd.u32 xb, %3, 4;\n\tmov.b64 da, {xa, %2};\n\tmov.b64 db, {xb, %4};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p1;\n\t"
+      "add.u32 xa, %1, 6;\n\tadd.u32 xb, %3, 6;\n\tmov.b64 da, {xa, %2};\n\tmov.b64 db, {xb, %4};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p1;\n\t"
+      "add.u32 xa, %1, 1024;\n\tadd.u32 xb, %3, 1024;\n\tmov.b64 da, {xa, %2};\n\tmov.b64 db, {xb, %4};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p1;\n\t"
+      "add.u32 xa, %1, 1026;\n\tadd.u32 xb, %3, 1026;\n\tmov.b64 da, {xa, %2};\n\tmov.b64 db, {xb, %4};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p1;\n\t"
+      "add.u32 xa, %1, 1028;\n\tadd.u32 xb, %3, 1028;\n\tmov.b64 da, {xa, %2};\n\tmov.b64 db, {xb, %4};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p1;\n\t"
+      "add.u32 xa, %1, 1030;\n\tadd.u32 xb, %3, 1030;\n\tmov.b64 da, {xa, %2};\n\tmov.b64 db, {xb, %4};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p1;\n\t}\n" ::"r"(d_tmem),
+      "r"(alo), "r"(ahi), "r"(blo), "r"(bhi), "r"(idesc), "r"(acc0)
+      : "memory");
+}
+
+// Same for a 64-element-deep contraction (one atom): four K=16 steps.
+__device__ __forceinline__ void umma_ss_k64(uint32_t d_tmem, uint32_t alo, uint32_t ahi, uint32_t blo, uint32_t bhi,
+                                            uint32_t idesc, uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 da, db;\n\t.reg .b32 xa, xb;\n\t"
+      "setp.ne.b32 p0, %6, 0;\n\tsetp.eq.u32 p1, 0, 0;\n\t"
+      "mov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p0;\n\t"
+      "add.u32 xa, %1, 2;\n\tadd.u32 xb, %3, 2;\n\tmov.b64 da, {xa, %2};\n\tmov.b64 db, {xb, %4};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p1;\n\t"
+      "add.u32 xa, %1, 4;\n\tadd.u32 xb, %3, 4;\n\tmov.b64 da, {xa, %2};\n\tmov.b64 db, {xb, %4};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p1;\n\t"
+      "add.u32 xa, %1, 6;\n\tadd.u32 xb, %3, 6;\n\tmov.b64 da, {xa, %2};\n\tmov.b64 db, {xb, %4};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p1;\n\t}\n" ::"r"(d_tmem),
+      "r"(alo), "r"(ahi), "r"(blo), "r"(bhi), "r"(idesc), "r"(acc0)
+      : "memory");
+}
+
+// Eight K=16 steps of D[tmem] (+)= A[tmem] B[smem]: A advances 8 columns (16 bf16) per step,
+// B (MN-major, 128-byte rows) advances 16 rows = 2048 B per step. acc0 = 0 overwrites D.
+__device__ __forceinline__ void umma_ts_k128(uint32_t d_tmem, uint32_t a_tmem, uint32_t blo, uint32_t bhi,
+                                             uint32_t idesc, uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 db;\n\t.reg .b32 ta, xb;\n\t"
+      "setp.ne.b32 p0, %5, 0;\n\tsetp.eq.u32 p1, 0, 0;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p0;\n\t"
+      "add.u32 ta, %1, 8;\n\tadd.u32 xb, %2, 128;\n\tmov.b64 db, {xb, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
+      "add.u32 ta, %1, 16;\n\tadd.u32 xb, %2, 256;\n\tmov.b64 db, {xb, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
+      "add.u32 ta, %1, 24;\n\tadd.u32 xb, %2, 384;\n\tmov.b64 db, {xb, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
+      "add.u32 ta, %1, 32;\n\tadd.u32 xb, %2, 512;\n\tmov.b64 db, {xb, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
+      "add.u32 ta, %1, 40;\n\tadd.u32 xb, %2, 640;\n\tmov.b64 db, {xb, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
+      "add.u32 ta, %1, 48;\n\tadd.u32 xb, %2, 768;\n\tmov.b64 db, {xb, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
+      "add.u32 ta, %1, 56;\n\tadd.u32 xb, %2, 896;\n\tmov.b64 db, {xb, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(blo), "r"(bhi), "r"(idesc), "r"(acc0)
+      : "memory");
+}
+
+// 32 lanes x 16 columns store (thread t of the warp writes lane base + t).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 async op issued so far by this thread completes.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -206,6 +299,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_maj
 }
 
 // ---------------------------------------------------------------- scalar helpers
+
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
