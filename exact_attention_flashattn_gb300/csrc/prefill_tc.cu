@@ -65,7 +65,8 @@ struct Cfg {
 struct Barriers {
   uint64_t q_full, q_empty;
   uint64_t s_full[2];
-  uint64_t p_full[2];
+  uint64_t p_full[2];   // first half of P (keys 0..63) stored
+  uint64_t p2_full[2];  // second half of P (keys 64..127) stored
   uint64_t o_full[2];
   uint64_t o_empty[2];
   uint64_t mma_done;
@@ -193,6 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar->s_full[i], 1);
       mbar_init(&bar->p_full[i], kBM);
+      mbar_init(&bar->p2_full[i], kBM);
       mbar_init(&bar->o_full[i], 1);
       mbar_init(&bar->o_empty[i], kBM);
     }
@@ -303,9 +305,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         umma_commit(&bar->s_full[t]);
         if (--s_left == 0) umma_commit(&bar->q_empty);  // last read of the Q tiles issued
       };
-      auto issue_pv = [&](int t, int i, bool accumulate) {  // O_t += P_t V, V in load slot of load i
-        umma_ts_k128(t ? tO1 : tO0, t ? tS1 : tS0, v_lo + (i % C::kStages) * slot_step, hi, idesc_pv,
-                     accumulate ? 1u : 0u);
+      // O_t += P_t V with V in the load slot of load i, one half of the keys at a time: the
+      // softmax releases P in two halves so that the first half's MMAs overlap the rest of it
+      auto issue_pv_half = [&](int t, int i, int half, bool accumulate) {
+        umma_ts_k64(t ? tO1 : tO0, (t ? tS1 : tS0) + half * 32, v_lo + (i % C::kStages) * slot_step + half * 512, hi,
+                    idesc_pv, accumulate ? 1u : 0u);
       };
 
       for (int k = 0; ok; ++k) {
@@ -333,9 +337,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             // the first P.V of an item overwrites O: the previous item's epilogue must be done
             if (j == 0 && ou0 > 0 && !(ok = mbar_wait(&bar->o_empty[0], (ou0 - 1) & 1, tmo, abort))) break;
             if (!(ok = mbar_wait(&bar->p_full[0], pt0 & 1, tmo, abort))) break;
+            tc_fence_after();
+            issue_pv_half(0, iv, 0, j > 0);
+            if (!(ok = mbar_wait(&bar->p2_full[0], pt0 & 1, tmo, abort))) break;
             ++pt0;
             tc_fence_after();
-            issue_pv(0, iv, j > 0);
+            issue_pv_half(0, iv, 1, true);
             if (j == nt0 - 1) {
               umma_commit(&bar->o_full[0]);
               ++ou0;
@@ -347,9 +354,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           if (j < nt1) {
             if (j == 0 && ou1 > 0 && !(ok = mbar_wait(&bar->o_empty[1], (ou1 - 1) & 1, tmo, abort))) break;
             if (!(ok = mbar_wait(&bar->p_full[1], pt1 & 1, tmo, abort))) break;
+            tc_fence_after();
+            issue_pv_half(1, iv, 0, j > 0);
+            if (!(ok = mbar_wait(&bar->p2_full[1], pt1 & 1, tmo, abort))) break;
             ++pt1;
             tc_fence_after();
-            issue_pv(1, iv, j > 0);
+            issue_pv_half(1, iv, 1, true);
             if (j == nt1 - 1) {
               umma_commit(&bar->o_full[1]);
               ++ou1;
@@ -441,25 +451,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         }
         const float nm = (m_ref == -INFINITY) ? 0.f : -m_ref;
         // p = 2^(s * scale * log2e - m) as bf16 pairs; keys 32c..32c+31 -> P columns 16c..16c+15,
-        // stored a quarter at a time; the sum runs as 8 independent chains
+        // stored a quarter at a time; fp32 pairs go through packed FMA / ADD; the sum runs as
+        // 4 independent pair chains
         float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         auto exp_quarter = [&](const uint32_t (&sc)[32], uint32_t col) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float p0 = ex2(fmaf(__uint_as_float(sc[2 * e]), sl2, nm));
-            const float p1 = ex2(fmaf(__uint_as_float(sc[2 * e + 1]), sl2, nm));
-            ls[(2 * e) & 7] += p0;
-            ls[(2 * e + 1) & 7] += p1;
+            float x0, x1;
+            ffma2(x0, x1, __uint_as_float(sc[2 * e]), __uint_as_float(sc[2 * e + 1]), sl2, nm);
+            const float p0 = ex2(x0);
+            const float p1 = ex2(x1);
+            fadd2(ls[(2 * e) & 7], ls[(2 * e + 1) & 7], p0, p1);
             pk[e] = pack_bf16x2(p0, p1);
           }
           tmem_st16(tS + col, pk);
         };
         exp_quarter(s0, 0);
         exp_quarter(s1, 16);
-        exp_quarter(s2, 32);
-        exp_quarter(s3, 48);
-        l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+        // O must carry the new reference max before this tile's P.V starts (rare)
         if (__any_sync(0xffffffffu, alpha_o != 1.f)) {
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
@@ -472,9 +482,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             tmem_st32(tO + c * 32, ov);
           }
         }
+        // keys 0..63 of P are in TMEM: the MMA warp may start on them
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bar->p_full[t]);
+        exp_quarter(s2, 32);
+        exp_quarter(s3, 48);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bar->p2_full[t]);
+        l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       }
       if (!ok) break;
       // ---- epilogue: O = o / l (bf16), LSE = (m + log2 l) * ln 2

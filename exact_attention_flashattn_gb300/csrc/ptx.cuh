@@ -217,6 +217,41 @@ __device__ __forceinline__ void umma_ts_k128(uint32_t d_tmem, uint32_t a_tmem, u
       : "memory");
 }
 
+// Four K=16 steps of D[tmem] (+)= A[tmem] B[smem] (one half of a 128-key P.V): A advances 8
+// columns per step, B (MN-major, 128-byte rows) 2048 B per step. acc0 = 0 overwrites D.
+__device__ __forceinline__ void umma_ts_k64(uint32_t d_tmem, uint32_t a_tmem, uint32_t blo, uint32_t bhi,
+                                            uint32_t idesc, uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 db;\n\t.reg .b32 ta, xb;\n\t"
+      "setp.ne.b32 p0, %5, 0;\n\tsetp.eq.u32 p1, 0, 0;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p0;\n\t"
+      "add.u32 ta, %1, 8;\n\tadd.u32 xb, %2, 128;\n\tmov.b64 db, {xb, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
+      "add.u32 ta, %1, 16;\n\tadd.u32 xb, %2, 256;\n\tmov.b64 db, {xb, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
+      "add.u32 ta, %1, 24;\n\tadd.u32 xb, %2, 384;\n\tmov.b64 db, {xb, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(blo), "r"(bhi), "r"(idesc), "r"(acc0)
+      : "memory");
+}
+
+// Packed fp32 pairs (one instruction for two lanes of work): d = a * b + c, d = a + b.
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b, float c) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %4};\n\tmov.b64 rc, {%5, %5};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}\n"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+__device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%0, %1};\n\tmov.b64 rb, {%2, %3};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}\n"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1));
+}
+
 // 32 lanes x 16 columns store (thread t of the warp writes lane base + t).
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
   asm volatile(
