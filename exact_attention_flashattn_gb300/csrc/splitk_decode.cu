@@ -16,7 +16,9 @@
 // are 16-byte vector loads straight into registers. To make them line up with the MMA
 // fragment layout without shared memory, the head-dim index is permuted identically on Q
 // and K (a permutation of the contraction index leaves the dot product unchanged), and the
-// output-channel index of the P V product is permuted and undone at the write.
+// output-channel index of the P V product is permuted and undone at the write. When a row
+// group has at most 8 rows (GQA groups of up to 8 heads) the padding half of the MMA rows is
+// fed zeros and its accumulators are not kept, which frees registers for more warps per SM.
 #include <math.h>
 
 #include "kernels.h"
@@ -31,6 +33,7 @@ constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kRowsPerGroup = 16;
 constexpr int kKeysPerStep = 16;
+constexpr int kMergeThreads = 256;
 
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
   uint4 r;
@@ -46,6 +49,18 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       "{%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Rows 8..15 are padding: A rows 8..15 are zero and their accumulators are discarded.
+__device__ __forceinline__ void mma_bf16_top(float& d0, float& d1, uint32_t a0, uint32_t a2, uint32_t b0,
+                                             uint32_t b1) {
+  float x2, x3;
+  asm volatile(
+      "{\n\t.reg .b32 z;\n\tmov.b32 z, 0;\n\t"
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, z, %5, z}, {%6, %7}, "
+      "{%0, %1, z, z};\n\t}\n"
+      : "+f"(d0), "+f"(d1), "=f"(x2), "=f"(x3)
+      : "r"(a0), "r"(a2), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ uint32_t word(const uint4& v, int w) {
@@ -90,7 +105,9 @@ __device__ __forceinline__ size_t ws_ml_index(const SplitKArgs& a, int unit, int
   return ((static_cast<size_t>(unit) * a.num_splits + s) * a.rows_max + r) * 2;
 }
 
-__global__ void __launch_bounds__(kThreads, 3) splitk_kernel(SplitKArgs a) {
+// NH = number of 8-row halves of the 16-row MMA tile that carry real rows (1 or 2).
+template <int NH>
+__global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(SplitKArgs a) {
   const int split = blockIdx.x;
   const int hkv = blockIdx.y % a.Hkv;
   const int grp = blockIdx.y / a.Hkv;
@@ -110,13 +127,13 @@ __global__ void __launch_bounds__(kThreads, 3) splitk_kernel(SplitKArgs a) {
   const int kbeg = min(u.nk, split * chunk);
   const int kend = min(u.nk, kbeg + chunk);
 
-  // Rows gr and gr + 8 of this group: (query i, head hh) and their key limits.
+  // Rows gr (and gr + 8) of this group: (query i, head hh) and their key limits.
   int lim[2];
   uint32_t qa[8][4];
 #pragma unroll
   for (int rr = 0; rr < 2; ++rr) {
     const int r = row0 + gr + 8 * rr;
-    const bool ok = r < R;
+    const bool ok = rr < NH && r < R;
     const int i = ok ? r / a.g : 0;
     const int hh = ok ? r % a.g : 0;
     lim[rr] = a.causal ? min(kend, u.nk - u.nq + i + 1) : kend;
@@ -137,9 +154,11 @@ __global__ void __launch_bounds__(kThreads, 3) splitk_kernel(SplitKArgs a) {
   int min_lim = kend;
   if (a.causal) min_lim = min(kend, u.nk - u.nq + row0 / a.g + 1);
 
-  float oacc[16][4];
+  float oacc[16][2 * NH];
 #pragma unroll
-  for (int nu = 0; nu < 16; ++nu) oacc[nu][0] = oacc[nu][1] = oacc[nu][2] = oacc[nu][3] = 0.f;
+  for (int nu = 0; nu < 16; ++nu)
+#pragma unroll
+    for (int c = 0; c < 2 * NH; ++c) oacc[nu][c] = 0.f;
   float m_run[2] = {-INFINITY, -INFINITY};
   float l_part[2] = {0.f, 0.f};
 
@@ -176,7 +195,10 @@ __global__ void __launch_bounds__(kThreads, 3) splitk_kernel(SplitKArgs a) {
         const uint4& c = kk[nt][kst >> 1];
         const uint32_t b0 = (kst & 1) ? c.z : c.x;
         const uint32_t b1 = (kst & 1) ? c.w : c.y;
-        mma_bf16(sacc[nt], qa[kst], b0, b1);
+        if constexpr (NH == 2)
+          mma_bf16(sacc[nt], qa[kst], b0, b1);
+        else
+          mma_bf16_top(sacc[nt][0], sacc[nt][1], qa[kst][0], qa[kst][2], b0, b1);
       }
     }
     // ---- scale (log2 units), mask, row max over the quad
@@ -185,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 3) splitk_kernel(SplitKArgs a) {
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2 * NH; ++c) {
         const int rr = c >> 1;
         float s = sacc[nt][c] * a.scale_log2;
         if (need_mask) {
@@ -196,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 3) splitk_kernel(SplitKArgs a) {
         mx[rr] = fmaxf(mx[rr], s);
       }
 #pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
+    for (int rr = 0; rr < NH; ++rr) {
       mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
       mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
     }
@@ -204,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 3) splitk_kernel(SplitKArgs a) {
     float mnew[2], muse[2];
     bool grow = false;
 #pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
+    for (int rr = 0; rr < NH; ++rr) {
       mnew[rr] = fmaxf(m_run[rr], mx[rr]);
       grow |= mnew[rr] > m_run[rr];
       muse[rr] = (mnew[rr] == -INFINITY) ? 0.f : mnew[rr];
@@ -212,35 +234,36 @@ __global__ void __launch_bounds__(kThreads, 3) splitk_kernel(SplitKArgs a) {
     if (__any_sync(0xffffffffu, grow)) {
       float al[2];
 #pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
+      for (int rr = 0; rr < NH; ++rr) {
         al[rr] = (m_run[rr] == -INFINITY) ? 0.f : ex2(m_run[rr] - muse[rr]);
         l_part[rr] *= al[rr];
       }
 #pragma unroll
-      for (int nu = 0; nu < 16; ++nu) {
-        oacc[nu][0] *= al[0];
-        oacc[nu][1] *= al[0];
-        oacc[nu][2] *= al[1];
-        oacc[nu][3] *= al[1];
-      }
+      for (int nu = 0; nu < 16; ++nu)
+#pragma unroll
+        for (int c = 0; c < 2 * NH; ++c) oacc[nu][c] *= al[c >> 1];
     }
-    m_run[0] = mnew[0];
-    m_run[1] = mnew[1];
+#pragma unroll
+    for (int rr = 0; rr < NH; ++rr) m_run[rr] = mnew[rr];
     uint32_t pa[4];
     {
       float p[2][4];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2 * NH; ++c) {
           p[nt][c] = ex2(sacc[nt][c] - muse[c >> 1]);
           l_part[c >> 1] += p[nt][c];
         }
       // A fragment of P (rows x 16 keys): k positions 2t,2t+1 from tile 0, 2t+8,2t+9 from tile 1
       pa[0] = pack_bf16x2(p[0][0], p[0][1]);
-      pa[1] = pack_bf16x2(p[0][2], p[0][3]);
       pa[2] = pack_bf16x2(p[1][0], p[1][1]);
-      pa[3] = pack_bf16x2(p[1][2], p[1][3]);
+      if constexpr (NH == 2) {
+        pa[1] = pack_bf16x2(p[0][2], p[0][3]);
+        pa[3] = pack_bf16x2(p[1][2], p[1][3]);
+      } else {
+        pa[1] = pa[3] = 0u;
+      }
     }
     // ---- O += P V over 16 output n-tiles
 #pragma unroll
@@ -250,7 +273,12 @@ __global__ void __launch_bounds__(kThreads, 3) splitk_kernel(SplitKArgs a) {
       const uint32_t sel = (e & 1) ? 0x7632u : 0x5410u;
       const uint32_t w0 = word((nu < 8) ? va[0] : vb[0], w), w1 = word((nu < 8) ? va[1] : vb[1], w);
       const uint32_t w2 = word((nu < 8) ? va[2] : vb[2], w), w3 = word((nu < 8) ? va[3] : vb[3], w);
-      mma_bf16(oacc[nu], pa, __byte_perm(w0, w1, sel), __byte_perm(w2, w3, sel));
+      if constexpr (NH == 2) {
+        float(&acc)[4] = *reinterpret_cast<float(*)[4]>(&oacc[nu][0]);
+        mma_bf16(acc, pa, __byte_perm(w0, w1, sel), __byte_perm(w2, w3, sel));
+      } else {
+        mma_bf16_top(oacc[nu][0], oacc[nu][1], pa[0], pa[2], __byte_perm(w0, w1, sel), __byte_perm(w2, w3, sel));
+      }
     }
   }
 
@@ -259,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 3) splitk_kernel(SplitKArgs a) {
   __shared__ float sm_l[kWarps][kRowsPerGroup];
   __shared__ float sm_o[kWarps][kRowsPerGroup][D + 4];
 #pragma unroll
-  for (int rr = 0; rr < 2; ++rr) {
+  for (int rr = 0; rr < NH; ++rr) {
     float l = l_part[rr];
     l += __shfl_xor_sync(0xffffffffu, l, 1);
     l += __shfl_xor_sync(0xffffffffu, l, 2);
@@ -272,15 +300,17 @@ __global__ void __launch_bounds__(kThreads, 3) splitk_kernel(SplitKArgs a) {
   for (int nu = 0; nu < 16; ++nu) {
     sm_o[warp][gr][dv_of(nu, 2 * t)] = oacc[nu][0];
     sm_o[warp][gr][dv_of(nu, 2 * t + 1)] = oacc[nu][1];
-    sm_o[warp][gr + 8][dv_of(nu, 2 * t)] = oacc[nu][2];
-    sm_o[warp][gr + 8][dv_of(nu, 2 * t + 1)] = oacc[nu][3];
+    if constexpr (NH == 2) {
+      sm_o[warp][gr + 8][dv_of(nu, 2 * t)] = oacc[nu][2];
+      sm_o[warp][gr + 8][dv_of(nu, 2 * t + 1)] = oacc[nu][3];
+    }
   }
   __syncthreads();
   const int unit = seq * a.Hkv + hkv;
-  const int nrows = min(kRowsPerGroup, R - row0);
+  const int nrows = min(8 * NH, R - row0);
   float* ws_o = a.ws + a.ws_o_offset;
-  // thread -> (row, channel quad): 16 rows x 32 quads = 512 items, 4 per thread
-  for (int it = threadIdx.x; it < kRowsPerGroup * (D / 4); it += kThreads) {
+  // thread -> (row, channel quad)
+  for (int it = threadIdx.x; it < 8 * NH * (D / 4); it += kThreads) {
     const int r = it / (D / 4);
     const int c4 = it % (D / 4);
     if (r >= nrows) continue;
@@ -309,14 +339,12 @@ __global__ void __launch_bounds__(kThreads, 3) splitk_kernel(SplitKArgs a) {
   }
 }
 
-// One warp per output row: merge the num_splits partials of (unit, row).
-__global__ void __launch_bounds__(256) merge_kernel(MergeArgs a) {
-  const int warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  const int units = a.num_seqs * a.Hkv;
-  if (warp_global >= units * a.rows_max) return;
-  const int unit = warp_global / a.rows_max;
-  const int r = warp_global % a.rows_max;
+// One CTA per output row: merge the num_splits partials of (unit, row). The global max comes
+// first; each warp then sums its share of the splits with weights e^{m_s - M}, and the warps'
+// sums are added in shared memory.
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(MergeArgs a) {
+  const int unit = blockIdx.x / a.rows_max;
+  const int r = blockIdx.x % a.rows_max;
   const int seq = unit / a.Hkv, hkv = unit % a.Hkv;
   int tok0, nq;
   if (a.cu_q) {
@@ -330,30 +358,58 @@ __global__ void __launch_bounds__(256) merge_kernel(MergeArgs a) {
   if (r >= nq * a.g) return;
   const int i = r / a.g, hh = r % a.g;
   const int S = a.num_splits;
-  const float* ml = a.ws + (static_cast<size_t>(unit) * S * a.rows_max + r) * 2;  // split stride rows_max*2
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int kMW = kMergeThreads / 32;
+  const float* ml = a.ws + (static_cast<size_t>(unit) * S * a.rows_max + r) * 2;
   const float* wo = a.ws + a.ws_o_offset + (static_cast<size_t>(unit) * S * a.rows_max + r) * D;
   const size_t ml_stride = static_cast<size_t>(a.rows_max) * 2;
   const size_t o_stride = static_cast<size_t>(a.rows_max) * D;
+  __shared__ float sh_red[kMW];
+  __shared__ float4 sh_o[kMW][D / 4];
+  __shared__ float sh_l[kMW];
 
+  // global max over the non-empty partials
   float M = -INFINITY;
-  for (int s = lane; s < S; s += 32) {
-    const float ls = ml[s * ml_stride + 1];
-    if (ls > 0.f) M = fmaxf(M, ml[s * ml_stride]);
+  for (int s = threadIdx.x; s < S; s += kMergeThreads) {
+    const float2 v = *reinterpret_cast<const float2*>(ml + s * ml_stride);
+    if (v.y > 0.f) M = fmaxf(M, v.x);
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  if (lane == 0) sh_red[warp] = M;
+  __syncthreads();
+  M = sh_red[0];
+#pragma unroll
+  for (int w = 1; w < kMW; ++w) M = fmaxf(M, sh_red[w]);
+
+  // this warp's splits: s = warp, warp + kMW, ...; lane owns channels 4*lane .. 4*lane+3
   float L = 0.f;
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = 0; s < S; ++s) {
-    const float ls = ml[s * ml_stride + 1];
-    if (!(ls > 0.f)) continue;
-    const float f = ex2(ml[s * ml_stride] - M);
-    L += f * ls;
+  for (int s = warp; s < S; s += kMW) {
+    const float2 v = *reinterpret_cast<const float2*>(ml + s * ml_stride);
+    if (!(v.y > 0.f)) continue;
+    const float f = ex2(v.x - M);
+    L += f * v.y;
     const float4 x = *reinterpret_cast<const float4*>(wo + s * o_stride + 4 * lane);
     o.x += f * x.x;
     o.y += f * x.y;
     o.z += f * x.z;
     o.w += f * x.w;
+  }
+  sh_o[warp][lane] = o;
+  if (lane == 0) sh_l[warp] = L;
+  __syncthreads();
+  if (warp != 0) return;
+  L = 0.f;
+  o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int w = 0; w < kMW; ++w) {
+    L += sh_l[w];
+    const float4 x = sh_o[w][lane];
+    o.x += x.x;
+    o.y += x.y;
+    o.z += x.z;
+    o.w += x.w;
   }
   const float inv = (L > 0.f) ? 1.f / L : 0.f;
   const int64_t orow = (static_cast<int64_t>(tok0 + i) * a.Hq + hkv * a.g + hh);
@@ -368,14 +424,18 @@ __global__ void __launch_bounds__(256) merge_kernel(MergeArgs a) {
 
 cudaError_t launch_splitk(const SplitKArgs& a, cudaStream_t stream) {
   dim3 grid(a.num_splits, a.Hkv * a.row_groups, a.num_seqs);
-  splitk_kernel<<<grid, kThreads, 0, stream>>>(a);
+  // every row group has at most 8 rows when the sequences' rows (n_q * g) never exceed 8
+  const bool half = a.cu_q ? (a.small_rows_limit <= 8) : (a.g <= 8);
+  if (half)
+    splitk_kernel<1><<<grid, kThreads, 0, stream>>>(a);
+  else
+    splitk_kernel<2><<<grid, kThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
-  const long warps = static_cast<long>(a.num_seqs) * a.Hkv * a.rows_max;
-  const long blocks = (warps * 32 + 255) / 256;
-  merge_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
+  const long blocks = static_cast<long>(a.num_seqs) * a.Hkv * a.rows_max;
+  merge_kernel<<<static_cast<unsigned>(blocks), kMergeThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
