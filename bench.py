@@ -43,10 +43,10 @@ HEADLINE = "prefill_causal_b4_h32_n4096_d128"
 # only while the kernel source is the profiled one (checked by hash); otherwise reported null.
 PROFILED_TRAFFIC = {
     "kernel_source": "exact_attention_flashattn_gb300/csrc/prefill_tc.cu",
-    "sha256": "4732e02d949746ed129f5d7ca189ef60539cdbddad31cea747c2eb728b076977",
-    # (201.78 MB read + 54.04 MB written) at B=2 (profiles/prefill_tc_b2_h32_n4096_d128.md),
+    "sha256": "89a597d9d9da5748b8e8332301b4bf04eeb4848cc6e30b4f6f0d15826e152521",
+    # (201.53 MB read + 46.26 MB written) at B=2 (profiles/prefill_tc_b2_h32_n4096_d128.md),
     # scaled x2 to the B=4 launch: traffic grows with the number of (batch, head) units
-    "bytes_per_launch": 511645184,
+    "bytes_per_launch": 495585792,
 }
 METRIC = "prefill TFLOP/s and decode KV GB/s, 1×GB300, as fraction of roofline"
 L2_BYTES = 129 * 1024 * 1024
