@@ -96,12 +96,19 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """Largest value over all ranks (the slowest rank's time sets the job's time)."""
     if world <= 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(units_per_rank, world, ms_max):
+    """Whole-job rate: the units all ranks processed divided by the slowest rank's time."""
+    return units_per_rank * world / (ms_max * 1e-3)
 
 
 # ------------------------------------------------------------------ clocks
@@ -329,7 +336,7 @@ def main():
     clocks = clk.summary()
     ms = max_over_ranks(statistics.mean(per), world)
     flops = rl.prefill_flops(w.B, w.Hq, w.Nq, w.Nk, w.d, True)
-    value = flops * world / (ms * 1e-3) / 1e12
+    value = job_throughput(flops, world, ms) / 1e12
     achieved = flops / (ms * 1e-3) / 1e12
     in_bytes = 3 * q.numel() * q.element_size()
 
