@@ -263,6 +263,16 @@ def run_case(args, world, stream, dev, peaks):
         ms = statistics.mean(per)
         out.update({"B": B, "ms": ms, "tflops": rl.prefill_flops(B, w.Hq, w.Nq, w.Nk, w.d, True) / ms / 1e9,
                     "launches": n})
+    elif args.case == "paged":
+        x = wl.make("decode_paged_b8_h32x8_n32768_d128_p16", device=dev)
+        wd = x["w"]
+        nk = x["nk"].to(dev)
+        ws = torch.empty(bw.decode_workspace_size(wd.B, wd.Hq, wd.d, wd.num_splits), dtype=torch.uint8, device=dev)
+        per, n = time_steps(lambda: bw.attn_decode_paged(x["q"], x["k_pages"], x["v_pages"], x["block_table"], nk,
+                                                         wd.num_splits, workspace=ws), args.steps, args.warmup, world,
+                            stream)
+        ms = statistics.mean(per)
+        out[wd.name] = {"ms": ms, "GB/s": rl.decode_kv_bytes([wd.Nk] * wd.B, wd.Hkv, wd.d) / ms / 1e6, "launches": n}
     elif args.case == "decode":
         for name in ("decode_gqa_b8_h32x8_n32768_d128", "decode_long_b1_h64x8_n262144_d128"):
             x = wl.make(name, device=dev)
@@ -303,7 +313,7 @@ def main():
     ap.add_argument("--impl", default="own", choices=["own", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-breakdown", action="store_true")
-    ap.add_argument("--case", default="all", choices=["all", "prefill", "decode", "varlen"],
+    ap.add_argument("--case", default="all", choices=["all", "prefill", "decode", "paged", "varlen"],
                     help="profiling aid: run one part only (no e2e, no CPU baseline)")
     ap.add_argument("--batch", type=int, default=0, help="profiling aid: override the prefill batch size")
     args = ap.parse_args()
@@ -387,6 +397,25 @@ def main():
                                             "note": "split-K pass + merge, two launches, timed together"}}
             del xd, od, ld, wsd, nk
             torch.cuda.empty_cache()
+        xp = wl.make("decode_paged_b8_h32x8_n32768_d128_p16", device=dev)
+        wp = xp["w"]
+        nkp = xp["nk"].to(dev)
+        wsp = torch.empty(bw.decode_workspace_size(wp.B, wp.Hq, wp.d, wp.num_splits), dtype=torch.uint8, device=dev)
+        op = torch.empty_like(xp["q"])
+        lp = torch.empty((wp.B, wp.Hq), dtype=torch.float32, device=dev)
+        fn = lambda: bw.attn_decode_paged(xp["q"], xp["k_pages"], xp["v_pages"], xp["block_table"], nkp,  # noqa: E731
+                                          wp.num_splits, workspace=wsp, out=op, lse=lp)
+        perp, _ = time_steps(fn, args.steps, args.warmup, world, stream)
+        msp = max_over_ranks(statistics.mean(perp), world)
+        kvb = rl.decode_kv_bytes([wp.Nk] * wp.B, wp.Hkv, wp.d)
+        gbs = kvb / (msp * 1e-3) / 1e9
+        breakdown[wp.name] = {"metric": "decode KV-cache GB/s", "value": gbs * world, "unit": "GB/s",
+                              "ms_per_step": msp, "num_splits": wp.num_splits, "page_size": wp.extra["page_size"],
+                              "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                           "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": kvb,
+                                           "traffic": None, "note": "paged split-K pass + merge, two launches"}}
+        del xp, wsp, op, lp, nkp
+        torch.cuda.empty_cache()
         xv = wl.make("varlen_append_64seq_h32x8_d128", device=dev)
         wv = xv["w"]
         cq, ck = xv["cu_q"].to(dev), xv["cu_k"].to(dev)

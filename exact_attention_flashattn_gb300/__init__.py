@@ -24,7 +24,7 @@ import threading
 import torch
 
 __all__ = [
-    "attn_fwd", "attn_decode", "attn_varlen", "decode_workspace_size", "varlen_workspace_size",
+    "attn_fwd", "attn_decode", "attn_decode_paged", "attn_varlen", "decode_workspace_size", "varlen_workspace_size",
     "get_status", "clear_status", "set_wait_timeout_ns", "test_wait_timeout", "launch_count", "lib",
     "BwattnError", "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_TIMEOUT",
 ]
@@ -62,6 +62,8 @@ def lib() -> ctypes.CDLL:
         L.attn_decode_workspace_size.restype = sz
         L.attn_decode.argtypes = [vp, vp, vp, vp, vp] + [ci] * 6 + [cf, vp, vp, sz, vp]
         L.attn_decode.restype = ci
+        L.attn_decode_paged.argtypes = [vp] * 6 + [ci] * 8 + [cf, vp, vp, sz, vp]
+        L.attn_decode_paged.restype = ci
         L.attn_varlen_workspace_size.argtypes = [ci] * 5
         L.attn_varlen_workspace_size.restype = sz
         L.attn_varlen.argtypes = [vp] * 7 + [ci] * 9 + [cf, vp, sz, vp]
@@ -190,6 +192,43 @@ def attn_decode(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Tensor, nk:
                            int(num_splits), _scale(scale, d), _ptr(lse_t), _ptr(workspace),
                            workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "attn_decode")
+    return out, lse_t
+
+
+def attn_decode_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor, block_table: torch.Tensor,
+                      nk: torch.Tensor, num_splits: int, scale: float | None = None,
+                      workspace: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                      lse: torch.Tensor | bool | None = True, stream=None):
+    """Paged decode. q [B, Hq, d]; pages [num_pages, page_size, Hkv, d]; block_table [B, max_pages]
+    int32 and nk [B] int32 on the device."""
+    if q.dim() != 3 or k_pages.dim() != 4 or block_table.dim() != 2:
+        raise ValueError("q must be [B, Hq, d], pages [num_pages, page_size, Hkv, d], block_table [B, max_pages]")
+    B, Hq, d = q.shape
+    num_pages, page_size, Hkv, dk = k_pages.shape
+    if dk != d or tuple(v_pages.shape) != tuple(k_pages.shape) or block_table.shape[0] != B:
+        raise ValueError("k_pages and v_pages must be [num_pages, page_size, Hkv, d]; block_table [B, max_pages]")
+    for t, n in ((q, "q"), (k_pages, "k_pages"), (v_pages, "v_pages")):
+        _cuda(t, n, torch.bfloat16)
+    _cuda(block_table, "block_table", torch.int32)
+    _cuda(nk, "nk", torch.int32)
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda(out, "out", torch.bfloat16)
+    lse_t = None
+    if lse is True:
+        lse_t = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    elif isinstance(lse, torch.Tensor):
+        lse_t = lse
+        _cuda(lse_t, "lse", torch.float32)
+    need = decode_workspace_size(B, Hq, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _cuda(workspace, "workspace")
+    rc = lib().attn_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(out), _ptr(block_table), _ptr(nk), B, Hq,
+                                 Hkv, page_size, num_pages, block_table.shape[1], d, int(num_splits), _scale(scale, d),
+                                 _ptr(lse_t), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                 _stream(stream))
+    _check(rc, "attn_decode_paged")
     return out, lse_t
 
 

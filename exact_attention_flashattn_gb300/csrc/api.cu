@@ -320,6 +320,68 @@ int attn_decode(const void* q, const void* kcache, const void* vcache, void* o, 
   return BWATTN_OK;
 }
 
+int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages, void* o, const int32_t* block_table,
+                      const int32_t* nk, int B, int Hq, int Hkv, int page_size, int num_pages, int max_pages_per_seq,
+                      int d, int num_splits, float scale, float* lse, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || num_pages <= 0 || max_pages_per_seq <= 0)
+    return BWATTN_ERR_INVALID_ARG;
+  if (page_size < 16 || page_size > 1024 || page_size % 16 != 0) return BWATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || !good_scale(scale) || num_splits < 1 || num_splits > 1024) return BWATTN_ERR_INVALID_ARG;
+  if (B > 65535 || static_cast<int64_t>(max_pages_per_seq) * page_size > 0x7fffffff) return BWATTN_ERR_INVALID_ARG;
+  const int g = Hq / Hkv;
+  if (d != 128 || g > 32 || Hkv > 32767) return BWATTN_ERR_UNSUPPORTED;
+  if (B == 0) return BWATTN_OK;
+  if (!q || !k_pages || !v_pages || !o || !block_table || !nk || !workspace) return BWATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o) || !aligned16(workspace) ||
+      !aligned4(block_table) || !aligned4(nk) || (lse && !aligned4(lse)))
+    return BWATTN_ERR_INVALID_ARG;
+  if (workspace_bytes < bw::splitk_ws_bytes(B * Hkv, num_splits, g, d)) return BWATTN_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  bw::SplitKArgs a{};
+  a.q = static_cast<const uint16_t*>(q);
+  a.k = static_cast<const uint16_t*>(k_pages);
+  a.v = static_cast<const uint16_t*>(v_pages);
+  a.ws = static_cast<float*>(workspace);
+  a.nk = nk;
+  a.num_seqs = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.g = g;
+  a.kv_head_stride = d;
+  a.kv_key_stride = static_cast<int64_t>(Hkv) * d;
+  a.num_splits = num_splits;
+  a.rows_max = g;
+  a.row_groups = (g + 15) / 16;
+  a.small_rows_limit = g;
+  a.ws_o_offset = bw::splitk_o_offset(B * Hkv, num_splits, g);
+  a.scale_log2 = scale * bw::kLog2e;
+  a.block_table = block_table;
+  a.page_size = page_size;
+  a.max_pages = max_pages_per_seq;
+  a.num_pages = num_pages;
+  cudaError_t e;
+  if ((e = bw::launch_splitk(a, st)) != cudaSuccess) return cuda_fail(e);
+  g_launches.fetch_add(1);
+  bw::MergeArgs m{};
+  m.ws = a.ws;
+  m.o = static_cast<uint16_t*>(o);
+  m.lse = lse;
+  m.nk = nk;
+  m.num_seqs = B;
+  m.Hq = Hq;
+  m.Hkv = Hkv;
+  m.g = g;
+  m.num_splits = num_splits;
+  m.rows_max = g;
+  m.small_rows_limit = g;
+  m.total_q = B;
+  m.ws_o_offset = a.ws_o_offset;
+  if ((e = bw::launch_merge(m, st)) != cudaSuccess) return cuda_fail(e);
+  g_launches.fetch_add(1);
+  return BWATTN_OK;
+}
+
 size_t attn_varlen_workspace_size(int num_seqs, int max_seqlen_k, int Hq, int Hkv, int d) {
   if (num_seqs <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || max_seqlen_k < 0) return 0;
   return bw::splitk_ws_bytes(num_seqs * Hkv, varlen_splits(max_seqlen_k), kSmallRowsLimit, d);

@@ -49,6 +49,11 @@ struct SplitKArgs {
   int small_rows_limit;  // varlen: a sequence takes this path iff n_q * g <= this
   size_t ws_o_offset;    // splitk_o_offset(num_seqs * Hkv, num_splits, rows_max)
   float scale_log2;
+  // paged KV cache (decode only) when block_table is non-null: k, v are [num_pages, page_size,
+  // Hkv, D]; key j of sequence b lives in page block_table[b * max_pages + j / page_size],
+  // row j % page_size (page_size a multiple of 16, so a 16-key step never crosses a page)
+  const int32_t* block_table;
+  int page_size, max_pages, num_pages;
 };
 cudaError_t launch_splitk(const SplitKArgs& a, cudaStream_t stream);
 

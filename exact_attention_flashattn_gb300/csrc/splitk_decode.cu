@@ -88,6 +88,13 @@ __device__ __forceinline__ UnitGeom unit_geom(const SplitKArgs& a, int seq, int 
     u.nk = min(max(a.cu_k[seq + 1] - k0, 0), a.total_k - k0);
     u.kv0 = static_cast<int64_t>(k0) * a.kv_key_stride + static_cast<int64_t>(hkv) * a.kv_head_stride;
     u.active = u.nq > 0 && u.nq * a.g <= a.small_rows_limit;
+  } else if (a.block_table) {
+    // paged cache: kv0 is the head's offset inside a page row; pages come from the block table
+    u.tok0 = seq;
+    u.nq = 1;
+    u.nk = min(max(a.nk[seq], 0), a.max_pages * a.page_size);
+    u.kv0 = static_cast<int64_t>(hkv) * a.kv_head_stride;
+    u.active = true;
   } else {
     u.tok0 = seq;
     u.nq = 1;
@@ -98,6 +105,17 @@ __device__ __forceinline__ UnitGeom unit_geom(const SplitKArgs& a, int seq, int 
   return u;
 }
 
+// Element offset of the first key row of the 16-key step starting at key kb (relative to the
+// unit's kv0): contiguous caches step by rows, paged caches look the page up in the block
+// table ("Attention Computation in Practice", PagedAttention's kernel difference).
+template <bool kPaged>
+__device__ __forceinline__ int64_t step_offset(const SplitKArgs& a, int seq, int kb) {
+  if constexpr (!kPaged) return static_cast<int64_t>(kb) * a.kv_key_stride;
+  int page = a.block_table[static_cast<int64_t>(seq) * a.max_pages + kb / a.page_size];
+  page = min(max(page, 0), a.num_pages - 1);  // a bad entry reads a wrong page, never outside the pool
+  return (static_cast<int64_t>(page) * a.page_size + kb % a.page_size) * a.kv_key_stride;
+}
+
 // Workspace: for unit (seq, hkv), split s, row r: ml[2] then o[D] are stored as
 //   ml: ws[((unit * S + s) * rows_max + r) * 2 + {0, 1}]
 //   o : ws[ws_o_offset + ((unit * S + s) * rows_max + r) * D + c]
@@ -105,8 +123,9 @@ __device__ __forceinline__ size_t ws_ml_index(const SplitKArgs& a, int unit, int
   return ((static_cast<size_t>(unit) * a.num_splits + s) * a.rows_max + r) * 2;
 }
 
-// NH = number of 8-row halves of the 16-row MMA tile that carry real rows (1 or 2).
-template <int NH>
+// NH = number of 8-row halves of the 16-row MMA tile that carry real rows (1 or 2);
+// kPaged: keys are gathered page by page through the block table.
+template <int NH, bool kPaged>
 __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(SplitKArgs a) {
   const int split = blockIdx.x;
   const int hkv = blockIdx.y % a.Hkv;
@@ -168,11 +187,12 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
 
   for (int kb = kbeg + warp * kKeysPerStep; kb < kend; kb += kWarps * kKeysPerStep) {
     // ---- loads: K rows kb + nt*8 + gr (chunks t + 4s); V rows kb + {2t, 2t+1, 2t+8, 2t+9}
+    const int64_t so = step_offset<kPaged>(a, seq, kb);
     uint4 kk[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       const int key = kb + nt * 8 + gr;
-      const uint16_t* kr = kbase + static_cast<int64_t>(key) * ks;
+      const uint16_t* kr = kbase + so + static_cast<int64_t>(nt * 8 + gr) * ks;
 #pragma unroll
       for (int s = 0; s < 4; ++s)
         kk[nt][s] = (key < kend) ? ld_stream(kr + 8 * (t + 4 * s)) : make_uint4(0, 0, 0, 0);
@@ -181,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
 #pragma unroll
     for (int x = 0; x < 4; ++x) {
       const int key = kb + 2 * t + (x & 1) + 8 * (x >> 1);
-      const uint16_t* vr = vbase + static_cast<int64_t>(key) * ks;
+      const uint16_t* vr = vbase + so + static_cast<int64_t>(key - kb) * ks;
       va[x] = (key < kend) ? ld_stream(vr + 8 * gr) : make_uint4(0, 0, 0, 0);
       vb[x] = (key < kend) ? ld_stream(vr + 64 + 8 * gr) : make_uint4(0, 0, 0, 0);
     }
@@ -426,10 +446,11 @@ cudaError_t launch_splitk(const SplitKArgs& a, cudaStream_t stream) {
   dim3 grid(a.num_splits, a.Hkv * a.row_groups, a.num_seqs);
   // every row group has at most 8 rows when the sequences' rows (n_q * g) never exceed 8
   const bool half = a.cu_q ? (a.small_rows_limit <= 8) : (a.g <= 8);
+  const bool paged = a.block_table != nullptr;
   if (half)
-    splitk_kernel<1><<<grid, kThreads, 0, stream>>>(a);
+    paged ? splitk_kernel<1, true><<<grid, kThreads, 0, stream>>>(a) : splitk_kernel<1, false><<<grid, kThreads, 0, stream>>>(a);
   else
-    splitk_kernel<2><<<grid, kThreads, 0, stream>>>(a);
+    paged ? splitk_kernel<2, true><<<grid, kThreads, 0, stream>>>(a) : splitk_kernel<2, false><<<grid, kThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

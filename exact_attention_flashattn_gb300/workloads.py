@@ -19,6 +19,8 @@ Workloads (names give their sizes):
 * ``decode_long_b1_h64x8_n262144_d128``: single-query decode, B=1, 64 query heads over 8 KV
   heads, cache length 262144, bf16 N(0, 1) keys and values times a per-channel scale
   c[Hkv, d] ~ U(0.5, 2) (separate draws for K and V), 128 KV splits.
+* ``decode_paged_b8_h32x8_n32768_d128_p16``: the GQA decode workload with its caches scattered
+  into 16-token pages in a seeded random order, read through a block table.
 * ``varlen_append_64seq_h32x8_d128``: 64 sequences with KV length ~ U[1024, 16384] and new
   query count uniform over {1, 4, 8, 512}, packed with cu_seqlens, 32 query heads over 8
   KV heads, d = 128, bf16 N(0, 1), causal aligned to each sequence's end.
@@ -72,6 +74,10 @@ WORKLOADS = {
                                                   torch.bfloat16, B=1, Hq=64, Hkv=8, Nq=1, Nk=262144, d=128,
                                                   causal=False, num_splits=128, seed=SEED_DECODE_LONG,
                                                   channel_scale=True),
+    "decode_paged_b8_h32x8_n32768_d128_p16": Workload("decode_paged_b8_h32x8_n32768_d128_p16", "decode_paged",
+                                                      torch.bfloat16, B=8, Hq=32, Hkv=8, Nq=1, Nk=32768, d=128,
+                                                      causal=False, num_splits=16, seed=SEED_DECODE,
+                                                      extra={"page_size": 16}),
     "varlen_append_64seq_h32x8_d128": Workload("varlen_append_64seq_h32x8_d128", "varlen", torch.bfloat16,
                                                Hq=32, Hkv=8, d=128, causal=True, seed=SEED_VARLEN,
                                                num_seqs=64, nk_range=(1024, 16384)),
@@ -136,6 +142,31 @@ def decode_inputs(B, Hq, Hkv, cap, d, dtype, seed, nk=None, channel_scale=False,
     return q, kc, vc, nk
 
 
+def paged_from_dense(kcache, vcache, page_size, seed):
+    """Scatter contiguous caches [B, Hkv, cap, d] into a shuffled page pool.
+
+    Returns k_pages, v_pages [B * cap / page_size, page_size, Hkv, d] and block_table
+    [B, cap / page_size] int32 (on the caches' device) such that key j of sequence b is row
+    j % page_size of page block_table[b, j // page_size]. The page order is a seeded random
+    permutation, so consecutive keys of a sequence are scattered over the pool.
+    """
+    B, Hkv, cap, d = kcache.shape
+    if cap % page_size:
+        raise ValueError("cache length must be a multiple of page_size")
+    npg = cap // page_size
+    g = _gen(seed + 104729)
+    perm = torch.randperm(B * npg, generator=g).to(kcache.device)
+
+    def scatter(c):
+        pages = c.view(B, Hkv, npg, page_size, d).permute(0, 2, 3, 1, 4).reshape(B * npg, page_size, Hkv, d)
+        out = torch.empty_like(pages)
+        out[perm] = pages
+        return out
+
+    table = perm.view(B, npg).to(torch.int32)
+    return scatter(kcache), scatter(vcache), table
+
+
 def varlen_lengths(num_seqs, seed, nk_range=(1024, 16384), nq_choices=VARLEN_NQ_CHOICES):
     """Per-sequence (n_q, n_k): n_k ~ U[lo, hi] (inclusive integers), n_q uniform over
     ``nq_choices``; n_q never exceeds n_k (the KV length includes the new tokens)."""
@@ -171,10 +202,14 @@ def make(name: str, device="cpu"):
     if w.kind == "fwd":
         q, k, v = prefill_inputs(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.dtype, w.seed, device)
         return {"q": q, "k": k, "v": v, "w": w}
-    if w.kind == "decode":
+    if w.kind in ("decode", "decode_paged"):
         q, kc, vc, nk = decode_inputs(w.B, w.Hq, w.Hkv, w.Nk, w.d, w.dtype, w.seed,
                                       channel_scale=w.channel_scale, device=device)
-        return {"q": q, "kcache": kc, "vcache": vc, "nk": nk, "w": w}
+        if w.kind == "decode":
+            return {"q": q, "kcache": kc, "vcache": vc, "nk": nk, "w": w}
+        kp, vp, table = paged_from_dense(kc, vc, w.extra["page_size"], w.seed)
+        del kc, vc
+        return {"q": q, "k_pages": kp, "v_pages": vp, "block_table": table, "nk": nk, "w": w}
     nq_list, nk_list = varlen_lengths(w.num_seqs, w.seed, w.nk_range)
     q, k, v, cq, ck = varlen_inputs(nq_list, nk_list, w.Hq, w.Hkv, w.d, w.dtype, w.seed, device)
     return {"q": q, "k": k, "v": v, "cu_q": cq, "cu_k": ck, "nq": nq_list, "nk": nk_list, "w": w}

@@ -105,6 +105,30 @@ int attn_decode(const void* q, const void* kcache, const void* vcache, void* o, 
                 size_t workspace_bytes, void* stream);
 
 /*
+ * attn_decode_paged: single-query decode against a paged KV cache: the cache is a pool of
+ * fixed-size pages and a per-sequence block table lists which page holds each run of
+ * page_size consecutive keys. ("Attention Computation in Practice", "PagedAttention's kernel
+ * difference": block_table[b] = [17, 3, 92, ...], read block 17, then 3, ...; the kernel takes
+ * the table as an argument and gathers.) Same split-K pass and merge as attn_decode.
+ *
+ *   q, o        : [B, Hq, d] bf16
+ *   k_pages,
+ *   v_pages     : [num_pages, page_size, Hkv, d] bf16 (a page holds page_size consecutive keys
+ *                 of every KV head)
+ *   block_table : [B, max_pages_per_seq] int32 DEVICE array; key j of sequence b is row
+ *                 j % page_size of page block_table[b][j / page_size]. Entries outside
+ *                 [0, num_pages) are clamped into the pool (wrong data, never an out-of-bounds read)
+ *   nk          : [B] int32 DEVICE array, 0 <= nk[b] <= max_pages_per_seq * page_size
+ *   page_size   : a multiple of 16, 16..1024
+ *   workspace   : at least attn_decode_workspace_size(B, Hq, d, num_splits) bytes
+ * Supported: d = 128, 1 <= g <= 32. Errors as for attn_decode.
+ */
+int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages, void* o, const int32_t* block_table,
+                      const int32_t* nk, int B, int Hq, int Hkv, int page_size, int num_pages, int max_pages_per_seq,
+                      int d, int num_splits, float scale, float* lse, void* workspace, size_t workspace_bytes,
+                      void* stream);
+
+/*
  * attn_decode_static: the same single-query split-K decode as attn_decode, for callers that
  * cannot allocate device memory. The pages have no counterpart to this entry point; it exists
  * for deployment. Some callers cannot call cudaMalloc or hand the library a workspace: a

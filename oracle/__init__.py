@@ -146,6 +146,21 @@ def decode(q, kcache, vcache, nk, scale: float | None = None, method: str = "spl
     return o, lse
 
 
+def decode_paged(q, k_pages, v_pages, block_table, nk, scale: float | None = None, method: str = "splitk",
+                 workers: int | None = None, block: int | None = None, nthreads: int = 0):
+    """Paged decode ("Attention Computation in Practice", PagedAttention's kernel difference):
+    pages [num_pages, page_size, Hkv, d], block_table [B, max_pages]. Key j of sequence b is row
+    j % page_size of page block_table[b][j // page_size]; the keys are gathered into contiguous
+    caches [B, Hkv, max_pages * page_size, d] (data movement only) and passed to ``decode``."""
+    kp, vp = _f64(k_pages), _f64(v_pages)
+    table = np.asarray(block_table, dtype=np.int64)
+    num_pages, ps, Hkv, d = kp.shape
+    B, mp = table.shape
+    kc = kp[table].reshape(B, mp * ps, Hkv, d).transpose(0, 2, 1, 3)
+    vc = vp[table].reshape(B, mp * ps, Hkv, d).transpose(0, 2, 1, 3)
+    return decode(q, kc, vc, nk, scale=scale, method=method, workers=workers, block=block, nthreads=nthreads)
+
+
 def varlen(q, k, v, cu_q, cu_k, causal: bool, scale: float | None = None, method: str = "tiled",
            block: int | None = None, workers: int | None = None, nthreads: int = 0):
     """Packed: q [total_q, Hq, d]; k, v [total_k, Hkv, d] -> (o [total_q, Hq, d], lse [total_q, Hq])."""

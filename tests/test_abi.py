@@ -28,7 +28,7 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ("attn_fwd", "attn_decode", "attn_varlen", "attn_decode_workspace_size", "attn_varlen_workspace_size",
+    for n in ("attn_fwd", "attn_decode", "attn_decode_paged", "attn_varlen", "attn_decode_workspace_size", "attn_varlen_workspace_size",
               "bwattn_get_status", "bwattn_clear_status", "bwattn_last_cuda_error", "bwattn_status_string",
               "bwattn_set_wait_timeout_ns", "bwattn_test_wait_timeout", "bwattn_launch_count", "bwattn_version"):
         assert n in names
@@ -118,3 +118,21 @@ def test_python_binding_rejects_host_tensors():
     q = torch.zeros(1, 1, 8, 64)
     with pytest.raises(ValueError):
         bw.attn_fwd(q, q, q)
+
+
+def test_paged_decode_argument_errors(L):
+    def pag(**kw):
+        a = dict(q=FAKE, kp=FAKE, vp=FAKE, o=FAKE, table=FAKE, nk=FAKE, B=2, Hq=8, Hkv=2, ps=16, npages=64, mp=8,
+                 d=128, S=4, scale=0.1, lse=None, ws=FAKE, wsb=1 << 30, stream=None)
+        a.update(kw)
+        return L.attn_decode_paged(a["q"], a["kp"], a["vp"], a["o"], a["table"], a["nk"], a["B"], a["Hq"], a["Hkv"],
+                                   a["ps"], a["npages"], a["mp"], a["d"], a["S"], a["scale"], a["lse"], a["ws"],
+                                   a["wsb"], a["stream"])
+    assert pag(table=None) == bw.ERR_INVALID_ARG
+    assert pag(ps=8) == bw.ERR_INVALID_ARG
+    assert pag(ps=24) == bw.ERR_INVALID_ARG
+    assert pag(npages=0) == bw.ERR_INVALID_ARG
+    assert pag(table=FAKE + 2) == bw.ERR_INVALID_ARG
+    assert pag(wsb=16) == bw.ERR_INVALID_ARG
+    assert pag(d=64) == bw.ERR_UNSUPPORTED
+    assert pag(B=0, q=None) == bw.OK

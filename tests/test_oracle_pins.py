@@ -402,3 +402,23 @@ def test_lse_matches_scipy_logsumexp():
     for h in range(2):
         for i in range(25):
             assert abs(lse[0, h, i] - logsumexp(s[0, h, i, :i + 1])) <= 1e-12
+
+
+def test_paged_decode_gathers_the_same_keys():
+    # scattering a contiguous cache into shuffled pages and reading it back through the block
+    # table must reproduce the contiguous decode exactly ("Attention Computation in Practice",
+    # PagedAttention's kernel difference)
+    from exact_attention_flashattn_gb300 import workloads as wl
+    q, kc, vc, nk = wl.decode_inputs(3, 8, 2, 64, 16, torch.float32, seed=61, nk=[64, 17, 30])
+    kp, vp, table = wl.paged_from_dense(kc, vc, 16, seed=61)
+    assert sorted(table.flatten().tolist()) == list(range(3 * 4))
+    o1, l1 = oracle.decode(q.numpy(), kc.numpy(), vc.numpy(), nk.numpy(), method="splitk", workers=3)
+    o2, l2 = oracle.decode_paged(q.numpy(), kp.numpy(), vp.numpy(), table.numpy(), nk.numpy(), method="splitk",
+                                 workers=3)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    # and a page that the table never references does not matter
+    kp2 = kp.clone()
+    kp2[int(table[1, 3])] = float("nan")  # sequence 1 has 17 keys: pages 0 and 1 only
+    o3, _ = oracle.decode_paged(q.numpy(), kp2.numpy(), vp.numpy(), table.numpy(), nk.numpy(), method="splitk",
+                                workers=3)
+    assert np.array_equal(o1, o3)

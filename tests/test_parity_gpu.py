@@ -195,6 +195,59 @@ def test_decode_workloads_full_size(name):
         check_bf16(o[b:b + 1], o_ref, lse[b:b + 1], lse_ref, what=(name, b))
 
 
+# ------------------------------------------------------------------ paged decode
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,cap,nk,S,ps", [
+    (3, 8, 2, 256, [256, 17, 0], 4, 16),    # 16-token pages, ragged lengths, an empty sequence
+    (2, 16, 2, 512, [512, 300], 9, 32),     # g = 8, 32-token pages
+    (1, 32, 1, 128, [128], 2, 64),          # g = 32: two row groups
+])
+def test_decode_paged(B, Hq, Hkv, cap, nk, S, ps):
+    q, kc, vc, nkt = wl.decode_inputs(B, Hq, Hkv, cap, 128, torch.bfloat16, seed=81 + cap, nk=nk)
+    kp, vp, table = wl.paged_from_dense(kc, vc, ps, seed=81)
+    o_ref, lse_ref = oracle.decode_paged(f64(q), f64(kp), f64(vp), table.numpy(), nkt.numpy(), method="splitk",
+                                         workers=S)
+    o, lse = bw.attn_decode_paged(q.cuda(), kp.cuda(), vp.cuda(), table.cuda(), nkt.cuda(), num_splits=S)
+    torch.cuda.synchronize()
+    check_bf16(o, o_ref, lse, lse_ref, what=("paged", B, Hq, Hkv, cap, nk, S, ps))
+
+
+def test_decode_paged_matches_contiguous_bit_for_bit_and_skips_unused_pages():
+    q, kc, vc, nkt = wl.decode_inputs(4, 32, 8, 1024, 128, torch.bfloat16, seed=83, nk=[1024, 1000, 517, 16])
+    q, kc, vc, nkt = q.cuda(), kc.cuda(), vc.cuda(), nkt.cuda()
+    kp, vp, table = wl.paged_from_dense(kc, vc, 16, seed=83)
+    o1, l1 = bw.attn_decode(q, kc, vc, nkt, num_splits=8)
+    o2, l2 = bw.attn_decode_paged(q, kp, vp, table, nkt, num_splits=8)
+    # pages past each sequence's length are never read
+    kp2, vp2 = kp.clone(), vp.clone()
+    for b, n in enumerate([1024, 1000, 517, 16]):
+        for j in range((n + 15) // 16, 1024 // 16):
+            kp2[int(table[b, j])] = float("nan")
+            vp2[int(table[b, j])] = float("nan")
+    o3, l3 = bw.attn_decode_paged(q, kp2, vp2, table, nkt, num_splits=8)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert torch.equal(o1, o3) and torch.equal(l1, l3)
+
+
+def test_decode_paged_workload_full_size():
+    x = wl.make("decode_paged_b8_h32x8_n32768_d128_p16", device="cuda")
+    w = x["w"]
+    o, lse = bw.attn_decode_paged(x["q"], x["k_pages"], x["v_pages"], x["block_table"], x["nk"].cuda(),
+                                  num_splits=w.num_splits)
+    torch.cuda.synchronize()
+    b = w.B - 1
+    tb = x["block_table"][b:b + 1].cpu()
+    used = tb.flatten().long()
+    kp = x["k_pages"].index_select(0, used.cuda())
+    vp = x["v_pages"].index_select(0, used.cuda())
+    local = torch.arange(used.numel(), dtype=torch.int32).view(1, -1)
+    o_ref, lse_ref = oracle.decode_paged(f64(x["q"][b:b + 1]), f64(kp), f64(vp), local.numpy(), [w.Nk],
+                                         method="splitk", workers=w.num_splits)
+    check_bf16(o[b:b + 1], o_ref, lse[b:b + 1], lse_ref, what="paged full size")
+
+
 # ------------------------------------------------------------------ varlen
 
 
