@@ -394,7 +394,7 @@ def main():
                                "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
                                             "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
                                             "algorithmic_bytes": kvb, "traffic": None,
-                                            "note": "split-K pass + merge, two launches, timed together"}}
+                                            "note": "split-K pass with the merge fused into the last CTA of each unit"}}
             del xd, od, ld, wsd, nk
             torch.cuda.empty_cache()
         xp = wl.make("decode_paged_b8_h32x8_n32768_d128_p16", device=dev)
@@ -413,7 +413,7 @@ def main():
                               "ms_per_step": msp, "num_splits": wp.num_splits, "page_size": wp.extra["page_size"],
                               "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                            "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": kvb,
-                                           "traffic": None, "note": "paged split-K pass + merge, two launches"}}
+                                           "traffic": None, "note": "paged split-K pass with the fused merge"}}
         del xp, wsp, op, lp, nkp
         torch.cuda.empty_cache()
         xv = wl.make("varlen_append_64seq_h32x8_d128", device=dev)

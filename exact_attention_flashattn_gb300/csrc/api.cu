@@ -22,6 +22,16 @@ constexpr int kSchedSlots = 4096;
 __device__ unsigned int g_sched_counters[2 * kSchedSlots];
 std::atomic<uint32_t> g_sched_next{0};
 
+// Merge tickets of the split-K kernel: each launch takes a contiguous block (zeroed, and left
+// zeroed by the kernel) from this ring; the ring holds 2^16 tickets, so blocks are reused only
+// after many later launches.
+constexpr uint32_t kTicketSlots = 1u << 16;
+// With more splits than this the separate merge kernel (one CTA per output row) is faster than
+// letting one CTA per unit walk all the splits.
+constexpr int kFusedMergeMaxSplits = 32;
+__device__ unsigned int g_merge_tickets[kTicketSlots];
+uint32_t g_ticket_next = 0;
+
 thread_local int t_last_cuda_error = 0;
 std::atomic<uint64_t> g_launches{0};
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
@@ -30,6 +40,7 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 unsigned int* g_status_ptr[kMaxDevices] = {};
 unsigned int* g_sched_ptr[kMaxDevices] = {};
+unsigned int* g_ticket_ptr[kMaxDevices] = {};
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -132,6 +143,27 @@ int varlen_splits(int max_seqlen_k) {
 namespace bw {
 void record_cuda_error(cudaError_t e) { t_last_cuda_error = static_cast<int>(e); }
 void count_launch() { g_launches.fetch_add(1); }
+
+cudaError_t merge_tickets(int n, unsigned int** out) {
+  *out = nullptr;
+  if (n <= 0 || static_cast<uint32_t>(n) > kTicketSlots / 16) return cudaSuccess;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_ticket_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_merge_tickets);
+    if (e != cudaSuccess) return e;
+    g_ticket_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  uint32_t pos = g_ticket_next;
+  if (pos + static_cast<uint32_t>(n) > kTicketSlots) pos = 0;
+  g_ticket_next = pos + static_cast<uint32_t>(n);
+  *out = g_ticket_ptr[dev] + pos;
+  return cudaSuccess;
+}
 }  // namespace bw
 
 extern "C" {
@@ -298,8 +330,14 @@ int attn_decode(const void* q, const void* kcache, const void* vcache, void* o, 
   a.ws_o_offset = bw::splitk_o_offset(B * Hkv, num_splits, g);
   a.scale_log2 = sl2;
   cudaError_t e;
+  if (num_splits <= kFusedMergeMaxSplits &&
+      (e = bw::merge_tickets(B * Hkv * a.row_groups, &a.tickets)) != cudaSuccess)
+    return cuda_fail(e);
+  a.o = static_cast<uint16_t*>(o);
+  a.lse = lse;
   if ((e = bw::launch_splitk(a, st)) != cudaSuccess) return cuda_fail(e);
   g_launches.fetch_add(1);
+  if (a.tickets) return BWATTN_OK;  // merged by the last CTA of each unit
   bw::MergeArgs m{};
   m.ws = a.ws;
   m.o = static_cast<uint16_t*>(o);
@@ -361,8 +399,14 @@ int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages, v
   a.max_pages = max_pages_per_seq;
   a.num_pages = num_pages;
   cudaError_t e;
+  if (num_splits <= kFusedMergeMaxSplits &&
+      (e = bw::merge_tickets(B * Hkv * a.row_groups, &a.tickets)) != cudaSuccess)
+    return cuda_fail(e);
+  a.o = static_cast<uint16_t*>(o);
+  a.lse = lse;
   if ((e = bw::launch_splitk(a, st)) != cudaSuccess) return cuda_fail(e);
   g_launches.fetch_add(1);
+  if (a.tickets) return BWATTN_OK;  // merged by the last CTA of each unit
   bw::MergeArgs m{};
   m.ws = a.ws;
   m.o = static_cast<uint16_t*>(o);
@@ -472,8 +516,13 @@ int attn_varlen(const void* q, const void* k, const void* v, void* o, float* lse
   s.small_rows_limit = kSmallRowsLimit;
   s.ws_o_offset = bw::splitk_o_offset(units, splits, kSmallRowsLimit);
   s.scale_log2 = sl2;
+  if (splits <= kFusedMergeMaxSplits && (e = bw::merge_tickets(units * s.row_groups, &s.tickets)) != cudaSuccess)
+    return cuda_fail(e);
+  s.o = static_cast<uint16_t*>(o);
+  s.lse = lse;
   if ((e = bw::launch_splitk(s, st)) != cudaSuccess) return cuda_fail(e);
   g_launches.fetch_add(1);
+  if (s.tickets) return BWATTN_OK;  // merged by the last CTA of each unit
   bw::MergeArgs m{};
   m.ws = s.ws;
   m.o = static_cast<uint16_t*>(o);

@@ -54,6 +54,11 @@ struct SplitKArgs {
   // row j % page_size (page_size a multiple of 16, so a 16-key step never crosses a page)
   const int32_t* block_table;
   int page_size, max_pages, num_pages;
+  // fused merge when tickets is non-null: units * row_groups zeroed counters owned by this
+  // launch (left zeroed again); the last CTA of each (unit, row group) writes o and lse
+  unsigned int* tickets;
+  uint16_t* o;
+  float* lse;
 };
 cudaError_t launch_splitk(const SplitKArgs& a, cudaStream_t stream);
 
@@ -95,6 +100,9 @@ cudaError_t launch_wait_timeout_probe(uint64_t timeout_ns, unsigned int* status,
 // bwattn_last_cuda_error(), count a successful launch for bwattn_launch_count().
 void record_cuda_error(cudaError_t e);
 void count_launch();
+// `n` zeroed merge tickets on the current device for one launch of the split-K kernel (null
+// when the request exceeds the ticket pool: the caller then launches the merge kernel).
+cudaError_t merge_tickets(int n, unsigned int** out);
 
 // Float offset of the o[] block of the split-K workspace (after the (m, l) pairs, 256-byte aligned).
 inline size_t splitk_o_offset(int units, int num_splits, int rows_max) {

@@ -357,6 +357,67 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
       a.ws[mi + 1] = L;
     }
   }
+  if (!a.tickets) return;  // the separate merge kernel combines the splits
+
+  // ---- the last CTA of this (unit, row group) to finish merges all its splits' partials
+  // (the two-state merge rule over the splits), then resets the ticket for the next call
+  __shared__ unsigned int sm_last;
+  __syncthreads();
+  unsigned int* ticket = a.tickets + static_cast<size_t>(unit) * a.row_groups + grp;
+  if (threadIdx.x == 0) {
+    __threadfence();  // this CTA's partials are visible before its ticket is counted
+    sm_last = (atomicAdd(ticket, 1u) == static_cast<unsigned int>(a.num_splits - 1)) ? 1u : 0u;
+  }
+  __syncthreads();
+  if (!sm_last) return;
+  __threadfence();  // every other split's partials are visible from here on
+  const size_t ml_stride = static_cast<size_t>(a.rows_max) * 2;
+  const size_t o_stride = static_cast<size_t>(a.rows_max) * D;
+  for (int it = threadIdx.x; it < 8 * NH * (D / 4); it += kThreads) {
+    const int r = it / (D / 4);
+    const int c4 = it % (D / 4);
+    if (r >= nrows) continue;
+    const float* ml = a.ws + ws_ml_index(a, unit, 0, row0 + r);
+    const float* wo = ws_o + (ws_ml_index(a, unit, 0, row0 + r) / 2) * D + 4 * c4;
+    float M = -INFINITY;
+    for (int sp = 0; sp < a.num_splits; ++sp) {
+      const float2 v = __ldcg(reinterpret_cast<const float2*>(ml + sp * ml_stride));
+      if (v.y > 0.f) M = fmaxf(M, v.x);
+    }
+    // empty partials hold l = 0 and o = 0: their weight is taken as 0, and their loads are
+    // issued with the others (four splits at a time) rather than behind a branch
+    float L = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sp0 = 0; sp0 < a.num_splits; sp0 += 4) {
+      float2 v[4];
+      float4 x[4];
+#pragma unroll
+      for (int u4 = 0; u4 < 4; ++u4) {
+        const int sp = min(sp0 + u4, a.num_splits - 1);
+        v[u4] = __ldcg(reinterpret_cast<const float2*>(ml + sp * ml_stride));
+        x[u4] = __ldcg(reinterpret_cast<const float4*>(wo + sp * o_stride));
+      }
+#pragma unroll
+      for (int u4 = 0; u4 < 4; ++u4) {
+        const float f = (sp0 + u4 < a.num_splits && v[u4].y > 0.f) ? ex2(v[u4].x - M) : 0.f;
+        L += f * v[u4].y;
+        o.x += f * x[u4].x;
+        o.y += f * x[u4].y;
+        o.z += f * x[u4].z;
+        o.w += f * x[u4].w;
+      }
+    }
+    const int rr = row0 + r;
+    const int i = rr / a.g, hh = rr % a.g;
+    const int64_t orow = static_cast<int64_t>(u.tok0 + i) * a.Hq + hkv * a.g + hh;
+    const float inv = (L > 0.f) ? 1.f / L : 0.f;
+    uint2 packed;
+    packed.x = pack_bf16x2(o.x * inv, o.y * inv);
+    packed.y = pack_bf16x2(o.z * inv, o.w * inv);
+    *reinterpret_cast<uint2*>(a.o + orow * D + 4 * c4) = packed;
+    if (a.lse && c4 == 0) a.lse[orow] = (L > 0.f) ? (M + log2f(L)) * kLn2 : -INFINITY;
+  }
+  if (threadIdx.x == 0) *ticket = 0u;  // no other CTA touches this ticket in this call
 }
 
 // One CTA per output row: merge the num_splits partials of (unit, row). The global max comes
