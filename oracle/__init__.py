@@ -63,9 +63,9 @@ def _load():
         D = ctypes.POINTER(ctypes.c_double)
         I32 = ctypes.POINTER(ctypes.c_int32)
         c_int, c_double = ctypes.c_int, ctypes.c_double
-        lib.oracle_attention.argtypes = [D, D, D, D, D] + [c_int] * 7 + [c_double] + [c_int] * 3
+        lib.oracle_attention.argtypes = [D, D, D, D, D] + [c_int] * 7 + [c_double] + [c_int] * 4
         lib.oracle_decode.argtypes = [D, D, D, I32, D, D] + [c_int] * 5 + [c_double] + [c_int] * 3
-        lib.oracle_varlen.argtypes = [D, D, D, I32, I32, D, D] + [c_int] * 5 + [c_double] + [c_int] * 3
+        lib.oracle_varlen.argtypes = [D, D, D, I32, I32, D, D] + [c_int] * 5 + [c_double] + [c_int] * 4
         lib.oracle_probs.argtypes = [D, D, D, c_int, c_int, c_int, c_int, c_double]
         lib.oracle_partials.argtypes = [D, D, D, c_int, c_int, c_double, c_int, D, D, D]
         lib.oracle_merge.argtypes = [c_double, c_double, D, c_double, c_double, D, c_int, D, D, D]
@@ -108,10 +108,12 @@ def hardware_threads() -> int:
 
 
 def attention(q, k, v, causal: bool, scale: float | None = None, method: str = "tiled",
-              block: int | None = None, workers: int | None = None, nthreads: int = 0):
+              block: int | None = None, workers: int | None = None, nthreads: int = 0, window: int = 0):
     """Dense layout: q [B, Hq, Nq, d]; k, v [B, Hkv, Nk, d] -> (o [B, Hq, Nq, d], lse [B, Hq, Nq]).
 
-    Causal masking is aligned to the end of the key sequence when Nq != Nk.
+    Causal masking is aligned to the end of the key sequence when Nq != Nk. ``window`` > 0 adds a
+    sliding window ("Attention Computation in Practice", Masking variants): query i sees keys
+    i' - window < j <= i' with i' = i + (Nk - Nq).
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, Hq, Nq, d = q.shape
@@ -122,7 +124,7 @@ def attention(q, k, v, causal: bool, scale: float | None = None, method: str = "
     lse = np.zeros((B, Hq, Nq), dtype=np.float64)
     m, p = _method(method, block, workers)
     rc = _load().oracle_attention(_dp(q), _dp(k), _dp(v), _dp(o), _dp(lse), B, Hq, Hkv, Nq, Nk, d,
-                                  int(bool(causal)), float(scale), m, p, int(nthreads))
+                                  int(bool(causal)), float(scale), m, p, int(nthreads), int(window))
     if rc != 0:
         raise ValueError(f"oracle_attention rejected its arguments (rc={rc})")
     return o, lse
@@ -162,7 +164,7 @@ def decode_paged(q, k_pages, v_pages, block_table, nk, scale: float | None = Non
 
 
 def varlen(q, k, v, cu_q, cu_k, causal: bool, scale: float | None = None, method: str = "tiled",
-           block: int | None = None, workers: int | None = None, nthreads: int = 0):
+           block: int | None = None, workers: int | None = None, nthreads: int = 0, window: int = 0):
     """Packed: q [total_q, Hq, d]; k, v [total_k, Hkv, d] -> (o [total_q, Hq, d], lse [total_q, Hq])."""
     q, k, v, cu_q, cu_k = _f64(q), _f64(k), _f64(v), _i32(cu_q), _i32(cu_k)
     tq, Hq, d = q.shape
@@ -174,7 +176,7 @@ def varlen(q, k, v, cu_q, cu_k, causal: bool, scale: float | None = None, method
     m, p = _method(method, block, workers)
     rc = _load().oracle_varlen(_dp(q), _dp(k), _dp(v), _ip(cu_q), _ip(cu_k), _dp(o), _dp(lse),
                                len(cu_q) - 1, Hq, Hkv, d, int(bool(causal)), float(scale), m, p,
-                               int(nthreads))
+                               int(nthreads), int(window))
     if rc != 0:
         raise ValueError(f"oracle_varlen rejected its arguments (rc={rc})")
     return o, lse

@@ -34,6 +34,9 @@
 //     (the guard in [P4] Code), and a partial with l == 0 contributes nothing to a merge.
 //     A row with no visible key returns O = 0 and LSE = -inf.
 //   * causal with Nq != Nk is aligned to the end: query i sees key j iff j <= i + (Nk - Nq).
+//   * sliding window W ([P3] Masking variants, i - W < j <= i) is applied on top of the causal
+//     mask with the same end alignment: query i sees keys i' - W < j <= i', i' = i + (Nk - Nq);
+//     W <= 0 means no window.
 //   * split-K slice w covers keys [w*c, min((w+1)*c, n)) with c = ceil(n / W) over the n
 //     visible keys of the row; slices past the end are empty.
 //   * GQA: query head h reads KV head floor(h / (Hq / Hkv)) ([P3] GQA in the kernel).
@@ -55,9 +58,10 @@ struct RowJob {
   const double* k;    // first key row; row j at k + j * kv_stride
   const double* v;    // first value row; row j at v + j * kv_stride
   int64_t kv_stride;  // elements between consecutive key (and value) rows
-  int n_vis;          // keys [0, n_vis) are visible to this query
+  int n_vis;          // keys [k_begin, n_vis) are visible to this query
   double* o;          // [d] output
   double* lse;        // nullable
+  int k_begin;        // first visible key (a sliding window starts past 0)
 };
 
 // Running state of the online softmax: max m, sum l, unnormalised output o.
@@ -130,7 +134,8 @@ void finish(const State& st, const RowJob& r, int d) {
 // Algorithm 0 for one row: the score row is materialised, then softmax, then P.V.
 // [P4] Concept (three steps); [P3] section 4, naive; safe softmax from [P1].
 void naive_row(const RowJob& r, int d, double scale) {
-  const int n = r.n_vis;
+  const int j0 = r.k_begin;
+  const int n = r.n_vis - j0;
   if (n <= 0) {
     for (int c = 0; c < d; ++c) r.o[c] = 0.0;
     if (r.lse) *r.lse = kNegInf;
@@ -139,7 +144,7 @@ void naive_row(const RowJob& r, int d, double scale) {
   std::vector<double> s(n);
   double mx = kNegInf;
   for (int j = 0; j < n; ++j) {
-    s[j] = scale * dot(r.q, r.k + j * r.kv_stride, d);
+    s[j] = scale * dot(r.q, r.k + (j0 + j) * r.kv_stride, d);
     mx = std::max(mx, s[j]);
   }
   double sum = 0.0;
@@ -150,7 +155,7 @@ void naive_row(const RowJob& r, int d, double scale) {
   for (int c = 0; c < d; ++c) r.o[c] = 0.0;
   for (int j = 0; j < n; ++j) {
     const double p = s[j] / sum;
-    const double* vj = r.v + j * r.kv_stride;
+    const double* vj = r.v + (j0 + j) * r.kv_stride;
     for (int c = 0; c < d; ++c) r.o[c] += p * vj[c];
   }
   if (r.lse) *r.lse = mx + std::log(sum);
@@ -159,21 +164,22 @@ void naive_row(const RowJob& r, int d, double scale) {
 // Tiled: key tiles [t*block, (t+1)*block) clipped to the visible range, in key order.
 void tiled_row(const RowJob& r, int d, double scale, int block) {
   State st(d);
-  for (int j0 = 0; j0 < r.n_vis; j0 += block) fold_tile(st, r, j0, std::min(j0 + block, r.n_vis), d, scale);
+  for (int j0 = r.k_begin / block * block; j0 < r.n_vis; j0 += block)
+    fold_tile(st, r, std::max(j0, r.k_begin), std::min(j0 + block, r.n_vis), d, scale);
   finish(st, r, d);
 }
 
 // Split-K: W slices of c = ceil(n/W) keys, each folded as one tile into its own partial,
 // merged left to right.
 void splitk_partials(const RowJob& r, int d, double scale, int workers, std::vector<State>& parts) {
-  const int n = r.n_vis;
+  const int n = r.n_vis - r.k_begin;
   parts.assign(workers, State(d));
   if (n <= 0) return;
   const int chunk = (n + workers - 1) / workers;
   for (int w = 0; w < workers; ++w) {
     const int j0 = std::min(n, w * chunk);
     const int j1 = std::min(n, j0 + chunk);
-    fold_tile(parts[w], r, j0, j1, d, scale);
+    fold_tile(parts[w], r, r.k_begin + j0, r.k_begin + j1, d, scale);
   }
 }
 
@@ -221,15 +227,23 @@ int visible_keys(int i, int nq, int nk, int causal) {
   return static_cast<int>(std::max(0L, std::min<long>(lim, nk)));
 }
 
+// First visible key under a sliding window of W keys ending at the causal limit (W <= 0: none).
+int first_visible_key(int i, int nq, int nk, int causal, int window) {
+  if (!causal || window <= 0) return 0;
+  const long lo = static_cast<long>(i) + (nk - nq) + 1 - window;
+  return static_cast<int>(std::max(0L, std::min<long>(lo, nk)));
+}
+
 }  // namespace
 
 extern "C" {
 
 // Dense layout: q, o [B, Hq, Nq, d]; k, v [B, Hkv, Nk, d]; lse [B, Hq, Nq] (nullable).
 // method 0 naive, 1 tiled(param = block), 2 split-K(param = workers). nthreads 0 = all cores.
+// window > 0 (with causal): sliding window of that many keys.
 int oracle_attention(const double* q, const double* k, const double* v, double* o, double* lse,
                      int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, double scale,
-                     int method, int param, int nthreads) {
+                     int method, int param, int nthreads, int window) {
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Nq < 0 || Nk < 0 || d <= 0 || Hq % Hkv) return 1;
   const int g = Hq / Hkv;
   std::vector<RowJob> jobs;
@@ -242,7 +256,7 @@ int oracle_attention(const double* q, const double* k, const double* v, double* 
       for (int i = 0; i < Nq; ++i) {
         const int64_t row = (static_cast<int64_t>(b) * Hq + h) * Nq + i;
         jobs.push_back(RowJob{q + row * d, kb, vb, d, visible_keys(i, Nq, Nk, causal), o + row * d,
-                              lse ? lse + row : nullptr});
+                              lse ? lse + row : nullptr, first_visible_key(i, Nq, Nk, causal, window)});
       }
     }
   return run_rows(jobs, d, scale, method, param, nthreads);
@@ -264,7 +278,7 @@ int oracle_decode(const double* q, const double* kc, const double* vc, const int
       const int64_t row = static_cast<int64_t>(b) * Hq + h;
       jobs.push_back(RowJob{q + row * d, kc + (static_cast<int64_t>(b) * Hkv + hk) * cap * d,
                             vc + (static_cast<int64_t>(b) * Hkv + hk) * cap * d, d, nk[b], o + row * d,
-                            lse ? lse + row : nullptr});
+                            lse ? lse + row : nullptr, 0});
     }
   }
   return run_rows(jobs, d, scale, method, param, nthreads);
@@ -275,7 +289,7 @@ int oracle_decode(const double* q, const double* kc, const double* vc, const int
 // lse [total_q, Hq] nullable. Causal is aligned to each sequence's end.
 int oracle_varlen(const double* q, const double* k, const double* v, const int32_t* cu_q,
                   const int32_t* cu_k, double* o, double* lse, int num_seqs, int Hq, int Hkv, int d,
-                  int causal, double scale, int method, int param, int nthreads) {
+                  int causal, double scale, int method, int param, int nthreads, int window) {
   if (num_seqs < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv) return 1;
   if (num_seqs > 0 && (cu_q[0] != 0 || cu_k[0] != 0)) return 1;
   const int g = Hq / Hkv;
@@ -290,7 +304,8 @@ int oracle_varlen(const double* q, const double* k, const double* v, const int32
         const int64_t row = static_cast<int64_t>(cu_q[s] + i) * Hq + h;
         const int64_t k0 = static_cast<int64_t>(cu_k[s]) * Hkv + hk;
         jobs.push_back(RowJob{q + row * d, k + k0 * d, v + k0 * d, static_cast<int64_t>(Hkv) * d,
-                              visible_keys(i, nq, nk, causal), o + row * d, lse ? lse + row : nullptr});
+                              visible_keys(i, nq, nk, causal), o + row * d, lse ? lse + row : nullptr,
+                              first_visible_key(i, nq, nk, causal, window)});
       }
   }
   return run_rows(jobs, d, scale, method, param, nthreads);
@@ -326,7 +341,7 @@ int oracle_probs(const double* q, const double* k, double* p, int Nq, int Nk, in
 int oracle_partials(const double* q, const double* k, const double* v, int n, int d, double scale,
                     int workers, double* m, double* l, double* o) {
   if (n < 0 || d <= 0 || workers < 1) return 1;
-  RowJob r{q, k, v, d, n, nullptr, nullptr};
+  RowJob r{q, k, v, d, n, nullptr, nullptr, 0};
   std::vector<State> parts;
   splitk_partials(r, d, scale, workers, parts);
   for (int w = 0; w < workers; ++w) {

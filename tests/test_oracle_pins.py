@@ -422,3 +422,74 @@ def test_paged_decode_gathers_the_same_keys():
     o3, _ = oracle.decode_paged(q.numpy(), kp2.numpy(), vp.numpy(), table.numpy(), nk.numpy(), method="splitk",
                                 workers=3)
     assert np.array_equal(o1, o3)
+
+
+# ---------------------------------------------------------------- sliding window
+# "Attention Computation in Practice", Masking variants: sliding window i - W < j <= i.
+
+
+def test_window_at_least_the_sequence_is_plain_causal():
+    r = rng(31)
+    q, k, v = dense(r, 1, 2, 1, 40, 55, 8)
+    o0, l0 = oracle.attention(q, k, v, True, method="tiled", block=8)
+    for w in (55, 56, 1000):
+        o1, l1 = oracle.attention(q, k, v, True, method="tiled", block=8, window=w)
+        assert np.array_equal(o0, o1) and np.array_equal(l0, l1)
+
+
+def test_window_of_one_returns_the_diagonal_value():
+    r = rng(32)
+    q, k, v = dense(r, 1, 1, 1, 20, 20, 8)
+    for method, kw in (("naive", {}), ("tiled", {"block": 3}), ("splitk", {"workers": 4})):
+        o, lse = oracle.attention(q, k, v, True, method=method, window=1, **kw)
+        assert np.array_equal(o[0, 0], v[0, 0])
+        s = np.einsum("id,id->i", q[0, 0], k[0, 0]) / math.sqrt(8)
+        assert np.max(np.abs(lse[0, 0] - s)) <= 1e-14
+
+
+@pytest.mark.parametrize("nq,nk,w", [(16, 16, 5), (6, 30, 7), (30, 30, 1)])
+def test_window_zero_queries_mean_over_window(nq, nk, w):
+    r = rng(33)
+    q = np.zeros((1, 1, nq, 4))
+    k, v = randn(r, 1, 1, nk, 4), randn(r, 1, 1, nk, 4)
+    for method, kw in (("naive", {}), ("tiled", {"block": 4}), ("splitk", {"workers": 3})):
+        o, lse = oracle.attention(q, k, v, True, method=method, window=w, **kw)
+        for i in range(nq):
+            hi = visible(i, nq, nk, True)
+            lo = max(0, hi - w)
+            assert np.max(np.abs(o[0, 0, i] - v[0, 0, lo:hi].mean(axis=0))) <= 1e-14
+            assert abs(lse[0, 0, i] - math.log(hi - lo)) <= 1e-14
+
+
+def test_window_brute_force_and_varlen():
+    r = rng(34)
+    q, k, v = randn(r, 5, 4), randn(r, 7, 4), randn(r, 7, 4)
+    w = 3
+    # brute force with the window restricting the visible range: keys [hi - 3, hi)
+    nq, nk = 5, 7
+    ref_o, ref_l = [], []
+    for i in range(nq):
+        hi = visible(i, nq, nk, True)
+        lo = max(0, hi - w)
+        s = [0.5 * sum(q[i][c] * k[j][c] for c in range(4)) for j in range(lo, hi)]
+        e = [math.exp(x) for x in s]
+        z = sum(e)
+        ref_o.append([sum(e[j - lo] / z * v[j][c] for j in range(lo, hi)) for c in range(4)])
+        ref_l.append(math.log(z))
+    o, lse = oracle.attention(q[None, None], k[None, None], v[None, None], True, window=w, method="tiled", block=2)
+    assert np.max(np.abs(o[0, 0] - np.array(ref_o))) <= 1e-14
+    assert np.max(np.abs(lse[0, 0] - np.array(ref_l))) <= 1e-14
+    # the packed form with the window equals the per-sequence dense form
+    nqs, nks = [1, 5, 3], [9, 7, 3]
+    Q = randn(r, sum(nqs), 2, 4)
+    K = randn(r, sum(nks), 1, 4)
+    V = randn(r, sum(nks), 1, 4)
+    cq = np.concatenate([[0], np.cumsum(nqs)]).astype(np.int32)
+    ck = np.concatenate([[0], np.cumsum(nks)]).astype(np.int32)
+    ov, lv = oracle.varlen(Q, K, V, cq, ck, True, window=2, method="tiled", block=2)
+    for s_ in range(3):
+        od, ld = oracle.attention(Q[cq[s_]:cq[s_ + 1]].transpose(1, 0, 2)[None],
+                                  K[ck[s_]:ck[s_ + 1]].transpose(1, 0, 2)[None],
+                                  V[ck[s_]:ck[s_ + 1]].transpose(1, 0, 2)[None], True, window=2, method="tiled",
+                                  block=2)
+        assert np.array_equal(ov[cq[s_]:cq[s_ + 1]], od[0].transpose(1, 0, 2))
