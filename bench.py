@@ -2,9 +2,10 @@
 
 Headline workload: causal bf16 prefill, B=4, 32 heads, Nq = Nk = 4096, d = 128 (outputs O bf16 and
 fp32 LSE), measured as prefill TFLOP/s with causal FLOPs counted as half (4*d*Nq*Nk/2 per head).
-The same line carries the decode KV-cache GB/s of the two decode workloads and the varlen append
-workload in ``breakdown``, each with its own roofline, so that one run covers every step of the
-path (prefill tiles, split-K decode + merge, varlen dispatch).
+The same line carries the decode KV-cache GB/s of the decode workloads (contiguous and paged), the
+sliding-window prefill and the varlen append workload in ``breakdown``, each with its own roofline,
+so that one run covers every step of the path (prefill tiles, split-K decode + merge, paged
+gather, window, varlen dispatch).
 
 Timing: W untimed warm-up steps, then K steps bracketed by a barrier and a device synchronize,
 CUDA events on the launching stream; every workload's inputs are larger than L2 (129 MB), so no
@@ -263,6 +264,17 @@ def run_case(args, world, stream, dev, peaks):
         ms = statistics.mean(per)
         out.update({"B": B, "ms": ms, "tflops": rl.prefill_flops(B, w.Hq, w.Nq, w.Nk, w.d, True) / ms / 1e9,
                     "launches": n})
+    elif args.case == "window":
+        w = wl.WORKLOADS["prefill_window_b4_h32_n4096_w1024_d128"]
+        B, W = args.batch or w.B, w.extra["window"]
+        q, k, v = wl.prefill_inputs(B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, torch.bfloat16, w.seed, device=dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, w.Hq, w.Nq), dtype=torch.float32, device=dev)
+        per, n = time_steps(lambda: bw.attn_fwd(q, k, v, causal=True, window=W, out=o, lse=lse), args.steps,
+                            args.warmup, world, stream)
+        ms = statistics.mean(per)
+        out.update({"B": B, "window": W, "ms": ms,
+                    "tflops": rl.window_prefill_flops(B, w.Hq, w.Nq, w.Nk, w.d, W) / ms / 1e9, "launches": n})
     elif args.case == "paged":
         x = wl.make("decode_paged_b8_h32x8_n32768_d128_p16", device=dev)
         wd = x["w"]
@@ -313,7 +325,7 @@ def main():
     ap.add_argument("--impl", default="own", choices=["own", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-breakdown", action="store_true")
-    ap.add_argument("--case", default="all", choices=["all", "prefill", "decode", "paged", "varlen"],
+    ap.add_argument("--case", default="all", choices=["all", "prefill", "window", "decode", "paged", "varlen"],
                     help="profiling aid: run one part only (no e2e, no CPU baseline)")
     ap.add_argument("--batch", type=int, default=0, help="profiling aid: override the prefill batch size")
     args = ap.parse_args()
@@ -415,6 +427,23 @@ def main():
                                            "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": kvb,
                                            "traffic": None, "note": "paged split-K pass with the fused merge"}}
         del xp, wsp, op, lp, nkp
+        torch.cuda.empty_cache()
+        xw = wl.make("prefill_window_b4_h32_n4096_w1024_d128", device=dev)
+        ww = xw["w"]
+        W = ww.extra["window"]
+        ow = torch.empty_like(xw["q"])
+        lw = torch.empty((ww.B, ww.Hq, ww.Nq), dtype=torch.float32, device=dev)
+        fn = lambda: bw.attn_fwd(xw["q"], xw["k"], xw["v"], causal=True, window=W, out=ow, lse=lw)  # noqa: E731
+        perw, _ = time_steps(fn, args.steps, args.warmup, world, stream)
+        msw = max_over_ranks(statistics.mean(perw), world)
+        fw = rl.window_prefill_flops(ww.B, ww.Hq, ww.Nq, ww.Nk, ww.d, W)
+        tw = fw / (msw * 1e-3) / 1e12
+        breakdown[ww.name] = {"metric": "window prefill TFLOP/s", "value": tw * world, "unit": "TFLOP/s",
+                              "ms_per_step": msw, "window": W, "flops_per_step": fw,
+                              "flop_convention": "visible (query, key) pairs counted exactly",
+                              "roofline": {"bound": "tensor", "achieved": tw, "peak": peaks["bf16_tflops"],
+                                           "unit": "TFLOP/s", "frac": tw / peaks["bf16_tflops"], "traffic": None}}
+        del xw, ow, lw
         torch.cuda.empty_cache()
         xv = wl.make("varlen_append_64seq_h32x8_d128", device=dev)
         wv = xv["w"]

@@ -58,6 +58,8 @@ def lib() -> ctypes.CDLL:
         vp, ci, cf, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         L.attn_fwd.argtypes = [vp, vp, vp, vp, vp] + [ci] * 7 + [cf, ci, vp]
         L.attn_fwd.restype = ci
+        L.attn_fwd_window.argtypes = [vp, vp, vp, vp, vp] + [ci] * 7 + [cf, ci, vp]
+        L.attn_fwd_window.restype = ci
         L.attn_decode_workspace_size.argtypes = [ci, ci, ci, ci]
         L.attn_decode_workspace_size.restype = sz
         L.attn_decode.argtypes = [vp, vp, vp, vp, vp] + [ci] * 6 + [cf, vp, vp, sz, vp]
@@ -68,6 +70,8 @@ def lib() -> ctypes.CDLL:
         L.attn_varlen_workspace_size.restype = sz
         L.attn_varlen.argtypes = [vp] * 7 + [ci] * 9 + [cf, vp, sz, vp]
         L.attn_varlen.restype = ci
+        L.attn_varlen_window.argtypes = [vp] * 7 + [ci] * 9 + [cf, vp, sz, vp]
+        L.attn_varlen_window.restype = ci
         L.bwattn_last_cuda_error.argtypes = []
         L.bwattn_last_cuda_error.restype = ci
         L.bwattn_status_string.argtypes = [ci]
@@ -127,8 +131,12 @@ def _scale(scale, d):
 
 
 def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = True, scale: float | None = None,
-             out: torch.Tensor | None = None, lse: torch.Tensor | bool | None = True, stream=None):
-    """Prefill / cross attention. q [B, Hq, Nq, d]; k, v [B, Hkv, Nk, d] -> (o, lse or None)."""
+             out: torch.Tensor | None = None, lse: torch.Tensor | bool | None = True, stream=None, window: int = 0):
+    """Prefill / cross attention. q [B, Hq, Nq, d]; k, v [B, Hkv, Nk, d] -> (o, lse or None).
+
+    ``window`` > 0 (causal only): sliding window of that many keys ending at each query's limit."""
+    if window and not causal:
+        raise ValueError("a sliding window needs causal=True")
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
         raise ValueError("q, k, v must be 4-D [B, H, N, d]")
     B, Hq, Nq, d = q.shape
@@ -152,6 +160,11 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = T
     elif isinstance(lse, torch.Tensor):
         lse_t = lse
         _cuda(lse_t, "lse", torch.float32)
+    if window:
+        rc = lib().attn_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse_t), B, Hq, Hkv, Nq, Nk, d,
+                                   int(window), _scale(scale, d), dt, _stream(stream))
+        _check(rc, "attn_fwd_window")
+        return out, lse_t
     rc = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse_t), B, Hq, Hkv, Nq, Nk, d, int(bool(causal)),
                         _scale(scale, d), dt, _stream(stream))
     _check(rc, "attn_fwd")
@@ -239,8 +252,12 @@ def varlen_workspace_size(num_seqs: int, max_seqlen_k: int, Hq: int, Hkv: int, d
 def attn_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q: torch.Tensor,
                 cu_seqlens_k: torch.Tensor, max_seqlen_q: int, max_seqlen_k: int, causal: bool = True,
                 scale: float | None = None, workspace: torch.Tensor | None = None, out: torch.Tensor | None = None,
-                lse: torch.Tensor | bool | None = True, stream=None):
-    """Packed varlen. q [total_q, Hq, d]; k, v [total_k, Hkv, d]; cu_seqlens int32 [num_seqs + 1] (device)."""
+                lse: torch.Tensor | bool | None = True, stream=None, window: int = 0):
+    """Packed varlen. q [total_q, Hq, d]; k, v [total_k, Hkv, d]; cu_seqlens int32 [num_seqs + 1] (device).
+
+    ``window`` > 0 (causal only): sliding window of that many keys ending at each query's limit."""
+    if window and not causal:
+        raise ValueError("a sliding window needs causal=True")
     if q.dim() != 3 or k.dim() != 3:
         raise ValueError("q must be [total_q, Hq, d] and k, v [total_k, Hkv, d]")
     tq, Hq, d = q.shape
@@ -267,11 +284,14 @@ def attn_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q:
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     _cuda(workspace, "workspace")
-    rc = lib().attn_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse_t), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
-                           num_seqs, tq, tk, int(max_seqlen_q), int(max_seqlen_k), Hq, Hkv, d, int(bool(causal)),
-                           _scale(scale, d), _ptr(workspace), workspace.numel() * workspace.element_size(),
-                           _stream(stream))
-    _check(rc, "attn_varlen")
+    if window:
+        fn, mode, what = lib().attn_varlen_window, int(window), "attn_varlen_window"
+    else:
+        fn, mode, what = lib().attn_varlen, int(bool(causal)), "attn_varlen"
+    rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse_t), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), num_seqs, tq,
+            tk, int(max_seqlen_q), int(max_seqlen_k), Hq, Hkv, d, mode, _scale(scale, d), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, what)
     return out, lse_t
 
 

@@ -222,8 +222,12 @@ int bwattn_test_wait_timeout(void* stream) {
   return BWATTN_OK;
 }
 
-int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
-             int Nk, int d, int causal, float scale, int dtype, void* stream) {
+}  // extern "C"
+
+namespace {
+
+int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq, int Nk,
+             int d, int causal, float scale, int dtype, int window, void* stream) {
   if (B < 0 || Nq < 0 || Nk < 0 || Hq <= 0 || Hkv <= 0 || d <= 0) return BWATTN_ERR_INVALID_ARG;
   if (Hq % Hkv != 0 || !good_scale(scale) || (causal != 0 && causal != 1)) return BWATTN_ERR_INVALID_ARG;
   if (B > 65535 || Hq > 65535) return BWATTN_ERR_INVALID_ARG;
@@ -238,7 +242,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   cudaError_t e;
   if (dtype == BWATTN_DTYPE_FP32) {
     bw::Fp32FwdArgs a{static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),
-                      static_cast<float*>(o), lse, B, Hq, Hkv, Nq, Nk, d, causal, sl2};
+                      static_cast<float*>(o), lse, B, Hq, Hkv, Nq, Nk, d, causal, sl2, window};
     if ((e = bw::launch_prefill_fp32(a, st)) != cudaSuccess) return cuda_fail(e);
     g_launches.fetch_add(1);
     return BWATTN_OK;
@@ -271,6 +275,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   a.num_seqs = B;
   a.small_rows_limit = 0;
   a.max_pairs = (Nq + 255) / 256;
+  a.window = window;
   a.scale_log2 = sl2;
   a.timeout_ns = g_timeout_ns.load();
   unsigned int* sp = nullptr;
@@ -280,6 +285,21 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   if ((e = bw::launch_prefill_tc(a, sp, sc, st)) != cudaSuccess) return cuda_fail(e);
   g_launches.fetch_add(1);
   return BWATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+             int Nk, int d, int causal, float scale, int dtype, void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale, dtype, 0, stream);
+}
+
+int attn_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+                    int Nk, int d, int window, float scale, int dtype, void* stream) {
+  if (window < 1) return BWATTN_ERR_INVALID_ARG;
+  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, 1, scale, dtype, window, stream);
 }
 
 size_t attn_decode_workspace_size(int B, int Hq, int d, int num_splits) {
@@ -431,9 +451,13 @@ size_t attn_varlen_workspace_size(int num_seqs, int max_seqlen_k, int Hq, int Hk
   return bw::splitk_ws_bytes(num_seqs * Hkv, varlen_splits(max_seqlen_k), kSmallRowsLimit, d);
 }
 
-int attn_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens_q,
+}  // extern "C"
+
+namespace {
+
+int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens_q,
                 const int32_t* cu_seqlens_k, int num_seqs, int total_q, int total_k, int max_seqlen_q,
-                int max_seqlen_k, int Hq, int Hkv, int d, int causal, float scale, void* workspace,
+                int max_seqlen_k, int Hq, int Hkv, int d, int causal, int window, float scale, void* workspace,
                 size_t workspace_bytes, void* stream) {
   if (num_seqs < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0) return BWATTN_ERR_INVALID_ARG;
   if (Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0 || !good_scale(scale) || (causal != 0 && causal != 1))
@@ -481,6 +505,7 @@ int attn_varlen(const void* q, const void* k, const void* v, void* o, float* lse
     a.num_seqs = num_seqs;
     a.small_rows_limit = kSmallRowsLimit;
     a.max_pairs = (max_seqlen_q + 255) / 256;
+    a.window = window;
     a.scale_log2 = sl2;
     a.timeout_ns = g_timeout_ns.load();
     unsigned int* sp = nullptr;
@@ -513,6 +538,7 @@ int attn_varlen(const void* q, const void* k, const void* v, void* o, float* lse
   s.rows_max = kSmallRowsLimit;
   s.row_groups = kSmallRowsLimit / 16;
   s.causal = causal;
+  s.window = window;
   s.small_rows_limit = kSmallRowsLimit;
   s.ws_o_offset = bw::splitk_o_offset(units, splits, kSmallRowsLimit);
   s.scale_log2 = sl2;
@@ -542,6 +568,27 @@ int attn_varlen(const void* q, const void* k, const void* v, void* o, float* lse
   if ((e = bw::launch_merge(m, st)) != cudaSuccess) return cuda_fail(e);
   g_launches.fetch_add(1);
   return BWATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens_q,
+                const int32_t* cu_seqlens_k, int num_seqs, int total_q, int total_k, int max_seqlen_q,
+                int max_seqlen_k, int Hq, int Hkv, int d, int causal, float scale, void* workspace,
+                size_t workspace_bytes, void* stream) {
+  return varlen_impl(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k, max_seqlen_q,
+                     max_seqlen_k, Hq, Hkv, d, causal, 0, scale, workspace, workspace_bytes, stream);
+}
+
+int attn_varlen_window(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens_q,
+                       const int32_t* cu_seqlens_k, int num_seqs, int total_q, int total_k, int max_seqlen_q,
+                       int max_seqlen_k, int Hq, int Hkv, int d, int window, float scale, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  if (window < 1) return BWATTN_ERR_INVALID_ARG;
+  return varlen_impl(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k, max_seqlen_q,
+                     max_seqlen_k, Hq, Hkv, d, 1, window, scale, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -22,6 +22,7 @@ struct Fp32FwdArgs {
   float* lse;
   int B, Hq, Hkv, Nq, Nk, d, causal;
   float scale_log2;  // scale * log2(e)
+  int window;        // > 0: sliding window of that many keys ending at the causal limit
 };
 cudaError_t launch_prefill_fp32(const Fp32FwdArgs& a, cudaStream_t stream);
 
@@ -46,6 +47,7 @@ struct SplitKArgs {
   int rows_max;       // workspace rows per (sequence, KV head)
   int row_groups;     // ceil(rows_max / 16)
   int causal;         // varlen: causal aligned to each sequence's end
+  int window;         // varlen: > 0 adds a sliding window of that many keys
   int small_rows_limit;  // varlen: a sequence takes this path iff n_q * g <= this
   size_t ws_o_offset;    // splitk_o_offset(num_seqs * Hkv, num_splits, rows_max)
   float scale_log2;
@@ -86,6 +88,7 @@ struct TcFwdArgs {
   int num_seqs;
   int small_rows_limit;  // varlen: sequences with n_q * g <= this are skipped here
   int max_pairs;         // grid.x: pairs of 128-row query tiles per (sequence, head)
+  int window;            // > 0: sliding window of that many keys ending at the causal limit
   float scale_log2;
   uint64_t timeout_ns;
 };

@@ -58,16 +58,20 @@ __global__ void __launch_bounds__(kThreads) prefill_fp32_kernel(Fp32FwdArgs a) {
     qr[i] = row_ok ? qrow[t + 4 * i] : make_float4(0.f, 0.f, 0.f, 0.f);
     acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  // keys [0, lim) are visible to this row
+  // keys [lo, lim) are visible to this row (lo > 0 only with a sliding window)
   int lim = a.causal ? min(a.Nk, row + shift + 1) : a.Nk;
   if (!row_ok) lim = 0;
+  const bool windowed = a.causal && a.window > 0;
+  const int lo = windowed ? max(0, row + shift + 1 - a.window) : 0;
   const int last_row = min(q0 + kRows - 1, a.Nq - 1);
   int kend = a.causal ? min(a.Nk, last_row + shift + 1) : a.Nk;
   kend = max(kend, 0);
+  // the CTA's first row has the lowest window start; tiles below it are skipped
+  const int kbeg = windowed ? max(0, q0 + shift + 1 - a.window) / KT * KT : 0;
 
   const unsigned quad = 0xFu << (threadIdx.x & 28);
   float m = -INFINITY, l = 0.f;
-  for (int j0 = 0; j0 < kend; j0 += KT) {
+  for (int j0 = kbeg; j0 < kend; j0 += KT) {
     __syncthreads();
     for (int idx = tid; idx < KT * C4; idx += kThreads) {
       const int key = j0 + idx / C4;
@@ -82,7 +86,8 @@ __global__ void __launch_bounds__(kThreads) prefill_fp32_kernel(Fp32FwdArgs a) {
     }
     __syncthreads();
     const int nvis = min(KT, lim - j0);  // same for the 4 threads of a row
-    for (int jj = 0; jj < nvis; jj += 8) {
+    const int jlo = lo - j0;              // keys of this tile below jlo are outside the window
+    for (int jj = max(0, jlo) & ~7; jj < nvis; jj += 8) {
       float s[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
@@ -100,10 +105,11 @@ __global__ void __launch_bounds__(kThreads) prefill_fp32_kernel(Fp32FwdArgs a) {
       float mt = -INFINITY;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        s[u] = (jj + u < nvis) ? s[u] * a.scale_log2 : -INFINITY;
+        s[u] = (jj + u < nvis && jj + u >= jlo) ? s[u] * a.scale_log2 : -INFINITY;
         mt = fmaxf(mt, s[u]);
       }
-      const float mn = fmaxf(m, mt);  // finite: key jj is visible
+      const float mn = fmaxf(m, mt);
+      if (mn == -INFINITY) continue;
       const float alpha = (m == -INFINITY) ? 0.f : exp2f(m - mn);
       l *= alpha;
 #pragma unroll

@@ -83,8 +83,11 @@ struct Item {
   bool active;
   int nq, nk;
   int q_lo[2];  // first row (within the sequence) of each query tile
-  int nt[2];    // K/V tiles each query tile needs
-  int nt_all;
+  int j0[2];    // first K/V tile each query tile needs
+  int j1[2];    // one past its last K/V tile
+  int nt[2];    // j1 - j0
+  int jmin;     // first K/V tile of the item (over both query tiles)
+  int nt_all;   // K/V tiles the item loads: jmin .. jmin + nt_all - 1
   // TMA coordinates: dense maps are {d, rows, seq*heads}, packed maps {d, heads, tokens}
   int q_c1, q_c2, kv_c1, kv_c2;
   bool packed;
@@ -95,6 +98,7 @@ struct Item {
 // Item numbering: bands of kBandUnits (sequence, head) units; inside a band all units of the
 // last query-tile pair come first, then those of the pair before, and so on (with a causal
 // mask later pairs see more keys).
+template <bool kWindow>
 __device__ __forceinline__ Item make_item(const TcFwdArgs& a, int idx) {
   Item w;
   const int units = a.num_seqs * a.Hq;
@@ -123,18 +127,48 @@ __device__ __forceinline__ Item make_item(const TcFwdArgs& a, int idx) {
   w.active = w.nq > 0 && pair * 2 * kBM < w.nq;
   if (w.packed && w.nq * g <= a.small_rows_limit) w.active = false;
   const int shift = w.nk - w.nq;
-  w.nt_all = 0;
-  for (int t = 0; t < 2; ++t) {
-    w.q_lo[t] = pair * 2 * kBM + t * kBM;
-    int nt = 0;
-    if (w.active && w.q_lo[t] < w.nq) {
-      const int q_hi = min(w.q_lo[t] + kBM - 1, w.nq - 1);
-      int kend = a.causal ? min(w.nk, q_hi + shift + 1) : w.nk;
-      kend = max(kend, 0);
-      nt = (kend + kBN - 1) / kBN;
+  if constexpr (!kWindow) {
+    // every query tile starts at K/V tile 0
+    w.jmin = 0;
+    w.nt_all = 0;
+    for (int t = 0; t < 2; ++t) {
+      w.q_lo[t] = pair * 2 * kBM + t * kBM;
+      int nt = 0;
+      if (w.active && w.q_lo[t] < w.nq) {
+        const int q_hi = min(w.q_lo[t] + kBM - 1, w.nq - 1);
+        int kend = a.causal ? min(w.nk, q_hi + shift + 1) : w.nk;
+        kend = max(kend, 0);
+        nt = (kend + kBN - 1) / kBN;
+      }
+      w.j0[t] = 0;
+      w.j1[t] = nt;
+      w.nt[t] = nt;
+      w.nt_all = max(w.nt_all, nt);
     }
-    w.nt[t] = nt;
-    w.nt_all = max(w.nt_all, nt);
+  } else {
+    int jmax = 0;
+    w.jmin = 0x7fffffff;
+    for (int t = 0; t < 2; ++t) {
+      w.q_lo[t] = pair * 2 * kBM + t * kBM;
+      int j0 = 0, j1 = 0;
+      if (w.active && w.q_lo[t] < w.nq) {
+        const int q_hi = min(w.q_lo[t] + kBM - 1, w.nq - 1);
+        const int kend = max(min(w.nk, q_hi + shift + 1), 0);
+        // the tile's first row sees nothing below this key
+        const int kbeg = min(max(0, w.q_lo[t] + shift + 1 - a.window), kend);
+        j0 = kbeg / kBN;
+        j1 = (kend > kbeg) ? (kend + kBN - 1) / kBN : j0;
+      }
+      w.j0[t] = j0;
+      w.j1[t] = j1;
+      w.nt[t] = j1 - j0;
+      if (j1 > j0) {
+        w.jmin = min(w.jmin, j0);
+        jmax = max(jmax, j1);
+      }
+    }
+    if (w.jmin > jmax) w.jmin = 0;
+    w.nt_all = jmax - w.jmin;
   }
   if (w.packed) {
     w.q_c1 = h;
@@ -174,7 +208,8 @@ __device__ __forceinline__ void tma_tile(const CUtensorMap* map, const Item& w, 
   }
 }
 
-template <int D>
+// kWindow: causal sliding window (its own instance; the plain path keeps K/V tile 0 as start)
+template <int D, bool kWindow>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ TcFwdArgs a,
                                                                  unsigned int* status, unsigned int* sched) {
   using C = Cfg<D>;
@@ -236,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         Item w;
         do {
           idx = static_cast<int>(atomicAdd(&sched[0], 1u));
-          if (idx < total_items) w = make_item(a, idx);
+          if (idx < total_items) w = make_item<kWindow>(a, idx);
         } while (idx < total_items && !w.active);
         if (idx >= total_items) idx = -1;
         const int qs = k % kItemSlots;
@@ -258,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           mbar_arrive_expect_tx(&bar->kv_full[slot], C::kTileBytes);
           for (int hf = 0; hf < C::kHalves; ++hf)
             tma_tile((i & 1) ? &a.tm_v : &a.tm_k, w, sRing + slot * C::kTileBytes + hf * (kBN * 128),
-                     &bar->kv_full[slot], hf, (i >> 1) * kBN, false);
+                     &bar->kv_full[slot], hf, (w.jmin + (i >> 1)) * kBN, false);
         }
       }
       if (!ok) raise_timeout(abort, status);
@@ -315,57 +350,60 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       for (int k = 0; ok; ++k) {
         const int idx = next_item(bar, k, true, tmo, abort, &ok);
         if (!ok || idx < 0) break;
-        const Item w = make_item(a, idx);
+        const Item w = make_item<kWindow>(a, idx);
         if (!(ok = mbar_wait(&bar->q_full, items & 1, tmo, abort))) break;
         tc_fence_after();
         ++items;
-        const int nt = w.nt_all, nt0 = w.nt[0], nt1 = w.nt[1];
+        const int nt = w.nt_all;
         const int base = nload;
-        s_left = nt0 + nt1;
+        // K/V tile jmin + j is used by query tile t iff j0[t] <= jmin + j < j1[t]
+        const int a0 = w.j0[0] - w.jmin, e0 = w.j1[0] - w.jmin;
+        const int a1 = w.j0[1] - w.jmin, e1 = w.j1[1] - w.jmin;
+        s_left = w.nt[0] + w.nt[1];
         if (s_left == 0) umma_commit(&bar->q_empty);
         if (nt > 0) {
           if (!(ok = wait_load(base))) break;
-          if (nt0 > 0) issue_s(0, base);
-          if (nt1 > 0) issue_s(1, base);
+          if (a0 == 0 && e0 > 0) issue_s(0, base);
+          if (a1 == 0 && e1 > 0) issue_s(1, base);
           umma_commit(&bar->kv_empty[base % C::kStages]);
         }
         for (int j = 0; j < nt; ++j) {
           const int iv = base + 2 * j + 1, ik = base + 2 * j + 2;
           if (!(ok = wait_load(iv))) break;
           // tile 0: P0 V_j, then S0 for the next K tile
-          if (j < nt0) {
+          if (j >= a0 && j < e0) {
             // the first P.V of an item overwrites O: the previous item's epilogue must be done
-            if (j == 0 && ou0 > 0 && !(ok = mbar_wait(&bar->o_empty[0], (ou0 - 1) & 1, tmo, abort))) break;
+            if (j == a0 && ou0 > 0 && !(ok = mbar_wait(&bar->o_empty[0], (ou0 - 1) & 1, tmo, abort))) break;
             if (!(ok = mbar_wait(&bar->p_full[0], pt0 & 1, tmo, abort))) break;
             tc_fence_after();
-            issue_pv_half(0, iv, 0, j > 0);
+            issue_pv_half(0, iv, 0, j > a0);
             if (!(ok = mbar_wait(&bar->p2_full[0], pt0 & 1, tmo, abort))) break;
             ++pt0;
             tc_fence_after();
             issue_pv_half(0, iv, 1, true);
-            if (j == nt0 - 1) {
+            if (j == e0 - 1) {
               umma_commit(&bar->o_full[0]);
               ++ou0;
             }
           }
           if (j + 1 < nt && !(ok = wait_load(ik))) break;
-          if (j + 1 < nt0) issue_s(0, ik);
+          if (j + 1 >= a0 && j + 1 < e0) issue_s(0, ik);
           // tile 1
-          if (j < nt1) {
-            if (j == 0 && ou1 > 0 && !(ok = mbar_wait(&bar->o_empty[1], (ou1 - 1) & 1, tmo, abort))) break;
+          if (j >= a1 && j < e1) {
+            if (j == a1 && ou1 > 0 && !(ok = mbar_wait(&bar->o_empty[1], (ou1 - 1) & 1, tmo, abort))) break;
             if (!(ok = mbar_wait(&bar->p_full[1], pt1 & 1, tmo, abort))) break;
             tc_fence_after();
-            issue_pv_half(1, iv, 0, j > 0);
+            issue_pv_half(1, iv, 0, j > a1);
             if (!(ok = mbar_wait(&bar->p2_full[1], pt1 & 1, tmo, abort))) break;
             ++pt1;
             tc_fence_after();
             issue_pv_half(1, iv, 1, true);
-            if (j == nt1 - 1) {
+            if (j == e1 - 1) {
               umma_commit(&bar->o_full[1]);
               ++ou1;
             }
           }
-          if (j + 1 < nt1) issue_s(1, ik);
+          if (j + 1 >= a1 && j + 1 < e1) issue_s(1, ik);
           if (j + 1 < nt) umma_commit(&bar->kv_empty[ik % C::kStages]);
           umma_commit(&bar->kv_empty[iv % C::kStages]);
         }
@@ -395,11 +433,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       __syncwarp();
       if (lane == 0 && ok) mbar_arrive(&bar->item_empty[k % kItemSlots]);
       if (!ok || idx < 0) break;
-      const Item w = make_item(a, idx);
-      const int q_row = w.q_lo[t] + row;
+      const Item w = make_item<kWindow>(a, idx);
+      // per-tile fields by select: a runtime index would put the item in local memory
+      const int q_row = (t ? w.q_lo[1] : w.q_lo[0]) + row;
       const bool row_ok = q_row < w.nq;
       const int lim = a.causal ? min(w.nk, q_row + (w.nk - w.nq) + 1) : w.nk;
-      const int ntile = w.nt[t];
+      // sliding window: keys below lo are outside this row's window
+      const int lo = kWindow ? q_row + (w.nk - w.nq) + 1 - a.window : 0;
+      const int ntile = t ? w.nt[1] : w.nt[0];
+      const int jfirst = t ? w.j0[1] : w.j0[0];
       float m_ref = -INFINITY, l = 0.f;
       for (int j = 0; j < ntile; ++j) {
         ok = mbar_wait(&bar->s_full[t], stiles & 1, tmo, abort);
@@ -417,15 +459,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         tmem_reg_fence(s1);
         tmem_reg_fence(s2);
         tmem_reg_fence(s3);
-        const int kv0 = j * kBN;
-        if (kv0 + kBN > lim) {
+        const int kv0 = (jfirst + j) * kBN;
+        if (kv0 + kBN > lim || (kWindow && kv0 < lo)) {
           const uint32_t ninf = __float_as_uint(-INFINITY);
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            if (kv0 + e >= lim) s0[e] = ninf;
-            if (kv0 + 32 + e >= lim) s1[e] = ninf;
-            if (kv0 + 64 + e >= lim) s2[e] = ninf;
-            if (kv0 + 96 + e >= lim) s3[e] = ninf;
+            if (kv0 + e >= lim || (kWindow && kv0 + e < lo)) s0[e] = ninf;
+            if (kv0 + 32 + e >= lim || (kWindow && kv0 + 32 + e < lo)) s1[e] = ninf;
+            if (kv0 + 64 + e >= lim || (kWindow && kv0 + 64 + e < lo)) s2[e] = ninf;
+            if (kv0 + 96 + e >= lim || (kWindow && kv0 + 96 + e < lo)) s3[e] = ninf;
           }
         }
         // row max: four chains of 3-input max (a single 128-long chain is pure latency)
@@ -575,10 +617,10 @@ __global__ void wait_timeout_probe_kernel(uint64_t timeout_ns, unsigned int* sta
 
 int g_num_sms[64] = {};
 
-template <int D>
+template <int D, bool kWindow>
 cudaError_t launch_d(const TcFwdArgs& a, unsigned int* status, unsigned int* sched, cudaStream_t stream) {
   using C = Cfg<D>;
-  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, kWindow>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(C::kSmemBytes));
   if (e != cudaSuccess) return e;
   int dev = 0;
@@ -591,15 +633,16 @@ cudaError_t launch_d(const TcFwdArgs& a, unsigned int* status, unsigned int* sch
   const long items = static_cast<long>(a.max_pairs) * a.num_seqs * a.Hq;
   const int grid = static_cast<int>(items < sms ? items : sms);
   if (grid <= 0) return cudaSuccess;
-  prefill_tc_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(a, status, sched);
+  prefill_tc_kernel<D, kWindow><<<grid, kThreads, C::kSmemBytes, stream>>>(a, status, sched);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_prefill_tc(const TcFwdArgs& a, unsigned int* status, unsigned int* sched, cudaStream_t stream) {
-  if (a.d == 64) return launch_d<64>(a, status, sched, stream);
-  return launch_d<128>(a, status, sched, stream);
+  const bool window = a.causal && a.window > 0;
+  if (a.d == 64) return window ? launch_d<64, true>(a, status, sched, stream) : launch_d<64, false>(a, status, sched, stream);
+  return window ? launch_d<128, true>(a, status, sched, stream) : launch_d<128, false>(a, status, sched, stream);
 }
 
 cudaError_t launch_wait_timeout_probe(uint64_t timeout_ns, unsigned int* status, cudaStream_t stream) {

@@ -124,8 +124,9 @@ __device__ __forceinline__ size_t ws_ml_index(const SplitKArgs& a, int unit, int
 }
 
 // NH = number of 8-row halves of the 16-row MMA tile that carry real rows (1 or 2);
-// kPaged: keys are gathered page by page through the block table.
-template <int NH, bool kPaged>
+// kPaged: keys are gathered page by page through the block table; kWindow: causal sliding
+// window (a separate instance, so the plain causal and paged paths carry no window registers).
+template <int NH, bool kPaged, bool kWindow>
 __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(SplitKArgs a) {
   const int split = blockIdx.x;
   const int hkv = blockIdx.y % a.Hkv;
@@ -146,8 +147,8 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
   const int kbeg = min(u.nk, split * chunk);
   const int kend = min(u.nk, kbeg + chunk);
 
-  // Rows gr (and gr + 8) of this group: (query i, head hh) and their key limits.
-  int lim[2];
+  // Rows gr (and gr + 8) of this group: (query i, head hh) and their key limits [lo, lim).
+  int lim[2], lo[2];
   uint32_t qa[8][4];
 #pragma unroll
   for (int rr = 0; rr < 2; ++rr) {
@@ -156,7 +157,11 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
     const int i = ok ? r / a.g : 0;
     const int hh = ok ? r % a.g : 0;
     lim[rr] = a.causal ? min(kend, u.nk - u.nq + i + 1) : kend;
-    if (!ok) lim[rr] = kend;
+    lo[rr] = kWindow ? u.nk - u.nq + i + 1 - a.window : 0;
+    if (!ok) {
+      lim[rr] = kend;
+      lo[rr] = 0;
+    }
     const uint16_t* qrow = a.q + (static_cast<int64_t>(u.tok0 + i) * a.Hq + hkv * a.g + hh) * D;
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
@@ -172,6 +177,15 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
   // lowest key limit over the CTA's rows: steps ending at or below it need no mask
   int min_lim = kend;
   if (a.causal) min_lim = min(kend, u.nk - u.nq + row0 / a.g + 1);
+  // with a sliding window: keys below the first row's window start are skipped (whole 16-key
+  // steps, so the step grid is kept), and steps starting below the last row's start are masked
+  int kstart = kbeg;
+  int max_lo = 0;
+  if constexpr (kWindow) {
+    kstart = max(kbeg, (u.nk - u.nq + row0 / a.g + 1 - a.window) / kKeysPerStep * kKeysPerStep);
+    const int last_r = min(row0 + kRowsPerGroup, R) - 1;
+    max_lo = u.nk - u.nq + last_r / a.g + 1 - a.window;
+  }
 
   float oacc[16][2 * NH];
 #pragma unroll
@@ -185,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
   const uint16_t* vbase = a.v + u.kv0;
   const int64_t ks = a.kv_key_stride;
 
-  for (int kb = kbeg + warp * kKeysPerStep; kb < kend; kb += kWarps * kKeysPerStep) {
+  for (int kb = kstart + warp * kKeysPerStep; kb < kend; kb += kWarps * kKeysPerStep) {
     // ---- loads: K rows kb + nt*8 + gr (chunks t + 4s); V rows kb + {2t, 2t+1, 2t+8, 2t+9}
     const int64_t so = step_offset<kPaged>(a, seq, kb);
     uint4 kk[2][4];
@@ -222,7 +236,8 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
       }
     }
     // ---- scale (log2 units), mask, row max over the quad
-    const bool need_mask = kb + kKeysPerStep > min_lim;
+    bool need_mask = kb + kKeysPerStep > min_lim;
+    if constexpr (kWindow) need_mask = need_mask || kb < max_lo;
     float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
@@ -232,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
         float s = sacc[nt][c] * a.scale_log2;
         if (need_mask) {
           const int key = kb + nt * 8 + 2 * t + (c & 1);
-          if (key >= lim[rr]) s = -INFINITY;
+          if (key >= lim[rr] || (kWindow && key < lo[rr])) s = -INFINITY;
         }
         sacc[nt][c] = s;
         mx[rr] = fmaxf(mx[rr], s);
@@ -508,10 +523,20 @@ cudaError_t launch_splitk(const SplitKArgs& a, cudaStream_t stream) {
   // every row group has at most 8 rows when the sequences' rows (n_q * g) never exceed 8
   const bool half = a.cu_q ? (a.small_rows_limit <= 8) : (a.g <= 8);
   const bool paged = a.block_table != nullptr;
-  if (half)
-    paged ? splitk_kernel<1, true><<<grid, kThreads, 0, stream>>>(a) : splitk_kernel<1, false><<<grid, kThreads, 0, stream>>>(a);
-  else
-    paged ? splitk_kernel<2, true><<<grid, kThreads, 0, stream>>>(a) : splitk_kernel<2, false><<<grid, kThreads, 0, stream>>>(a);
+  const bool window = a.causal && a.window > 0;
+  if (paged && window) return cudaErrorInvalidValue;  // no entry point pairs the two
+  if (window) {
+    if (half)
+      splitk_kernel<1, false, true><<<grid, kThreads, 0, stream>>>(a);
+    else
+      splitk_kernel<2, false, true><<<grid, kThreads, 0, stream>>>(a);
+  } else if (half) {
+    paged ? splitk_kernel<1, true, false><<<grid, kThreads, 0, stream>>>(a)
+          : splitk_kernel<1, false, false><<<grid, kThreads, 0, stream>>>(a);
+  } else {
+    paged ? splitk_kernel<2, true, false><<<grid, kThreads, 0, stream>>>(a)
+          : splitk_kernel<2, false, false><<<grid, kThreads, 0, stream>>>(a);
+  }
   return cudaGetLastError();
 }
 

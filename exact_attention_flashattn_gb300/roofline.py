@@ -27,14 +27,23 @@ def prefill_flops(B: int, Hq: int, Nq: int, Nk: int, d: int, causal: bool) -> fl
     return 4.0 * d * pairs * B * Hq
 
 
-def prefill_visible_pairs(Nq: int, Nk: int, causal: bool) -> int:
-    """Exact count of visible (query, key) pairs for one head (causal aligned to the end)."""
+def prefill_visible_pairs(Nq: int, Nk: int, causal: bool, window: int = 0) -> int:
+    """Exact count of visible (query, key) pairs for one head (causal aligned to the end;
+    ``window`` > 0 keeps the last ``window`` keys up to each query's limit)."""
     if not causal:
         return Nq * Nk
     total = 0
     for i in range(Nq):
-        total += max(0, min(Nk, i + (Nk - Nq) + 1))
+        hi = min(Nk, i + (Nk - Nq) + 1)
+        lo = max(0, i + (Nk - Nq) + 1 - window) if window > 0 else 0
+        total += max(0, hi - lo)
     return total
+
+
+def window_prefill_flops(B: int, Hq: int, Nq: int, Nk: int, d: int, window: int) -> float:
+    """Sliding-window prefill: 4*d FLOPs per visible pair, pairs counted exactly (there is no
+    half-of-the-square convention for a band)."""
+    return 4.0 * d * float(prefill_visible_pairs(Nq, Nk, True, window)) * B * Hq
 
 
 def prefill_bytes(B: int, Hq: int, Hkv: int, Nq: int, Nk: int, d: int, elem_bytes: int,

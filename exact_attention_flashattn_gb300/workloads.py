@@ -67,6 +67,12 @@ WORKLOADS = {
     "prefill_causal_b4_h32_n4096_d128": Workload("prefill_causal_b4_h32_n4096_d128", "fwd", torch.bfloat16,
                                                  B=4, Hq=32, Hkv=32, Nq=4096, Nk=4096, d=128, causal=True,
                                                  seed=SEED_PREFILL),
+    # the prefill inputs under a sliding window of 1024 keys ("Attention Computation in Practice",
+    # Masking variants)
+    "prefill_window_b4_h32_n4096_w1024_d128": Workload("prefill_window_b4_h32_n4096_w1024_d128", "fwd",
+                                                       torch.bfloat16, B=4, Hq=32, Hkv=32, Nq=4096, Nk=4096,
+                                                       d=128, causal=True, seed=SEED_PREFILL,
+                                                       extra={"window": 1024}),
     "decode_gqa_b8_h32x8_n32768_d128": Workload("decode_gqa_b8_h32x8_n32768_d128", "decode", torch.bfloat16,
                                                 B=8, Hq=32, Hkv=8, Nq=1, Nk=32768, d=128, causal=False,
                                                 num_splits=16, seed=SEED_DECODE),

@@ -73,6 +73,16 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
              int Nk, int d, int causal, float scale, int dtype, void* stream);
 
 /*
+ * attn_fwd_window: causal prefill with a sliding window ("Attention Computation in Practice",
+ * "Masking variants": sliding window i - W < j <= i). Same layouts, dtypes and errors as
+ * attn_fwd with causal = 1; query i sees keys j with i' - window < j <= i', i' = i + (Nk - Nq).
+ * K/V tiles entirely outside every row's window are not read. window >= 1, else INVALID_ARG;
+ * window >= Nk gives the plain causal result.
+ */
+int attn_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+                    int Nk, int d, int window, float scale, int dtype, void* stream);
+
+/*
  * attn_decode_workspace_size: bytes of caller-provided workspace attn_decode needs for the
  * per-split partial states (m, l, o[d]) in fp32.
  */
@@ -187,6 +197,15 @@ int attn_varlen(const void* q, const void* k, const void* v, void* o, float* lse
                 const int32_t* cu_seqlens_k, int num_seqs, int total_q, int total_k, int max_seqlen_q,
                 int max_seqlen_k, int Hq, int Hkv, int d, int causal, float scale, void* workspace,
                 size_t workspace_bytes, void* stream);
+
+/*
+ * attn_varlen_window: attn_varlen with causal = 1 and a sliding window of `window` keys ending
+ * at each query's causal limit (aligned to each sequence's end). window >= 1, else INVALID_ARG.
+ */
+int attn_varlen_window(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens_q,
+                       const int32_t* cu_seqlens_k, int num_seqs, int total_q, int total_k, int max_seqlen_q,
+                       int max_seqlen_k, int Hq, int Hkv, int d, int window, float scale, void* workspace,
+                       size_t workspace_bytes, void* stream);
 
 /* ---- status and diagnostics ---- */
 

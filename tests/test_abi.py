@@ -28,7 +28,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ("attn_fwd", "attn_decode", "attn_decode_paged", "attn_varlen", "attn_decode_workspace_size", "attn_varlen_workspace_size",
+    for n in ("attn_fwd", "attn_fwd_window", "attn_decode", "attn_decode_paged", "attn_varlen", "attn_varlen_window",
+              "attn_decode_workspace_size", "attn_varlen_workspace_size",
               "bwattn_get_status", "bwattn_clear_status", "bwattn_last_cuda_error", "bwattn_status_string",
               "bwattn_set_wait_timeout_ns", "bwattn_test_wait_timeout", "bwattn_launch_count", "bwattn_version"):
         assert n in names
@@ -111,6 +112,38 @@ def test_varlen_argument_errors(L):
     assert var(d=64) == bw.ERR_UNSUPPORTED
     assert var(n=0) == bw.OK
     assert L.attn_varlen_workspace_size(3, 16, 8, 2, 128) > 0
+
+
+def test_window_argument_errors(L):
+    def fw(window, **kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, B=1, Hq=2, Hkv=1, Nq=8, Nk=8, d=128, scale=0.1,
+                 dtype=bw.DTYPE_BF16, stream=None)
+        a.update(kw)
+        return L.attn_fwd_window(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Hq"], a["Hkv"], a["Nq"],
+                                 a["Nk"], a["d"], window, a["scale"], a["dtype"], a["stream"])
+
+    def vw(window, **kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, cq=FAKE, ck=FAKE, n=3, tq=10, tk=30, mq=8, mk=16, Hq=8,
+                 Hkv=2, d=128, scale=0.1, ws=FAKE, wsb=1 << 30, stream=None)
+        a.update(kw)
+        return L.attn_varlen_window(a["q"], a["k"], a["v"], a["o"], a["lse"], a["cq"], a["ck"], a["n"], a["tq"],
+                                    a["tk"], a["mq"], a["mk"], a["Hq"], a["Hkv"], a["d"], window, a["scale"], a["ws"],
+                                    a["wsb"], a["stream"])
+    for w in (0, -1, -(1 << 31)):
+        assert fw(w) == bw.ERR_INVALID_ARG
+        assert vw(w) == bw.ERR_INVALID_ARG
+    assert fw(4, q=None) == bw.ERR_INVALID_ARG
+    assert fw(4, d=96) == bw.ERR_UNSUPPORTED
+    assert fw(4, B=0, q=None, k=None, v=None, o=None) == bw.OK
+    assert vw(4, cq=None) == bw.ERR_INVALID_ARG
+    assert vw(4, n=0) == bw.OK
+
+
+def test_python_binding_rejects_window_without_causal():
+    import torch
+    q = torch.zeros(1, 1, 8, 64)
+    with pytest.raises(ValueError):
+        bw.attn_fwd(q, q, q, causal=False, window=4)
 
 
 def test_python_binding_rejects_host_tensors():

@@ -79,3 +79,15 @@ def test_decode_bytes_of_workloads():
     b4 = roofline.decode_kv_bytes([262144], 8, 128)
     assert b4 == b
     assert math.isclose(roofline.decode_partial_bytes(8, 32, 128, 16), 8 * 32 * 16 * 130 * 4)
+
+
+def test_window_pairs_closed_form():
+    # square, window W: rows i < W see i + 1 keys, the rest see W
+    for n, w in ((4096, 1024), (100, 1), (100, 100), (37, 500)):
+        wc = min(w, n)
+        closed = wc * (wc + 1) // 2 + (n - wc) * wc
+        assert roofline.prefill_visible_pairs(n, n, True, w) == closed
+    assert roofline.prefill_visible_pairs(300, 300, True, 10**6) == roofline.prefill_visible_pairs(300, 300, True)
+    # bottom-right alignment: 2 queries over 10 keys, W 3 -> keys 6..8 and 7..9
+    assert roofline.prefill_visible_pairs(2, 10, True, 3) == 6
+    assert roofline.window_prefill_flops(1, 1, 2, 10, 64, 3) == 4 * 64 * 6

@@ -287,6 +287,107 @@ def test_varlen_workload_full_size_sampled_rows():
     assert torch.isfinite(o).all()
 
 
+# ------------------------------------------------------------------ sliding window
+# "Attention Computation in Practice", Masking variants: query i sees keys i' - W < j <= i'.
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d,W", [
+    (2, 4, 2, 200, 333, 64, 50),
+    (1, 1, 1, 130, 60, 128, 17),     # more queries than keys
+    (1, 2, 1, 300, 300, 128, 1),     # each row sees its diagonal key only
+])
+def test_fp32_prefill_window(B, Hq, Hkv, Nq, Nk, d, W):
+    q, k, v = wl.prefill_inputs(B, Hq, Hkv, Nq, Nk, d, torch.float32, seed=3 + Nq + W)
+    o_ref, lse_ref = oracle.attention(f64(q), f64(k), f64(v), True, method="tiled", block=128, window=W)
+    o, lse = bw.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True, window=W)
+    torch.cuda.synchronize()
+    assert np.abs(f64(o) - o_ref).max() <= TOL_FP32_MAX
+    lg = f64(lse)
+    assert np.all(np.isneginf(lg) == np.isneginf(lse_ref))
+    fin = np.isfinite(lse_ref)
+    assert np.abs(lg[fin] - lse_ref[fin]).max() <= TOL_FP32_MAX
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d,W", [
+    (2, 4, 2, 640, 640, 128, 200),   # several query and key tiles, window inside one pair
+    (1, 2, 1, 333, 1000, 128, 129),  # ragged, bottom-right, window one past a tile
+    (2, 2, 2, 700, 700, 64, 64),     # head dim 64
+    (1, 1, 1, 512, 512, 128, 1),     # diagonal only
+    (1, 2, 2, 200, 90, 128, 30),     # more queries than keys
+    (1, 4, 2, 4096, 4096, 128, 1000),
+])
+def test_bf16_prefill_window(B, Hq, Hkv, Nq, Nk, d, W):
+    q, k, v = wl.prefill_inputs(B, Hq, Hkv, Nq, Nk, d, torch.bfloat16, seed=13 + Nq + W)
+    o_ref, lse_ref = oracle.attention(f64(q), f64(k), f64(v), True, method="tiled", block=128, window=W)
+    o, lse = bw.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True, window=W)
+    torch.cuda.synchronize()
+    check_bf16(o, o_ref, lse, lse_ref, what=("window", B, Hq, Hkv, Nq, Nk, d, W))
+
+
+def test_bf16_window_covering_every_key_is_plain_causal_bit_for_bit():
+    q, k, v = wl.prefill_inputs(1, 4, 2, 700, 900, 128, torch.bfloat16, seed=31)
+    q, k, v = q.cuda(), k.cuda(), v.cuda()
+    o1, l1 = bw.attn_fwd(q, k, v, causal=True)
+    o2, l2 = bw.attn_fwd(q, k, v, causal=True, window=900)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_window_skips_keys_below_every_row(dtype):
+    # Nq 256, Nk 2048, W 300: row 0 starts at key 1493, so no row sees keys < 1493. Keys below
+    # 1408 sit in K/V tiles no row needs and are never read (NaN there must not reach O); keys
+    # 1408..1492 are read but masked (large finite values there must not change one bit).
+    q, k, v = wl.prefill_inputs(1, 2, 1, 256, 2048, 128, dtype, seed=41)
+    q, k, v = q.cuda(), k.cuda(), v.cuda()
+    o1, l1 = bw.attn_fwd(q, k, v, causal=True, window=300)
+    k2, v2 = k.clone(), v.clone()
+    k2[:, :, :1408] = float("nan")
+    v2[:, :, :1408] = float("nan")
+    k2[:, :, 1408:1493] = 3.0e4
+    v2[:, :, 1408:1493] = -3.0e4
+    o2, l2 = bw.attn_fwd(q, k2, v2, causal=True, window=300)
+    torch.cuda.synchronize()
+    assert torch.isfinite(o1).all()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_window_workload_full_size_sampled_rows():
+    x = wl.make("prefill_window_b4_h32_n4096_w1024_d128", device="cuda")
+    w = x["w"]
+    W = w.extra["window"]
+    o, lse = bw.attn_fwd(x["q"], x["k"], x["v"], causal=True, window=W)
+    torch.cuda.synchronize()
+    errs = []
+    for b in (0, w.B - 1):
+        for h in (0, 17, w.Hq - 1):
+            for i in (0, 127, 128, W - 1, W, 2000, 3000, w.Nq - 1):
+                lo = max(0, i + 1 - W)
+                qi = f64(x["q"][b, h, i])[None, None, None]
+                ki = f64(x["k"][b, h, lo:i + 1])[None, None]
+                vi = f64(x["v"][b, h, lo:i + 1])[None, None]
+                o_ref, lse_ref = oracle.attention(qi, ki, vi, False, method="naive")
+                e = np.abs(f64(o[b, h, i]) - o_ref[0, 0, 0])
+                errs.append(e)
+                assert e.max() <= TOL_BF16_MAX, (b, h, i, e.max())
+                assert abs(float(lse[b, h, i]) - lse_ref[0, 0, 0]) <= TOL_LSE
+    assert np.mean(np.concatenate(errs)) <= TOL_BF16_MEAN
+    assert torch.isfinite(o).all()
+
+
+@pytest.mark.parametrize("W", [1, 100, 5000])
+def test_varlen_window(W):
+    nq = [1, 4, 8, 200, 300, 3, 129]
+    nk = [50, 700, 8, 200, 1000, 2100, 129]
+    q, k, v, cq, ck = wl.varlen_inputs(nq, nk, 8, 2, 128, torch.bfloat16, seed=53 + W)
+    o_ref, lse_ref = oracle.varlen(f64(q), f64(k), f64(v), cq.numpy(), ck.numpy(), True, method="tiled", block=128,
+                                   window=W)
+    o, lse = bw.attn_varlen(q.cuda(), k.cuda(), v.cuda(), cq.cuda(), ck.cuda(), max(nq), max(nk), causal=True,
+                            window=W)
+    torch.cuda.synchronize()
+    check_bf16(o, o_ref, lse, lse_ref, what=("varlen window", W))
+
+
 # ------------------------------------------------------------------ status and failure detection
 
 
