@@ -17,6 +17,8 @@ returns numpy float64 arrays. Sources, by page title and section:
   "Attention from the kernel's side", Flash-decoding.
 * GQA by index: "Attention Computation in Practice", GQA in the kernel.
 * varlen: "Attention Computation in Practice", the four attention kernels (APPEND / MIXED).
+* FP8 KV cache: E4M3 codes times a per-(KV head, channel) scale, decoded from the format's
+  definition ("Attention from the kernel's side", Why a quantised cache needs a fused kernel).
 
 Parity pins for every function live in ``tests/test_oracle_pins.py``; none is unpinned.
 """
@@ -70,8 +72,9 @@ def _load():
         lib.oracle_partials.argtypes = [D, D, D, c_int, c_int, c_double, c_int, D, D, D]
         lib.oracle_merge.argtypes = [c_double, c_double, D, c_double, c_double, D, c_int, D, D, D]
         lib.oracle_hardware_threads.argtypes = []
+        lib.oracle_e4m3_decode.argtypes = [ctypes.c_void_p, ctypes.c_int64, D]
         for f in ("oracle_attention", "oracle_decode", "oracle_varlen", "oracle_probs",
-                  "oracle_partials", "oracle_merge", "oracle_hardware_threads"):
+                  "oracle_partials", "oracle_merge", "oracle_hardware_threads", "oracle_e4m3_decode"):
             getattr(lib, f).restype = c_int
         _lib = lib
         return lib
@@ -160,6 +163,32 @@ def decode_paged(q, k_pages, v_pages, block_table, nk, scale: float | None = Non
     B, mp = table.shape
     kc = kp[table].reshape(B, mp * ps, Hkv, d).transpose(0, 2, 1, 3)
     vc = vp[table].reshape(B, mp * ps, Hkv, d).transpose(0, 2, 1, 3)
+    return decode(q, kc, vc, nk, scale=scale, method=method, workers=workers, block=block, nthreads=nthreads)
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """FP8 E4M3 codes (uint8, any shape) -> float64 values of the same shape."""
+    x = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+    out = np.empty(x.shape, dtype=np.float64)
+    rc = _load().oracle_e4m3_decode(x.ctypes.data_as(ctypes.c_void_p), int(x.size), _dp(out))
+    if rc != 0:
+        raise ValueError("oracle_e4m3_decode rejected its arguments")
+    return out
+
+
+def decode_fp8(q, k_codes, v_codes, k_scale, v_scale, nk, scale: float | None = None, method: str = "splitk",
+               workers: int | None = None, block: int | None = None, nthreads: int = 0):
+    """Decode against an FP8 KV cache: caches [B, Hkv, cap, d] of E4M3 codes (uint8), scales
+    [Hkv, d]; the cached value is e4m3(code) * scale[head, channel] ("Attention from the
+    kernel's side", Why a quantised cache needs a fused kernel). The caches are decoded to
+    float64 and passed to ``decode``."""
+    kq, vq = np.asarray(k_codes, dtype=np.uint8), np.asarray(v_codes, dtype=np.uint8)
+    ks, vs = _f64(k_scale), _f64(v_scale)
+    B, Hkv, cap, d = kq.shape
+    if ks.shape != (Hkv, d) or vs.shape != (Hkv, d) or vq.shape != kq.shape:
+        raise ValueError("k/v codes [B, Hkv, cap, d] and scales [Hkv, d] expected")
+    kc = e4m3_decode(kq) * ks[None, :, None, :]
+    vc = e4m3_decode(vq) * vs[None, :, None, :]
     return decode(q, kc, vc, nk, scale=scale, method=method, workers=workers, block=block, nthreads=nthreads)
 
 

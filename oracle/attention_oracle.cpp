@@ -372,6 +372,32 @@ int oracle_merge(double ma, double la, const double* oa, double mb, double lb, c
   return 0;
 }
 
+// FP8 E4M3 code -> value (the 8-bit float of the OCP FP8 formats: 1 sign bit, 4 exponent bits
+// with bias 7, 3 mantissa bits; exponent field 0 is subnormal (m/8 * 2^-6); no infinities, the
+// codes S.1111.111 are NaN; largest finite 448). Used for the FP8 KV cache, whose value is this
+// decoded code times a per-(KV head, channel) scale ("Attention from the kernel's side", Why a
+// quantised cache needs a fused kernel: the cache stores a narrow code plus a scale, and the
+// kernel turns the codes into values as it reads them).
+int oracle_e4m3_decode(const uint8_t* x, int64_t n, double* out) {
+  if (n < 0 || (n > 0 && (!x || !out))) return 1;
+  for (int64_t i = 0; i < n; ++i) {
+    const int b = x[i];
+    const double sign = (b & 0x80) ? -1.0 : 1.0;
+    const int e = (b >> 3) & 0xF;
+    const int m = b & 0x7;
+    double mag;
+    if (e == 0xF && m == 0x7) {
+      mag = std::numeric_limits<double>::quiet_NaN();
+    } else if (e == 0) {
+      mag = std::ldexp(static_cast<double>(m) / 8.0, -6);
+    } else {
+      mag = std::ldexp(1.0 + static_cast<double>(m) / 8.0, e - 7);
+    }
+    out[i] = sign * mag;
+  }
+  return 0;
+}
+
 int oracle_hardware_threads(void) {
   unsigned hw = std::thread::hardware_concurrency();
   return hw ? static_cast<int>(hw) : 1;

@@ -493,3 +493,109 @@ def test_window_brute_force_and_varlen():
                                   V[ck[s_]:ck[s_ + 1]].transpose(1, 0, 2)[None], True, window=2, method="tiled",
                                   block=2)
         assert np.array_equal(ov[cq[s_]:cq[s_ + 1]], od[0].transpose(1, 0, 2))
+
+
+# ---------------------------------------------------------------- FP8 (E4M3) KV cache
+# The cached value is e4m3(code) * scale[KV head, channel] ("Attention from the kernel's side",
+# Why a quantised cache needs a fused kernel); the code format is the OCP FP8 E4M3 float.
+
+
+def test_e4m3_decode_matches_torch_for_every_code():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_decode(codes)
+    theirs = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(theirs)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert list(np.flatnonzero(nan)) == [0x7F, 0xFF]
+    assert np.array_equal(ours[~nan], theirs[~nan])
+    assert np.array_equal(np.signbit(ours[~nan]), np.signbit(theirs[~nan]))
+
+
+def test_e4m3_landmarks_and_order():
+    v = oracle.e4m3_decode(np.arange(256, dtype=np.uint8))
+    assert v[0x38] == 1.0 and v[0x30] == 0.5 and v[0x40] == 2.0
+    assert v[0x7E] == 448.0                 # largest finite
+    assert v[0x01] == 2.0 ** -9             # smallest subnormal
+    assert v[0x08] == 2.0 ** -6             # smallest normal
+    assert v[0x07] == 7 * 2.0 ** -9         # largest subnormal
+    assert v[0x00] == 0.0 and np.signbit(v[0x80]) and v[0x80] == 0.0
+    pos = v[:0x7F]
+    assert np.all(np.diff(pos) > 0)        # codes 0..126 strictly increasing
+    assert np.array_equal(v[0x80:0xFF], -pos)  # sign-magnitude
+    # spacing: 8 values per binade above the subnormals
+    for e in range(1, 15):
+        run = pos[8 * e:8 * e + 8]
+        assert np.allclose(np.diff(run), 2.0 ** (e - 7) / 8, rtol=0, atol=0)
+
+
+def test_e4m3_round_trip_through_torch_quantiser():
+    r = rng(61)
+    x = torch.from_numpy(np.clip(randn(r, 4096) * 100, -448, 448)).to(torch.float32)
+    codes = x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    back = x.to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(oracle.e4m3_decode(codes), back)
+    # relative rounding error of a normal value is at most half a unit in the last place (2^-4)
+    xn = x.double().numpy()
+    big = np.abs(xn) >= 2.0 ** -6
+    assert np.max(np.abs(back[big] - xn[big]) / np.abs(xn[big])) <= 2.0 ** -4
+
+
+def fp8_cache(r, B, Hkv, cap, d):
+    k = r.integers(0, 256, size=(B, Hkv, cap, d), dtype=np.uint8)
+    v = r.integers(0, 256, size=(B, Hkv, cap, d), dtype=np.uint8)
+    # no NaN codes: a saturating quantiser never writes them
+    k[(k & 0x7F) == 0x7F] = 0x7E
+    v[(v & 0x7F) == 0x7F] = 0x7E
+    ks = r.uniform(0.5, 2.0, size=(Hkv, d)) / 64
+    vs = r.uniform(0.5, 2.0, size=(Hkv, d)) / 64
+    return k, v, ks, vs
+
+
+def test_decode_fp8_matches_torch_sdpa_on_torch_dequantised_cache():
+    r = rng(62)
+    B, Hq, Hkv, cap, d = 2, 4, 2, 40, 16
+    k8, v8, ks, vs = fp8_cache(r, B, Hkv, cap, d)
+    q = randn(r, B, Hq, d)
+    nk = np.array([40, 17], dtype=np.int32)
+    o, lse = oracle.decode_fp8(q, k8, v8, ks, vs, nk, method="splitk", workers=3)
+
+    def deq(c, s):
+        return torch.from_numpy(c).view(torch.float8_e4m3fn).to(torch.float64) * torch.from_numpy(s)[None, :, None, :]
+    K, V = deq(k8, ks), deq(v8, vs)
+    for b in range(B):
+        for h in range(Hq):
+            kk = K[b, h // 2, :nk[b]][None, None]
+            vv = V[b, h // 2, :nk[b]][None, None]
+            qq = torch.from_numpy(q[b, h])[None, None, None]
+            ref = torch.nn.functional.scaled_dot_product_attention(qq, kk, vv)[0, 0, 0].numpy()
+            assert np.max(np.abs(o[b, h] - ref)) <= 1e-12
+            s = (kk[0, 0].numpy() @ q[b, h]) / math.sqrt(d)
+            assert abs(lse[b, h] - logsumexp(s)) <= 1e-12
+
+
+def test_decode_fp8_closed_forms():
+    r = rng(63)
+    B, Hq, Hkv, cap, d = 1, 2, 1, 33, 8
+    k8, v8, ks, vs = fp8_cache(r, B, Hkv, cap, d)
+    nk = np.array([33], dtype=np.int32)
+    # zero query: the mean of the decoded values times the value scale, LSE = ln n
+    o, lse = oracle.decode_fp8(np.zeros((B, Hq, d)), k8, v8, ks, vs, nk, method="naive")
+    torch_v = torch.from_numpy(v8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    mean = torch_v[0, 0].mean(axis=0) * vs[0]
+    assert np.max(np.abs(o[0] - mean[None])) <= 1e-14
+    assert np.max(np.abs(lse - math.log(33))) <= 1e-14
+    # doubling the value scale doubles O exactly; the key scale acts like the softmax scale
+    q = randn(r, B, Hq, d)
+    o1, l1 = oracle.decode_fp8(q, k8, v8, ks, vs, nk, method="tiled", block=4)
+    o2, l2 = oracle.decode_fp8(q, k8, v8, ks, 2 * vs, nk, method="tiled", block=4)
+    assert np.array_equal(o2, 2 * o1) and np.array_equal(l1, l2)
+    ones = np.ones_like(ks)
+    o3, l3 = oracle.decode_fp8(q, k8, v8, 3 * ones, vs, nk, method="naive")
+    o4, l4 = oracle.decode_fp8(q, k8, v8, ones, vs, nk, method="naive", scale=3 / math.sqrt(d))
+    # (the codes reach 448, so scores and LSE are large: compare LSE relative to its size)
+    assert np.max(np.abs(o3 - o4)) <= 1e-13 and np.max(np.abs(l3 - l4) / np.maximum(1, np.abs(l3))) <= 1e-14
+    # NaN codes decode to NaN (the format has no infinities)
+    bad = k8.copy()
+    bad[0, 0, 0, 0] = 0x7F
+    o5, _ = oracle.decode_fp8(q, bad, v8, ks, vs, nk, method="naive")
+    assert np.isnan(o5).all()
