@@ -251,6 +251,39 @@ def run_reference(args, rank, world):
 # ------------------------------------------------------------------ single-part runs (profiling aid)
 
 
+def bench_fp8(name, args, world, stream, dev, peaks):
+    """FP8 (E4M3) KV-cache decode: KV bytes are one per element (plus the [Hkv, d] scales)."""
+    x = wl.make(name, device=dev)
+    w = x["w"]
+    nk = x["nk"].to(dev)
+    o = torch.empty_like(x["q"])
+    lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
+    ws = torch.empty(bw.decode_workspace_size(w.B, w.Hq, w.d, w.num_splits), dtype=torch.uint8, device=dev)
+    if w.kind == "decode_paged_fp8":
+        fn = lambda: bw.attn_decode_paged_fp8(x["q"], x["k_pages"], x["v_pages"], x["k_scale"],  # noqa: E731
+                                              x["v_scale"], x["block_table"], nk, w.num_splits, workspace=ws,
+                                              out=o, lse=lse)
+    else:
+        fn = lambda: bw.attn_decode_fp8(x["q"], x["kcache"], x["vcache"], x["k_scale"], x["v_scale"],  # noqa: E731
+                                        nk, w.num_splits, workspace=ws, out=o, lse=lse)
+    per, _ = time_steps(fn, args.steps, args.warmup, world, stream)
+    ms = max_over_ranks(statistics.mean(per), world)
+    kvb = rl.decode_kv_bytes([w.Nk] * w.B, w.Hkv, w.d, elem_bytes=1)
+    gbs = kvb / (ms * 1e-3) / 1e9
+    out = {"metric": "decode KV-cache GB/s (FP8 E4M3 codes)", "value": gbs * world, "unit": "GB/s",
+           "ms_per_step": ms, "num_splits": w.num_splits,
+           "keys_per_s": float(w.Nk) * w.B * w.Hkv * world / (ms * 1e-3),
+           "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": kvb, "traffic": None,
+                        "note": "split-K pass, codes turned into f16 in registers" +
+                                (", fused merge" if w.num_splits <= 32 else ", separate merge")}}
+    if "page_size" in w.extra:
+        out["page_size"] = w.extra["page_size"]
+    del x, o, lse, ws, nk
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_case(args, world, stream, dev, peaks):
     out = {"case": args.case}
     if args.case == "prefill":
@@ -275,6 +308,11 @@ def run_case(args, world, stream, dev, peaks):
         ms = statistics.mean(per)
         out.update({"B": B, "window": W, "ms": ms,
                     "tflops": rl.window_prefill_flops(B, w.Hq, w.Nq, w.Nk, w.d, W) / ms / 1e9, "launches": n})
+    elif args.case == "fp8":
+        for name in ("decode_fp8_gqa_b8_h32x8_n32768_d128", "decode_fp8_paged_b8_h32x8_n32768_d128_p16",
+                     "decode_fp8_long_b1_h64x8_n262144_d128"):
+            r = bench_fp8(name, args, world, stream, dev, peaks)
+            out[name] = {"ms": r["ms_per_step"], "GB/s": r["value"], "frac": r["roofline"]["frac"]}
     elif args.case == "paged":
         x = wl.make("decode_paged_b8_h32x8_n32768_d128_p16", device=dev)
         wd = x["w"]
@@ -325,7 +363,8 @@ def main():
     ap.add_argument("--impl", default="own", choices=["own", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-breakdown", action="store_true")
-    ap.add_argument("--case", default="all", choices=["all", "prefill", "window", "decode", "paged", "varlen"],
+    ap.add_argument("--case", default="all",
+                    choices=["all", "prefill", "window", "decode", "paged", "fp8", "varlen"],
                     help="profiling aid: run one part only (no e2e, no CPU baseline)")
     ap.add_argument("--batch", type=int, default=0, help="profiling aid: override the prefill batch size")
     args = ap.parse_args()
@@ -428,6 +467,9 @@ def main():
                                            "traffic": None, "note": "paged split-K pass with the fused merge"}}
         del xp, wsp, op, lp, nkp
         torch.cuda.empty_cache()
+        for name in ("decode_fp8_gqa_b8_h32x8_n32768_d128", "decode_fp8_paged_b8_h32x8_n32768_d128_p16",
+                     "decode_fp8_long_b1_h64x8_n262144_d128"):
+            breakdown[name] = bench_fp8(name, args, world, stream, dev, peaks)
         xw = wl.make("prefill_window_b4_h32_n4096_w1024_d128", device=dev)
         ww = xw["w"]
         W = ww.extra["window"]

@@ -65,6 +65,8 @@ def lib() -> ctypes.CDLL:
         L.attn_decode.argtypes = [vp, vp, vp, vp, vp] + [ci] * 6 + [cf, vp, vp, sz, vp]
         L.attn_decode.restype = ci
         L.attn_decode_paged.argtypes = [vp] * 6 + [ci] * 8 + [cf, vp, vp, sz, vp]
+        L.attn_decode_fp8.argtypes = [vp] * 7 + [ci] * 6 + [cf, vp, vp, sz, vp]
+        L.attn_decode_paged_fp8.argtypes = [vp] * 8 + [ci] * 8 + [cf, vp, vp, sz, vp]
         L.attn_decode_paged.restype = ci
         L.attn_varlen_workspace_size.argtypes = [ci] * 5
         L.attn_varlen_workspace_size.restype = sz
@@ -242,6 +244,84 @@ def attn_decode_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Ten
                                  _ptr(lse_t), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                  _stream(stream))
     _check(rc, "attn_decode_paged")
+    return out, lse_t
+
+
+_FP8_CODES = (torch.uint8, torch.float8_e4m3fn)
+
+
+def _fp8_cache(k, v, k_scale, v_scale, Hkv, d, names):
+    for t, n in ((k, names[0]), (v, names[1])):
+        _cuda(t, n)
+        if t.dtype not in _FP8_CODES:
+            raise ValueError(f"{n} must hold E4M3 codes (uint8 or float8_e4m3fn), got {t.dtype}")
+    for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        _cuda(t, n, torch.float32)
+        if tuple(t.shape) != (Hkv, d):
+            raise ValueError(f"{n} must be [Hkv, d] = [{Hkv}, {d}]")
+
+
+def _decode_outputs(q, B, Hq, d, num_splits, out, lse, workspace):
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda(out, "out", torch.bfloat16)
+    lse_t = None
+    if lse is True:
+        lse_t = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    elif isinstance(lse, torch.Tensor):
+        lse_t = lse
+        _cuda(lse_t, "lse", torch.float32)
+    need = decode_workspace_size(B, Hq, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _cuda(workspace, "workspace")
+    return out, lse_t, workspace
+
+
+def attn_decode_fp8(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Tensor, k_scale: torch.Tensor,
+                    v_scale: torch.Tensor, nk: torch.Tensor, num_splits: int, scale: float | None = None,
+                    workspace: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                    lse: torch.Tensor | bool | None = True, stream=None):
+    """Decode against an FP8 cache. q [B, Hq, d] bf16; caches [B, Hkv, cap, d] of E4M3 codes;
+    k_scale, v_scale [Hkv, d] fp32 (value = e4m3(code) * scale[head, channel]); nk [B] int32."""
+    if q.dim() != 3 or kcache.dim() != 4:
+        raise ValueError("q must be [B, Hq, d] and caches [B, Hkv, cap, d]")
+    B, Hq, d = q.shape
+    Bk, Hkv, cap, dk = kcache.shape
+    if Bk != B or dk != d or tuple(vcache.shape) != tuple(kcache.shape):
+        raise ValueError("kcache and vcache must be [B, Hkv, cap, d] with q's B and d")
+    _cuda(q, "q", torch.bfloat16)
+    _fp8_cache(kcache, vcache, k_scale, v_scale, Hkv, d, ("kcache", "vcache"))
+    _cuda(nk, "nk", torch.int32)
+    out, lse_t, workspace = _decode_outputs(q, B, Hq, d, num_splits, out, lse, workspace)
+    rc = lib().attn_decode_fp8(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(k_scale), _ptr(v_scale), _ptr(out), _ptr(nk),
+                               B, Hq, Hkv, cap, d, int(num_splits), _scale(scale, d), _ptr(lse_t), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "attn_decode_fp8")
+    return out, lse_t
+
+
+def attn_decode_paged_fp8(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor, k_scale: torch.Tensor,
+                          v_scale: torch.Tensor, block_table: torch.Tensor, nk: torch.Tensor, num_splits: int,
+                          scale: float | None = None, workspace: torch.Tensor | None = None,
+                          out: torch.Tensor | None = None, lse: torch.Tensor | bool | None = True, stream=None):
+    """Paged decode against FP8 pages [num_pages, page_size, Hkv, d] of E4M3 codes."""
+    if q.dim() != 3 or k_pages.dim() != 4 or block_table.dim() != 2:
+        raise ValueError("q must be [B, Hq, d], pages [num_pages, page_size, Hkv, d], block_table [B, max_pages]")
+    B, Hq, d = q.shape
+    num_pages, page_size, Hkv, dk = k_pages.shape
+    if dk != d or tuple(v_pages.shape) != tuple(k_pages.shape) or block_table.shape[0] != B:
+        raise ValueError("k_pages and v_pages must be [num_pages, page_size, Hkv, d]; block_table [B, max_pages]")
+    _cuda(q, "q", torch.bfloat16)
+    _fp8_cache(k_pages, v_pages, k_scale, v_scale, Hkv, d, ("k_pages", "v_pages"))
+    _cuda(block_table, "block_table", torch.int32)
+    _cuda(nk, "nk", torch.int32)
+    out, lse_t, workspace = _decode_outputs(q, B, Hq, d, num_splits, out, lse, workspace)
+    rc = lib().attn_decode_paged_fp8(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(k_scale), _ptr(v_scale), _ptr(out),
+                                     _ptr(block_table), _ptr(nk), B, Hq, Hkv, page_size, num_pages,
+                                     block_table.shape[1], d, int(num_splits), _scale(scale, d), _ptr(lse_t),
+                                     _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "attn_decode_paged_fp8")
     return out, lse_t
 
 

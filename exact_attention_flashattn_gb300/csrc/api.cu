@@ -308,47 +308,25 @@ size_t attn_decode_workspace_size(int B, int Hq, int d, int num_splits) {
   return bw::splitk_ws_bytes(B, num_splits, Hq, d);
 }
 
-int attn_decode(const void* q, const void* kcache, const void* vcache, void* o, const int32_t* nk, int B, int Hq,
-                int Hkv, int nk_cap, int d, int num_splits, float scale, float* lse, void* workspace,
-                size_t workspace_bytes, void* stream) {
-  if (B < 0 || Hq <= 0 || Hkv <= 0 || nk_cap < 0 || d <= 0) return BWATTN_ERR_INVALID_ARG;
-  if (Hq % Hkv != 0 || !good_scale(scale) || num_splits < 1 || num_splits > 1024) return BWATTN_ERR_INVALID_ARG;
-  if (B > 65535) return BWATTN_ERR_INVALID_ARG;
-  const int g = Hq / Hkv;
-  if (d != 128 || g > 32 || Hkv > 32767) return BWATTN_ERR_UNSUPPORTED;
-  if (B == 0) return BWATTN_OK;
-  if (!q || !kcache || !vcache || !o || !nk || !workspace) return BWATTN_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) || !aligned16(workspace) ||
-      !aligned4(nk) || (lse && !aligned4(lse)))
-    return BWATTN_ERR_INVALID_ARG;
-  // workspace: units = B * Hkv, rows_max = g
-  const size_t need = bw::splitk_ws_bytes(B * Hkv, num_splits, g, d);
-  if (workspace_bytes < need) return BWATTN_ERR_INVALID_ARG;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const float sl2 = scale * bw::kLog2e;
-  bw::SplitKArgs a{};
-  a.q = static_cast<const uint16_t*>(q);
-  a.k = static_cast<const uint16_t*>(kcache);
-  a.v = static_cast<const uint16_t*>(vcache);
-  a.ws = static_cast<float*>(workspace);
+}  // extern "C"
+
+namespace {
+
+// The split-K launch of a decode call, then the separate merge when the splits are not merged
+// by the split kernel itself.
+int run_decode(bw::SplitKArgs& a, int B, int Hq, int Hkv, int g, int num_splits, const int32_t* nk, void* o,
+               float* lse, cudaStream_t st) {
   a.nk = nk;
-  a.cu_q = a.cu_k = nullptr;
   a.num_seqs = B;
   a.Hq = Hq;
   a.Hkv = Hkv;
   a.g = g;
-  a.kv_seq_stride = static_cast<int64_t>(Hkv) * nk_cap * d;
-  a.kv_head_stride = static_cast<int64_t>(nk_cap) * d;
-  a.kv_key_stride = d;
-  a.kv_cap = nk_cap;
-  a.total_q = a.total_k = 0;
   a.num_splits = num_splits;
   a.rows_max = g;
   a.row_groups = (g + 15) / 16;
   a.causal = 0;
   a.small_rows_limit = g;
   a.ws_o_offset = bw::splitk_o_offset(B * Hkv, num_splits, g);
-  a.scale_log2 = sl2;
   cudaError_t e;
   if (num_splits <= kFusedMergeMaxSplits &&
       (e = bw::merge_tickets(B * Hkv * a.row_groups, &a.tickets)) != cudaSuccess)
@@ -378,10 +356,51 @@ int attn_decode(const void* q, const void* kcache, const void* vcache, void* o, 
   return BWATTN_OK;
 }
 
-int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages, void* o, const int32_t* block_table,
-                      const int32_t* nk, int B, int Hq, int Hkv, int page_size, int num_pages, int max_pages_per_seq,
-                      int d, int num_splits, float scale, float* lse, void* workspace, size_t workspace_bytes,
-                      void* stream) {
+// Contiguous cache [B, Hkv, nk_cap, d]; bf16 (k_scale == v_scale == nullptr, fp8 false) or FP8
+// E4M3 codes with per-(KV head, channel) scales.
+int decode_contig(const void* q, const void* kcache, const void* vcache, const float* k_scale, const float* v_scale,
+                  bool fp8, void* o, const int32_t* nk, int B, int Hq, int Hkv, int nk_cap, int d, int num_splits,
+                  float scale, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || nk_cap < 0 || d <= 0) return BWATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || !good_scale(scale) || num_splits < 1 || num_splits > 1024) return BWATTN_ERR_INVALID_ARG;
+  if (B > 65535) return BWATTN_ERR_INVALID_ARG;
+  const int g = Hq / Hkv;
+  if (d != 128 || g > 32 || Hkv > 32767) return BWATTN_ERR_UNSUPPORTED;
+  if (B == 0) return BWATTN_OK;
+  if (!q || !kcache || !vcache || !o || !nk || !workspace) return BWATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) || !aligned16(workspace) ||
+      !aligned4(nk) || (lse && !aligned4(lse)))
+    return BWATTN_ERR_INVALID_ARG;
+  if (fp8 && (!k_scale || !v_scale || !aligned16(k_scale) || !aligned16(v_scale))) return BWATTN_ERR_INVALID_ARG;
+  // workspace: units = B * Hkv, rows_max = g
+  if (workspace_bytes < bw::splitk_ws_bytes(B * Hkv, num_splits, g, d)) return BWATTN_ERR_INVALID_ARG;
+  bw::SplitKArgs a{};
+  a.q = static_cast<const uint16_t*>(q);
+  if (fp8) {
+    a.k8 = static_cast<const uint8_t*>(kcache);
+    a.v8 = static_cast<const uint8_t*>(vcache);
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+  } else {
+    a.k = static_cast<const uint16_t*>(kcache);
+    a.v = static_cast<const uint16_t*>(vcache);
+  }
+  a.ws = static_cast<float*>(workspace);
+  a.cu_q = a.cu_k = nullptr;
+  a.kv_seq_stride = static_cast<int64_t>(Hkv) * nk_cap * d;
+  a.kv_head_stride = static_cast<int64_t>(nk_cap) * d;
+  a.kv_key_stride = d;
+  a.kv_cap = nk_cap;
+  a.total_q = a.total_k = 0;
+  a.scale_log2 = scale * bw::kLog2e;
+  return run_decode(a, B, Hq, Hkv, g, num_splits, nk, o, lse, static_cast<cudaStream_t>(stream));
+}
+
+// Paged cache [num_pages, page_size, Hkv, d] through a block table; bf16 or FP8 as above.
+int decode_paged(const void* q, const void* k_pages, const void* v_pages, const float* k_scale, const float* v_scale,
+                 bool fp8, void* o, const int32_t* block_table, const int32_t* nk, int B, int Hq, int Hkv,
+                 int page_size, int num_pages, int max_pages_per_seq, int d, int num_splits, float scale, float* lse,
+                 void* workspace, size_t workspace_bytes, void* stream) {
   if (B < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || num_pages <= 0 || max_pages_per_seq <= 0)
     return BWATTN_ERR_INVALID_ARG;
   if (page_size < 16 || page_size > 1024 || page_size % 16 != 0) return BWATTN_ERR_INVALID_ARG;
@@ -394,56 +413,62 @@ int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages, v
   if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o) || !aligned16(workspace) ||
       !aligned4(block_table) || !aligned4(nk) || (lse && !aligned4(lse)))
     return BWATTN_ERR_INVALID_ARG;
+  if (fp8 && (!k_scale || !v_scale || !aligned16(k_scale) || !aligned16(v_scale))) return BWATTN_ERR_INVALID_ARG;
   if (workspace_bytes < bw::splitk_ws_bytes(B * Hkv, num_splits, g, d)) return BWATTN_ERR_INVALID_ARG;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   bw::SplitKArgs a{};
   a.q = static_cast<const uint16_t*>(q);
-  a.k = static_cast<const uint16_t*>(k_pages);
-  a.v = static_cast<const uint16_t*>(v_pages);
+  if (fp8) {
+    a.k8 = static_cast<const uint8_t*>(k_pages);
+    a.v8 = static_cast<const uint8_t*>(v_pages);
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+  } else {
+    a.k = static_cast<const uint16_t*>(k_pages);
+    a.v = static_cast<const uint16_t*>(v_pages);
+  }
   a.ws = static_cast<float*>(workspace);
-  a.nk = nk;
-  a.num_seqs = B;
-  a.Hq = Hq;
-  a.Hkv = Hkv;
-  a.g = g;
   a.kv_head_stride = d;
   a.kv_key_stride = static_cast<int64_t>(Hkv) * d;
-  a.num_splits = num_splits;
-  a.rows_max = g;
-  a.row_groups = (g + 15) / 16;
-  a.small_rows_limit = g;
-  a.ws_o_offset = bw::splitk_o_offset(B * Hkv, num_splits, g);
   a.scale_log2 = scale * bw::kLog2e;
   a.block_table = block_table;
   a.page_size = page_size;
   a.max_pages = max_pages_per_seq;
   a.num_pages = num_pages;
-  cudaError_t e;
-  if (num_splits <= kFusedMergeMaxSplits &&
-      (e = bw::merge_tickets(B * Hkv * a.row_groups, &a.tickets)) != cudaSuccess)
-    return cuda_fail(e);
-  a.o = static_cast<uint16_t*>(o);
-  a.lse = lse;
-  if ((e = bw::launch_splitk(a, st)) != cudaSuccess) return cuda_fail(e);
-  g_launches.fetch_add(1);
-  if (a.tickets) return BWATTN_OK;  // merged by the last CTA of each unit
-  bw::MergeArgs m{};
-  m.ws = a.ws;
-  m.o = static_cast<uint16_t*>(o);
-  m.lse = lse;
-  m.nk = nk;
-  m.num_seqs = B;
-  m.Hq = Hq;
-  m.Hkv = Hkv;
-  m.g = g;
-  m.num_splits = num_splits;
-  m.rows_max = g;
-  m.small_rows_limit = g;
-  m.total_q = B;
-  m.ws_o_offset = a.ws_o_offset;
-  if ((e = bw::launch_merge(m, st)) != cudaSuccess) return cuda_fail(e);
-  g_launches.fetch_add(1);
-  return BWATTN_OK;
+  return run_decode(a, B, Hq, Hkv, g, num_splits, nk, o, lse, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_decode(const void* q, const void* kcache, const void* vcache, void* o, const int32_t* nk, int B, int Hq,
+                int Hkv, int nk_cap, int d, int num_splits, float scale, float* lse, void* workspace,
+                size_t workspace_bytes, void* stream) {
+  return decode_contig(q, kcache, vcache, nullptr, nullptr, false, o, nk, B, Hq, Hkv, nk_cap, d, num_splits, scale,
+                       lse, workspace, workspace_bytes, stream);
+}
+
+int attn_decode_fp8(const void* q, const void* kcache, const void* vcache, const float* k_scale,
+                    const float* v_scale, void* o, const int32_t* nk, int B, int Hq, int Hkv, int nk_cap, int d,
+                    int num_splits, float scale, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_contig(q, kcache, vcache, k_scale, v_scale, true, o, nk, B, Hq, Hkv, nk_cap, d, num_splits, scale,
+                       lse, workspace, workspace_bytes, stream);
+}
+
+int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages, void* o, const int32_t* block_table,
+                      const int32_t* nk, int B, int Hq, int Hkv, int page_size, int num_pages, int max_pages_per_seq,
+                      int d, int num_splits, float scale, float* lse, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  return decode_paged(q, k_pages, v_pages, nullptr, nullptr, false, o, block_table, nk, B, Hq, Hkv, page_size,
+                      num_pages, max_pages_per_seq, d, num_splits, scale, lse, workspace, workspace_bytes, stream);
+}
+
+int attn_decode_paged_fp8(const void* q, const void* k_pages, const void* v_pages, const float* k_scale,
+                          const float* v_scale, void* o, const int32_t* block_table, const int32_t* nk, int B, int Hq,
+                          int Hkv, int page_size, int num_pages, int max_pages_per_seq, int d, int num_splits,
+                          float scale, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_paged(q, k_pages, v_pages, k_scale, v_scale, true, o, block_table, nk, B, Hq, Hkv, page_size,
+                      num_pages, max_pages_per_seq, d, num_splits, scale, lse, workspace, workspace_bytes, stream);
 }
 
 size_t attn_varlen_workspace_size(int num_seqs, int max_seqlen_k, int Hq, int Hkv, int d) {

@@ -56,6 +56,12 @@ struct SplitKArgs {
   // row j % page_size (page_size a multiple of 16, so a 16-key step never crosses a page)
   const int32_t* block_table;
   int page_size, max_pages, num_pages;
+  // FP8 KV cache when k8 is non-null (k, v unused): E4M3 codes laid out like k, v; the value of
+  // element (head h, channel c) is e4m3(code) * k_scale[h * D + c] (v_scale for V)
+  const uint8_t* k8;
+  const uint8_t* v8;
+  const float* k_scale;
+  const float* v_scale;
   // fused merge when tickets is non-null: units * row_groups zeroed counters owned by this
   // launch (left zeroed again); the last CTA of each (unit, row group) writes o and lse
   unsigned int* tickets;

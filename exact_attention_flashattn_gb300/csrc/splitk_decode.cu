@@ -19,6 +19,15 @@
 // output-channel index of the P V product is permuted and undone at the write. When a row
 // group has at most 8 rows (GQA groups of up to 8 heads) the padding half of the MMA rows is
 // fed zeros and its accumulators are not kept, which frees registers for more warps per SM.
+//
+// FP8 KV cache ("Attention from the kernel's side", Why a quantised cache needs a fused kernel:
+// the codes are turned into values inside the tile load, so HBM carries only the codes): the
+// cache holds E4M3 codes with a per-(KV head, channel) scale. Each 16-byte load brings 16
+// codes; `cvt.rn.f16x2.e4m3x2` turns code pairs into f16 pairs exactly (every E4M3 value is an
+// f16 value) and the contractions run as f16 MMAs. The K scale is folded into Q once per CTA
+// (s = sum_c (q_c k_scale_c) code_c), with a per-row power of two that keeps q * k_scale in
+// f16 range and is given back in the row's score scale; the V scale multiplies each output
+// channel of the partial o (o_c = v_scale_c sum_j p_j code_jc).
 #include <math.h>
 
 #include "kernels.h"
@@ -63,12 +72,47 @@ __device__ __forceinline__ void mma_bf16_top(float& d0, float& d1, uint32_t a0, 
       : "r"(a0), "r"(a2), "r"(b0), "r"(b1));
 }
 
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_f16_top(float& d0, float& d1, uint32_t a0, uint32_t a2, uint32_t b0,
+                                            uint32_t b1) {
+  float x2, x3;
+  asm volatile(
+      "{\n\t.reg .b32 z;\n\tmov.b32 z, 0;\n\t"
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, z, %5, z}, {%6, %7}, "
+      "{%0, %1, z, z};\n\t}\n"
+      : "+f"(d0), "+f"(d1), "=f"(x2), "=f"(x3)
+      : "r"(a0), "r"(a2), "r"(b0), "r"(b1));
+}
+
+// Two E4M3 codes (low byte -> low half) to an f16 pair; exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes16) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}\n" : "=r"(r) : "r"(codes16));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t word(const uint4& v, int w) {
   return w == 0 ? v.x : (w == 1 ? v.y : (w == 2 ? v.z : v.w));
 }
 
 // Output channel held by MMA column position p (0..7) of output n-tile nu (0..15).
 __device__ __forceinline__ int dv_of(int nu, int p) { return (nu < 8) ? (8 * p + nu) : (64 + 8 * p + (nu - 8)); }
+// The same for the FP8 cache, whose V loads are 16-channel chunks: column p of n-tile nu is
+// channel 16 p + nu.
+__device__ __forceinline__ int dv8_of(int nu, int p) { return 16 * p + nu; }
 
 struct UnitGeom {
   int tok0;     // first query token of the sequence
@@ -125,8 +169,9 @@ __device__ __forceinline__ size_t ws_ml_index(const SplitKArgs& a, int unit, int
 
 // NH = number of 8-row halves of the 16-row MMA tile that carry real rows (1 or 2);
 // kPaged: keys are gathered page by page through the block table; kWindow: causal sliding
-// window (a separate instance, so the plain causal and paged paths carry no window registers).
-template <int NH, bool kPaged, bool kWindow>
+// window (a separate instance, so the plain causal and paged paths carry no window registers);
+// kFp8: FP8 E4M3 cache with per-channel scales (k8, v8, k_scale, v_scale).
+template <int NH, bool kPaged, bool kWindow, bool kFp8>
 __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(SplitKArgs a) {
   const int split = blockIdx.x;
   const int hkv = blockIdx.y % a.Hkv;
@@ -150,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
   // Rows gr (and gr + 8) of this group: (query i, head hh) and their key limits [lo, lim).
   int lim[2], lo[2];
   uint32_t qa[8][4];
+  float sl2[2] = {a.scale_log2, a.scale_log2};  // FP8: the row's score scale (see below)
 #pragma unroll
   for (int rr = 0; rr < 2; ++rr) {
     const int r = row0 + gr + 8 * rr;
@@ -163,15 +209,60 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
       lo[rr] = 0;
     }
     const uint16_t* qrow = a.q + (static_cast<int64_t>(u.tok0 + i) * a.Hq + hkv * a.g + hh) * D;
+    if constexpr (!kFp8) {
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      uint4 c = make_uint4(0, 0, 0, 0);
-      if (ok) c = *reinterpret_cast<const uint4*>(qrow + 8 * (t + 4 * s));
-      // k-step 2s uses words 0,1 of chunk t+4s; k-step 2s+1 words 2,3 (same permutation as K)
-      qa[2 * s][rr] = c.x;
-      qa[2 * s][rr + 2] = c.y;
-      qa[2 * s + 1][rr] = c.z;
-      qa[2 * s + 1][rr + 2] = c.w;
+      for (int s = 0; s < 4; ++s) {
+        uint4 c = make_uint4(0, 0, 0, 0);
+        if (ok) c = *reinterpret_cast<const uint4*>(qrow + 8 * (t + 4 * s));
+        // k-step 2s uses words 0,1 of chunk t+4s; k-step 2s+1 words 2,3 (same permutation as K)
+        qa[2 * s][rr] = c.x;
+        qa[2 * s][rr + 2] = c.y;
+        qa[2 * s + 1][rr] = c.z;
+        qa[2 * s + 1][rr + 2] = c.w;
+      }
+    } else {
+      // this thread's K loads are the 16-code chunks t and t + 4, so it holds q * k_scale for
+      // channels 16t..16t+15 (k-steps 0..3) and 16(t+4)..16(t+4)+15 (k-steps 4..7)
+      float qs[32];
+      const float* ksc = a.k_scale + hkv * D;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int c0 = 16 * (t + 4 * hf);
+#pragma unroll
+        for (int s8 = 0; s8 < 2; ++s8) {
+          uint4 c = make_uint4(0, 0, 0, 0);
+          if (ok) c = *reinterpret_cast<const uint4*>(qrow + c0 + 8 * s8);
+          const float4 k0 = *reinterpret_cast<const float4*>(ksc + c0 + 8 * s8);
+          const float4 k1 = *reinterpret_cast<const float4*>(ksc + c0 + 8 * s8 + 4);
+          const uint32_t wv[4] = {c.x, c.y, c.z, c.w};
+          const float kv[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const uint32_t bits = (e & 1) ? (wv[e >> 1] & 0xFFFF0000u) : (wv[e >> 1] << 16);
+            qs[16 * hf + 8 * s8 + e] = __uint_as_float(bits) * kv[e];
+          }
+        }
+      }
+      // row scale 2^e so that max |q * k_scale| * 2^-e lies in [8, 16): f16 keeps 11 bits of
+      // every significant product and cannot overflow; the scores get the 2^e back
+      float amax = 0.f;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) amax = fmaxf(amax, fabsf(qs[e]));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      int ex = 0;
+      if (amax > 0.f && amax <= 3.0e38f) {
+        frexpf(amax, &ex);
+        ex = min(max(ex - 4, -120), 120);
+      }
+      const float down = __int_as_float((127 - ex) << 23);  // 2^-ex
+      sl2[rr] = a.scale_log2 * __int_as_float((127 + ex) << 23);
+#pragma unroll
+      for (int kst = 0; kst < 8; ++kst) {
+        const int b = 16 * (kst >> 2) + 4 * (kst & 3);
+        qa[kst][rr] = pack_f16x2(qs[b] * down, qs[b + 1] * down);
+        qa[kst][rr + 2] = pack_f16x2(qs[b + 2] * down, qs[b + 3] * down);
+      }
     }
   }
   // lowest key limit over the CTA's rows: steps ending at or below it need no mask
@@ -197,42 +288,79 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
 
   const uint16_t* kbase = a.k + u.kv0;
   const uint16_t* vbase = a.v + u.kv0;
+  const uint8_t* kbase8 = a.k8 + u.kv0;
+  const uint8_t* vbase8 = a.v8 + u.kv0;
   const int64_t ks = a.kv_key_stride;
 
   for (int kb = kstart + warp * kKeysPerStep; kb < kend; kb += kWarps * kKeysPerStep) {
     // ---- loads: K rows kb + nt*8 + gr (chunks t + 4s); V rows kb + {2t, 2t+1, 2t+8, 2t+9}
     const int64_t so = step_offset<kPaged>(a, seq, kb);
-    uint4 kk[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      const int key = kb + nt * 8 + gr;
-      const uint16_t* kr = kbase + so + static_cast<int64_t>(nt * 8 + gr) * ks;
-#pragma unroll
-      for (int s = 0; s < 4; ++s)
-        kk[nt][s] = (key < kend) ? ld_stream(kr + 8 * (t + 4 * s)) : make_uint4(0, 0, 0, 0);
-    }
-    uint4 va[4], vb[4];
-#pragma unroll
-    for (int x = 0; x < 4; ++x) {
-      const int key = kb + 2 * t + (x & 1) + 8 * (x >> 1);
-      const uint16_t* vr = vbase + so + static_cast<int64_t>(key - kb) * ks;
-      va[x] = (key < kend) ? ld_stream(vr + 8 * gr) : make_uint4(0, 0, 0, 0);
-      vb[x] = (key < kend) ? ld_stream(vr + 64 + 8 * gr) : make_uint4(0, 0, 0, 0);
-    }
-    // ---- S = Q K^T for 16 keys: two n8 tiles, 8 k16 steps over the head dim
     float sacc[2][4];
+    uint4 va[4], vb[4];  // FP8: va only (16 codes of chunk gr per key)
+    if constexpr (!kFp8) {
+      uint4 kk[2][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+      for (int nt = 0; nt < 2; ++nt) {
+        const int key = kb + nt * 8 + gr;
+        const uint16_t* kr = kbase + so + static_cast<int64_t>(nt * 8 + gr) * ks;
 #pragma unroll
-      for (int kst = 0; kst < 8; ++kst) {
-        const uint4& c = kk[nt][kst >> 1];
-        const uint32_t b0 = (kst & 1) ? c.z : c.x;
-        const uint32_t b1 = (kst & 1) ? c.w : c.y;
-        if constexpr (NH == 2)
-          mma_bf16(sacc[nt], qa[kst], b0, b1);
-        else
-          mma_bf16_top(sacc[nt][0], sacc[nt][1], qa[kst][0], qa[kst][2], b0, b1);
+        for (int s = 0; s < 4; ++s)
+          kk[nt][s] = (key < kend) ? ld_stream(kr + 8 * (t + 4 * s)) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const int key = kb + 2 * t + (x & 1) + 8 * (x >> 1);
+        const uint16_t* vr = vbase + so + static_cast<int64_t>(key - kb) * ks;
+        va[x] = (key < kend) ? ld_stream(vr + 8 * gr) : make_uint4(0, 0, 0, 0);
+        vb[x] = (key < kend) ? ld_stream(vr + 64 + 8 * gr) : make_uint4(0, 0, 0, 0);
+      }
+      // ---- S = Q K^T for 16 keys: two n8 tiles, 8 k16 steps over the head dim
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+#pragma unroll
+        for (int kst = 0; kst < 8; ++kst) {
+          const uint4& c = kk[nt][kst >> 1];
+          const uint32_t b0 = (kst & 1) ? c.z : c.x;
+          const uint32_t b1 = (kst & 1) ? c.w : c.y;
+          if constexpr (NH == 2)
+            mma_bf16(sacc[nt], qa[kst], b0, b1);
+          else
+            mma_bf16_top(sacc[nt][0], sacc[nt][1], qa[kst][0], qa[kst][2], b0, b1);
+        }
+      }
+    } else {
+      // K: codes of chunks t and t + 4 of rows kb + nt*8 + gr; V: chunk gr of 4 key rows
+      uint4 kk[2][2];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int key = kb + nt * 8 + gr;
+        const uint8_t* kr = kbase8 + so + static_cast<int64_t>(nt * 8 + gr) * ks;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf)
+          kk[nt][hf] = (key < kend) ? ld_stream(kr + 16 * (t + 4 * hf)) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const int key = kb + 2 * t + (x & 1) + 8 * (x >> 1);
+        const uint8_t* vr = vbase8 + so + static_cast<int64_t>(key - kb) * ks;
+        va[x] = (key < kend) ? ld_stream(vr + 16 * gr) : make_uint4(0, 0, 0, 0);
+      }
+      // k-step kst takes word kst & 3 of chunk kst >> 2: codes (c0, c1) -> k = 2t, 2t+1 and
+      // (c2, c3) -> k = 2t+8, 2t+9, the channel order Q was packed in
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+#pragma unroll
+        for (int kst = 0; kst < 8; ++kst) {
+          const uint32_t w = word(kk[nt][kst >> 2], kst & 3);
+          const uint32_t b0 = e4m3x2_to_f16x2(w & 0xFFFFu);
+          const uint32_t b1 = e4m3x2_to_f16x2(w >> 16);
+          if constexpr (NH == 2)
+            mma_f16(sacc[nt], qa[kst], b0, b1);
+          else
+            mma_f16_top(sacc[nt][0], sacc[nt][1], qa[kst][0], qa[kst][2], b0, b1);
+        }
       }
     }
     // ---- scale (log2 units), mask, row max over the quad
@@ -244,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
 #pragma unroll
       for (int c = 0; c < 2 * NH; ++c) {
         const int rr = c >> 1;
-        float s = sacc[nt][c] * a.scale_log2;
+        float s = sacc[nt][c] * (kFp8 ? sl2[rr] : a.scale_log2);
         if (need_mask) {
           const int key = kb + nt * 8 + 2 * t + (c & 1);
           if (key >= lim[rr] || (kWindow && key < lo[rr])) s = -INFINITY;
@@ -291,28 +419,62 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
           l_part[c >> 1] += p[nt][c];
         }
       // A fragment of P (rows x 16 keys): k positions 2t,2t+1 from tile 0, 2t+8,2t+9 from tile 1
-      pa[0] = pack_bf16x2(p[0][0], p[0][1]);
-      pa[2] = pack_bf16x2(p[1][0], p[1][1]);
-      if constexpr (NH == 2) {
-        pa[1] = pack_bf16x2(p[0][2], p[0][3]);
-        pa[3] = pack_bf16x2(p[1][2], p[1][3]);
+      if constexpr (!kFp8) {
+        pa[0] = pack_bf16x2(p[0][0], p[0][1]);
+        pa[2] = pack_bf16x2(p[1][0], p[1][1]);
+        if constexpr (NH == 2) {
+          pa[1] = pack_bf16x2(p[0][2], p[0][3]);
+          pa[3] = pack_bf16x2(p[1][2], p[1][3]);
+        } else {
+          pa[1] = pa[3] = 0u;
+        }
       } else {
-        pa[1] = pa[3] = 0u;
+        pa[0] = pack_f16x2(p[0][0], p[0][1]);
+        pa[2] = pack_f16x2(p[1][0], p[1][1]);
+        if constexpr (NH == 2) {
+          pa[1] = pack_f16x2(p[0][2], p[0][3]);
+          pa[3] = pack_f16x2(p[1][2], p[1][3]);
+        } else {
+          pa[1] = pa[3] = 0u;
+        }
       }
     }
     // ---- O += P V over 16 output n-tiles
+    if constexpr (!kFp8) {
 #pragma unroll
-    for (int nu = 0; nu < 16; ++nu) {
-      const int e = nu & 7;
-      const int w = e >> 1;
-      const uint32_t sel = (e & 1) ? 0x7632u : 0x5410u;
-      const uint32_t w0 = word((nu < 8) ? va[0] : vb[0], w), w1 = word((nu < 8) ? va[1] : vb[1], w);
-      const uint32_t w2 = word((nu < 8) ? va[2] : vb[2], w), w3 = word((nu < 8) ? va[3] : vb[3], w);
-      if constexpr (NH == 2) {
-        float(&acc)[4] = *reinterpret_cast<float(*)[4]>(&oacc[nu][0]);
-        mma_bf16(acc, pa, __byte_perm(w0, w1, sel), __byte_perm(w2, w3, sel));
-      } else {
-        mma_bf16_top(oacc[nu][0], oacc[nu][1], pa[0], pa[2], __byte_perm(w0, w1, sel), __byte_perm(w2, w3, sel));
+      for (int nu = 0; nu < 16; ++nu) {
+        const int e = nu & 7;
+        const int w = e >> 1;
+        const uint32_t sel = (e & 1) ? 0x7632u : 0x5410u;
+        const uint32_t w0 = word((nu < 8) ? va[0] : vb[0], w), w1 = word((nu < 8) ? va[1] : vb[1], w);
+        const uint32_t w2 = word((nu < 8) ? va[2] : vb[2], w), w3 = word((nu < 8) ? va[3] : vb[3], w);
+        if constexpr (NH == 2) {
+          float(&acc)[4] = *reinterpret_cast<float(*)[4]>(&oacc[nu][0]);
+          mma_bf16(acc, pa, __byte_perm(w0, w1, sel), __byte_perm(w2, w3, sel));
+        } else {
+          mma_bf16_top(oacc[nu][0], oacc[nu][1], pa[0], pa[2], __byte_perm(w0, w1, sel), __byte_perm(w2, w3, sel));
+        }
+      }
+    } else {
+      // n-tile nu, column gr = channel 16 gr + nu: code nu of each key's chunk. One byte
+      // permute pairs keys (2t, 2t+1) for channels nu and nu + 1 at once; likewise (2t+8, 2t+9).
+#pragma unroll
+      for (int nu = 0; nu < 16; nu += 2) {
+        const int w = nu >> 2, k = nu & 3;
+        const uint32_t sel = k | ((4 + k) << 4) | ((k + 1) << 8) | ((5 + k) << 12);
+        const uint32_t lo2 = __byte_perm(word(va[0], w), word(va[1], w), sel);
+        const uint32_t hi2 = __byte_perm(word(va[2], w), word(va[3], w), sel);
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const uint32_t b0 = e4m3x2_to_f16x2(h2 ? (lo2 >> 16) : (lo2 & 0xFFFFu));
+          const uint32_t b1 = e4m3x2_to_f16x2(h2 ? (hi2 >> 16) : (hi2 & 0xFFFFu));
+          if constexpr (NH == 2) {
+            float(&acc)[4] = *reinterpret_cast<float(*)[4]>(&oacc[nu + h2][0]);
+            mma_f16(acc, pa, b0, b1);
+          } else {
+            mma_f16_top(oacc[nu + h2][0], oacc[nu + h2][1], pa[0], pa[2], b0, b1);
+          }
+        }
       }
     }
   }
@@ -331,13 +493,29 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
       sm_l[warp][gr + 8 * rr] = l;
     }
   }
+  if constexpr (!kFp8) {
 #pragma unroll
-  for (int nu = 0; nu < 16; ++nu) {
-    sm_o[warp][gr][dv_of(nu, 2 * t)] = oacc[nu][0];
-    sm_o[warp][gr][dv_of(nu, 2 * t + 1)] = oacc[nu][1];
-    if constexpr (NH == 2) {
-      sm_o[warp][gr + 8][dv_of(nu, 2 * t)] = oacc[nu][2];
-      sm_o[warp][gr + 8][dv_of(nu, 2 * t + 1)] = oacc[nu][3];
+    for (int nu = 0; nu < 16; ++nu) {
+      sm_o[warp][gr][dv_of(nu, 2 * t)] = oacc[nu][0];
+      sm_o[warp][gr][dv_of(nu, 2 * t + 1)] = oacc[nu][1];
+      if constexpr (NH == 2) {
+        sm_o[warp][gr + 8][dv_of(nu, 2 * t)] = oacc[nu][2];
+        sm_o[warp][gr + 8][dv_of(nu, 2 * t + 1)] = oacc[nu][3];
+      }
+    }
+  } else {
+    // this thread's channels are 32t .. 32t + 31: apply the V scale there
+    const float* vsc = a.v_scale + hkv * D;
+#pragma unroll
+    for (int nu = 0; nu < 16; ++nu) {
+      const int c0 = dv8_of(nu, 2 * t), c1 = dv8_of(nu, 2 * t + 1);
+      const float s0 = vsc[c0], s1 = vsc[c1];
+      sm_o[warp][gr][c0] = oacc[nu][0] * s0;
+      sm_o[warp][gr][c1] = oacc[nu][1] * s1;
+      if constexpr (NH == 2) {
+        sm_o[warp][gr + 8][c0] = oacc[nu][2] * s0;
+        sm_o[warp][gr + 8][c1] = oacc[nu][3] * s1;
+      }
     }
   }
   __syncthreads();
@@ -524,18 +702,26 @@ cudaError_t launch_splitk(const SplitKArgs& a, cudaStream_t stream) {
   const bool half = a.cu_q ? (a.small_rows_limit <= 8) : (a.g <= 8);
   const bool paged = a.block_table != nullptr;
   const bool window = a.causal && a.window > 0;
-  if (paged && window) return cudaErrorInvalidValue;  // no entry point pairs the two
-  if (window) {
+  const bool fp8 = a.k8 != nullptr;
+  if ((paged || fp8) && window) return cudaErrorInvalidValue;  // no entry point pairs them
+  if (fp8) {
     if (half)
-      splitk_kernel<1, false, true><<<grid, kThreads, 0, stream>>>(a);
+      paged ? splitk_kernel<1, true, false, true><<<grid, kThreads, 0, stream>>>(a)
+            : splitk_kernel<1, false, false, true><<<grid, kThreads, 0, stream>>>(a);
     else
-      splitk_kernel<2, false, true><<<grid, kThreads, 0, stream>>>(a);
+      paged ? splitk_kernel<2, true, false, true><<<grid, kThreads, 0, stream>>>(a)
+            : splitk_kernel<2, false, false, true><<<grid, kThreads, 0, stream>>>(a);
+  } else if (window) {
+    if (half)
+      splitk_kernel<1, false, true, false><<<grid, kThreads, 0, stream>>>(a);
+    else
+      splitk_kernel<2, false, true, false><<<grid, kThreads, 0, stream>>>(a);
   } else if (half) {
-    paged ? splitk_kernel<1, true, false><<<grid, kThreads, 0, stream>>>(a)
-          : splitk_kernel<1, false, false><<<grid, kThreads, 0, stream>>>(a);
+    paged ? splitk_kernel<1, true, false, false><<<grid, kThreads, 0, stream>>>(a)
+          : splitk_kernel<1, false, false, false><<<grid, kThreads, 0, stream>>>(a);
   } else {
-    paged ? splitk_kernel<2, true, false><<<grid, kThreads, 0, stream>>>(a)
-          : splitk_kernel<2, false, false><<<grid, kThreads, 0, stream>>>(a);
+    paged ? splitk_kernel<2, true, false, false><<<grid, kThreads, 0, stream>>>(a)
+          : splitk_kernel<2, false, false, false><<<grid, kThreads, 0, stream>>>(a);
   }
   return cudaGetLastError();
 }

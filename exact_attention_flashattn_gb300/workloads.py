@@ -36,6 +36,12 @@ SEED_PREFILL = 1002
 SEED_DECODE = 1003
 SEED_DECODE_LONG = 1004
 SEED_VARLEN = 1005
+SEED_FP8_GQA = 1006
+SEED_FP8_LONG = 1007
+# FP8 caches: N(0, 1) draws are quantised with 448 / 4.5 codes per unit, so |z| up to 4.5 is
+# representable and larger draws saturate at the largest code
+FP8_SIGMAS = 4.5
+FP8_MAX = 448.0
 
 VARLEN_NQ_CHOICES = (1, 4, 8, 512)
 
@@ -84,6 +90,21 @@ WORKLOADS = {
                                                       torch.bfloat16, B=8, Hq=32, Hkv=8, Nq=1, Nk=32768, d=128,
                                                       causal=False, num_splits=16, seed=SEED_DECODE,
                                                       extra={"page_size": 16}),
+    # FP8 E4M3 caches with per-(KV head, channel) scales: the GQA decode shape, its paged form,
+    # and the long-context decode
+    "decode_fp8_gqa_b8_h32x8_n32768_d128": Workload("decode_fp8_gqa_b8_h32x8_n32768_d128", "decode_fp8",
+                                                    torch.uint8, B=8, Hq=32, Hkv=8, Nq=1, Nk=32768, d=128,
+                                                    causal=False, num_splits=16, seed=SEED_FP8_GQA,
+                                                    channel_scale=True),
+    "decode_fp8_paged_b8_h32x8_n32768_d128_p16": Workload("decode_fp8_paged_b8_h32x8_n32768_d128_p16",
+                                                          "decode_paged_fp8", torch.uint8, B=8, Hq=32, Hkv=8,
+                                                          Nq=1, Nk=32768, d=128, causal=False, num_splits=16,
+                                                          seed=SEED_FP8_GQA, channel_scale=True,
+                                                          extra={"page_size": 16}),
+    "decode_fp8_long_b1_h64x8_n262144_d128": Workload("decode_fp8_long_b1_h64x8_n262144_d128", "decode_fp8",
+                                                      torch.uint8, B=1, Hq=64, Hkv=8, Nq=1, Nk=262144, d=128,
+                                                      causal=False, num_splits=128, seed=SEED_FP8_LONG,
+                                                      channel_scale=True),
     "varlen_append_64seq_h32x8_d128": Workload("varlen_append_64seq_h32x8_d128", "varlen", torch.bfloat16,
                                                Hq=32, Hkv=8, d=128, causal=True, seed=SEED_VARLEN,
                                                num_seqs=64, nk_range=(1024, 16384)),
@@ -146,6 +167,40 @@ def decode_inputs(B, Hq, Hkv, cap, d, dtype, seed, nk=None, channel_scale=False,
     else:
         nk = torch.as_tensor(nk, dtype=torch.int32)
     return q, kc, vc, nk
+
+
+def fp8_decode_inputs(B, Hq, Hkv, cap, d, seed, nk=None, channel_scale=True, device="cpu"):
+    """FP8 KV cache: q [B, Hq, d] bf16; k, v codes [B, Hkv, cap, d] uint8 (E4M3); k_scale,
+    v_scale [Hkv, d] fp32; nk [B] int32.
+
+    Each cached element is z ~ N(0, 1) (fp32) quantised as code = e4m3(clamp(z * 448 / 4.5)),
+    round to nearest even, by torch's float8_e4m3fn cast; its scale is c * 4.5 / 448 with c the
+    per-channel factor U(0.5, 2) of ``channel_scale`` (else 1), so code * scale ~ z * c.
+    """
+    g = _gen(seed, device)
+    q = _randn((B, Hq, d), g, torch.bfloat16, device)
+    if channel_scale:
+        ck = 0.5 + 1.5 * torch.rand((Hkv, d), generator=g, dtype=torch.float32, device=device)
+        cv = 0.5 + 1.5 * torch.rand((Hkv, d), generator=g, dtype=torch.float32, device=device)
+    else:
+        ck = torch.ones((Hkv, d), dtype=torch.float32, device=device)
+        cv = torch.ones((Hkv, d), dtype=torch.float32, device=device)
+    k_scale = (ck * (FP8_SIGMAS / FP8_MAX)).contiguous()
+    v_scale = (cv * (FP8_SIGMAS / FP8_MAX)).contiguous()
+    codes = []
+    for _ in range(2):
+        c = torch.empty((B, Hkv, cap, d), dtype=torch.uint8, device=device)
+        for b in range(B):
+            for h in range(Hkv):
+                z = torch.randn((cap, d), generator=g, dtype=torch.float32, device=device)
+                z = (z * (FP8_MAX / FP8_SIGMAS)).clamp_(-FP8_MAX, FP8_MAX)
+                c[b, h] = z.to(torch.float8_e4m3fn).view(torch.uint8)
+        codes.append(c)
+    if nk is None:
+        nk = torch.full((B,), cap, dtype=torch.int32)
+    else:
+        nk = torch.as_tensor(nk, dtype=torch.int32)
+    return q, codes[0], codes[1], k_scale, v_scale, nk
 
 
 def paged_from_dense(kcache, vcache, page_size, seed):
@@ -216,6 +271,15 @@ def make(name: str, device="cpu"):
         kp, vp, table = paged_from_dense(kc, vc, w.extra["page_size"], w.seed)
         del kc, vc
         return {"q": q, "k_pages": kp, "v_pages": vp, "block_table": table, "nk": nk, "w": w}
+    if w.kind in ("decode_fp8", "decode_paged_fp8"):
+        q, k8, v8, ks, vs, nk = fp8_decode_inputs(w.B, w.Hq, w.Hkv, w.Nk, w.d, w.seed,
+                                                  channel_scale=w.channel_scale, device=device)
+        if w.kind == "decode_fp8":
+            return {"q": q, "kcache": k8, "vcache": v8, "k_scale": ks, "v_scale": vs, "nk": nk, "w": w}
+        kp, vp, table = paged_from_dense(k8, v8, w.extra["page_size"], w.seed)
+        del k8, v8
+        return {"q": q, "k_pages": kp, "v_pages": vp, "k_scale": ks, "v_scale": vs, "block_table": table,
+                "nk": nk, "w": w}
     nq_list, nk_list = varlen_lengths(w.num_seqs, w.seed, w.nk_range)
     q, k, v, cq, ck = varlen_inputs(nq_list, nk_list, w.Hq, w.Hkv, w.d, w.dtype, w.seed, device)
     return {"q": q, "k": k, "v": v, "cu_q": cq, "cu_k": ck, "nq": nq_list, "nk": nk_list, "w": w}

@@ -139,6 +139,34 @@ int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages, v
                       void* stream);
 
 /*
+ * attn_decode_fp8 / attn_decode_paged_fp8: attn_decode / attn_decode_paged against an FP8 KV
+ * cache, each code turned into its value inside the kernel as it is loaded ("Attention from the
+ * kernel's side", "Why a quantised cache needs a fused kernel": a separate dequantise pass would
+ * move more bytes than the 16-bit cache it replaces; rule 3 of "Rules I use"). The pages' own
+ * format (TBQ4) belongs to another project; this is the generic FP8 form:
+ *
+ *   kcache, vcache /
+ *   k_pages, v_pages : the layouts of attn_decode / attn_decode_paged with one byte per element,
+ *                      an OCP FP8 E4M3 code (bias 7, no infinities, S.1111.111 = NaN, max 448)
+ *   k_scale, v_scale : [Hkv, d] fp32 DEVICE arrays, 16-byte aligned; the cached value of channel
+ *                      c of KV head h is e4m3(code) * k_scale[h * d + c] (v_scale for V)
+ *   q, o, lse, nk, block_table, page_size, num_splits, scale, workspace: as for attn_decode /
+ *                      attn_decode_paged (same workspace size)
+ * The cache is read exactly once; arithmetic is f16 x f16 products of the codes against
+ * q * k_scale (rescaled per query row by a power of two) with fp32 accumulation. Supported:
+ * d = 128, 1 <= g <= 32. Errors as for attn_decode, plus INVALID_ARG for NULL or unaligned
+ * scales.
+ */
+int attn_decode_fp8(const void* q, const void* kcache, const void* vcache, const float* k_scale,
+                    const float* v_scale, void* o, const int32_t* nk, int B, int Hq, int Hkv, int nk_cap, int d,
+                    int num_splits, float scale, float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+int attn_decode_paged_fp8(const void* q, const void* k_pages, const void* v_pages, const float* k_scale,
+                          const float* v_scale, void* o, const int32_t* block_table, const int32_t* nk, int B, int Hq,
+                          int Hkv, int page_size, int num_pages, int max_pages_per_seq, int d, int num_splits,
+                          float scale, float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * attn_decode_static: the same single-query split-K decode as attn_decode, for callers that
  * cannot allocate device memory. The pages have no counterpart to this entry point; it exists
  * for deployment. Some callers cannot call cudaMalloc or hand the library a workspace: a

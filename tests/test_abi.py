@@ -28,7 +28,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ("attn_fwd", "attn_fwd_window", "attn_decode", "attn_decode_paged", "attn_varlen", "attn_varlen_window",
+    for n in ("attn_fwd", "attn_fwd_window", "attn_decode", "attn_decode_paged", "attn_decode_fp8",
+              "attn_decode_paged_fp8", "attn_varlen", "attn_varlen_window",
               "attn_decode_workspace_size", "attn_varlen_workspace_size",
               "bwattn_get_status", "bwattn_clear_status", "bwattn_last_cuda_error", "bwattn_status_string",
               "bwattn_set_wait_timeout_ns", "bwattn_test_wait_timeout", "bwattn_launch_count", "bwattn_version"):
@@ -137,6 +138,41 @@ def test_window_argument_errors(L):
     assert fw(4, B=0, q=None, k=None, v=None, o=None) == bw.OK
     assert vw(4, cq=None) == bw.ERR_INVALID_ARG
     assert vw(4, n=0) == bw.OK
+
+
+def test_fp8_decode_argument_errors(L):
+    def d8(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, ks=FAKE, vs=FAKE, o=FAKE, nk=FAKE, B=2, Hq=8, Hkv=2, cap=64, d=128, S=4,
+                 scale=0.1, lse=None, ws=FAKE, wsb=1 << 30, stream=None)
+        a.update(kw)
+        return L.attn_decode_fp8(a["q"], a["k"], a["v"], a["ks"], a["vs"], a["o"], a["nk"], a["B"], a["Hq"], a["Hkv"],
+                                 a["cap"], a["d"], a["S"], a["scale"], a["lse"], a["ws"], a["wsb"], a["stream"])
+
+    def p8(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, ks=FAKE, vs=FAKE, o=FAKE, bt=FAKE, nk=FAKE, B=2, Hq=8, Hkv=2, ps=16, np_=8,
+                 mp=4, d=128, S=4, scale=0.1, lse=None, ws=FAKE, wsb=1 << 30, stream=None)
+        a.update(kw)
+        return L.attn_decode_paged_fp8(a["q"], a["k"], a["v"], a["ks"], a["vs"], a["o"], a["bt"], a["nk"], a["B"],
+                                       a["Hq"], a["Hkv"], a["ps"], a["np_"], a["mp"], a["d"], a["S"], a["scale"],
+                                       a["lse"], a["ws"], a["wsb"], a["stream"])
+    for f in (d8, p8):
+        assert f(ks=None) == bw.ERR_INVALID_ARG
+        assert f(vs=None) == bw.ERR_INVALID_ARG
+        assert f(ks=FAKE + 4) == bw.ERR_INVALID_ARG  # scales are read as 16-byte vectors
+        assert f(k=FAKE + 8) == bw.ERR_INVALID_ARG
+        assert f(ws=None) == bw.ERR_INVALID_ARG
+        assert f(d=64) == bw.ERR_UNSUPPORTED
+        assert f(Hq=8, Hkv=3) == bw.ERR_INVALID_ARG
+        assert f(B=0, q=None) == bw.OK
+    assert p8(ps=24) == bw.ERR_INVALID_ARG
+
+
+def test_python_binding_fp8_checks():
+    import torch
+    q = torch.zeros(1, 2, 128)
+    with pytest.raises(ValueError):
+        bw.attn_decode_fp8(q, torch.zeros(1, 1, 4, 128, dtype=torch.uint8), torch.zeros(1, 1, 4, 128, dtype=torch.uint8),
+                           torch.ones(1, 128), torch.ones(1, 128), torch.zeros(1, dtype=torch.int32), 1)
 
 
 def test_python_binding_rejects_window_without_causal():

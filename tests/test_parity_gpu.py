@@ -39,7 +39,7 @@ def f64(t):
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def check_bf16(o_gpu, o_ref, lse_gpu=None, lse_ref=None, what=""):
+def check_bf16(o_gpu, o_ref, lse_gpu=None, lse_ref=None, what="", lse_tol=None):
     err = np.abs(f64(o_gpu) - o_ref)
     assert np.all(np.isfinite(err)), what
     assert err.max() <= TOL_BF16_MAX, (what, err.max())
@@ -50,7 +50,8 @@ def check_bf16(o_gpu, o_ref, lse_gpu=None, lse_ref=None, what=""):
         assert np.all(same_inf), what
         fin = np.isfinite(lr)
         if fin.any():
-            assert np.abs(lg[fin] - lr[fin]).max() <= TOL_LSE, (what, np.abs(lg[fin] - lr[fin]).max())
+            tol = TOL_LSE if lse_tol is None else np.broadcast_to(lse_tol, lr.shape)[fin]
+            assert np.all(np.abs(lg[fin] - lr[fin]) <= tol), (what, np.abs(lg[fin] - lr[fin]).max())
 
 
 # ------------------------------------------------------------------ fp32 prefill
@@ -246,6 +247,130 @@ def test_decode_paged_workload_full_size():
     o_ref, lse_ref = oracle.decode_paged(f64(x["q"][b:b + 1]), f64(kp), f64(vp), local.numpy(), [w.Nk],
                                          method="splitk", workers=w.num_splits)
     check_bf16(o[b:b + 1], o_ref, lse[b:b + 1], lse_ref, what="paged full size")
+
+
+# ------------------------------------------------------------------ FP8 (E4M3) KV cache
+# Oracle: the codes decoded from the format's definition, times the per-channel scales, then the
+# fp64 decode. O: the bf16 tolerances. LSE: the kernel multiplies the codes (exact in f16) by
+# q * k_scale rounded to f16, a relative error of at most 2^-11 per product term, so a score
+# s_j = scale * sum_c q_c ks_c code_jc moves by at most 2^-11 * scale * sum_c |q_c ks_c code_jc|
+# and the LSE by at most the largest such move over the visible keys; the LSE bar is 2e-3 plus
+# that bound, computed per row from the inputs.
+
+
+def fp8_ref(q, k8, v8, ks, vs, nk, S):
+    o, lse = oracle.decode_fp8(f64(q), k8.cpu().numpy(), v8.cpu().numpy(), f64(ks), f64(vs), np.asarray(nk),
+                               method="splitk", workers=S)
+    qd, kd, ksd = f64(q), oracle.e4m3_decode(k8.cpu().numpy()), f64(ks)
+    B, Hq, d = qd.shape
+    Hkv = kd.shape[1]
+    g = Hq // Hkv
+    tol = np.full((B, Hq), TOL_LSE)
+    for b in range(B):
+        n = int(np.asarray(nk)[b])
+        if n == 0:
+            continue
+        for hk in range(Hkv):
+            qa = np.abs(qd[b, hk * g:(hk + 1) * g] * ksd[hk][None])      # [g, d]
+            bound = (np.abs(kd[b, hk, :n]) @ qa.T).max(axis=0)            # [g]
+            tol[b, hk * g:(hk + 1) * g] += 2.0 ** -11 * bound / math.sqrt(d)
+    return o, lse, tol
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,cap,nk,S", [
+    (3, 8, 2, 300, [300, 17, 0], 4),     # g = 4 (8-row tile), ragged lengths, an empty sequence
+    (2, 8, 8, 1000, [1000, 999], 7),     # g = 1
+    (1, 16, 2, 513, [513], 64),          # g = 8, empty splits, separate merge (64 > 32 splits)
+    (2, 16, 1, 400, [400, 250], 3),      # g = 16 (16-row tile)
+    (1, 32, 1, 200, [200], 1),           # g = 32: two row groups, one split
+])
+def test_decode_fp8(B, Hq, Hkv, cap, nk, S):
+    q, k8, v8, ks, vs, nkt = wl.fp8_decode_inputs(B, Hq, Hkv, cap, 128, seed=91 + cap, nk=nk)
+    o_ref, lse_ref, tol = fp8_ref(q, k8, v8, ks, vs, nkt.numpy(), S)
+    o, lse = bw.attn_decode_fp8(q.cuda(), k8.cuda(), v8.cuda(), ks.cuda(), vs.cuda(), nkt.cuda(), num_splits=S)
+    torch.cuda.synchronize()
+    check_bf16(o, o_ref, lse, lse_ref, what=("fp8", B, Hq, Hkv, cap, nk, S), lse_tol=tol)
+
+
+@pytest.mark.parametrize("mult", [1e-5, 1e4])
+def test_decode_fp8_extreme_key_scales(mult):
+    # q * k_scale far from 1 in either direction: the per-row power of two keeps it in f16 range
+    q, k8, v8, ks, vs, nkt = wl.fp8_decode_inputs(2, 16, 2, 256, 128, seed=97, nk=[256, 100])
+    ks = ks * mult
+    if mult > 1:
+        q = q * 1e-3  # keeps the scores moderate: a softmax of huge scores is one-hot in both
+    o_ref, lse_ref, tol = fp8_ref(q, k8, v8, ks, vs, nkt.numpy(), 4)
+    o, lse = bw.attn_decode_fp8(q.cuda(), k8.cuda(), v8.cuda(), ks.cuda(), vs.cuda(), nkt.cuda(), num_splits=4)
+    torch.cuda.synchronize()
+    check_bf16(o, o_ref, lse, lse_ref, what=("fp8 scale", mult), lse_tol=tol)
+
+
+def test_decode_fp8_every_code_value():
+    # every finite code appears in K and V: codes 0..255 minus the two NaN codes, cycled over keys
+    B, Hq, Hkv, cap = 1, 8, 1, 512
+    codes = torch.tensor([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=torch.uint8)
+    k8 = codes[torch.arange(cap * 128) % codes.numel()].view(1, 1, cap, 128).contiguous()
+    v8 = codes[(torch.arange(cap * 128) * 7 + 3) % codes.numel()].view(1, 1, cap, 128).contiguous()
+    g = torch.Generator().manual_seed(99)
+    q = torch.randn((B, Hq, 128), generator=g).to(torch.bfloat16)
+    ks = torch.full((Hkv, 128), 1.0 / 256)
+    vs = torch.full((Hkv, 128), 1.0 / 64)
+    nkt = torch.tensor([cap], dtype=torch.int32)
+    o_ref, lse_ref, tol = fp8_ref(q, k8, v8, ks, vs, nkt.numpy(), 3)
+    o, lse = bw.attn_decode_fp8(q.cuda(), k8.cuda(), v8.cuda(), ks.cuda(), vs.cuda(), nkt.cuda(), num_splits=3)
+    torch.cuda.synchronize()
+    check_bf16(o, o_ref, lse, lse_ref, what="fp8 codes", lse_tol=tol)
+
+
+def test_decode_paged_fp8_matches_contiguous_bit_for_bit():
+    q, k8, v8, ks, vs, nkt = wl.fp8_decode_inputs(4, 32, 8, 1024, 128, seed=93, nk=[1024, 1000, 517, 16])
+    q, k8, v8, ks, vs, nkt = q.cuda(), k8.cuda(), v8.cuda(), ks.cuda(), vs.cuda(), nkt.cuda()
+    kp, vp, table = wl.paged_from_dense(k8, v8, 16, seed=93)
+    o1, l1 = bw.attn_decode_fp8(q, k8, v8, ks, vs, nkt, num_splits=8)
+    o2, l2 = bw.attn_decode_paged_fp8(q, kp, vp, ks, vs, table, nkt, num_splits=8)
+    # codes past a sequence's length are never read: NaN codes there leave every bit unchanged
+    k82, v82 = k8.clone(), v8.clone()
+    k82[1, :, 1000:] = 0x7F
+    v82[2, :, 517:] = 0xFF
+    o3, l3 = bw.attn_decode_fp8(q, k82, v82, ks, vs, nkt, num_splits=8)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert torch.equal(o1, o3) and torch.equal(l1, l3)
+    o_ref, lse_ref, tol = fp8_ref(q, k8, v8, ks, vs, nkt.cpu().numpy(), 8)
+    check_bf16(o1, o_ref, l1, lse_ref, what="fp8 paged", lse_tol=tol)
+
+
+@pytest.mark.parametrize("name", ["decode_fp8_gqa_b8_h32x8_n32768_d128", "decode_fp8_long_b1_h64x8_n262144_d128"])
+def test_decode_fp8_workloads_full_size(name):
+    x = wl.make(name, device="cuda")
+    w = x["w"]
+    o, lse = bw.attn_decode_fp8(x["q"], x["kcache"], x["vcache"], x["k_scale"], x["v_scale"], x["nk"].cuda(),
+                                num_splits=w.num_splits)
+    torch.cuda.synchronize()
+    # the oracle takes the query heads of the first and last KV head of the last sequence
+    b = w.B - 1
+    g = w.Hq // w.Hkv
+    for hk in (0, w.Hkv - 1):
+        sl = slice(hk * g, (hk + 1) * g)
+        o_ref, lse_ref, tol = fp8_ref(x["q"][b:b + 1, sl], x["kcache"][b:b + 1, hk:hk + 1],
+                                      x["vcache"][b:b + 1, hk:hk + 1], x["k_scale"][hk:hk + 1],
+                                      x["v_scale"][hk:hk + 1], [w.Nk], w.num_splits)
+        check_bf16(o[b:b + 1, sl], o_ref, lse[b:b + 1, sl], lse_ref, what=(name, hk), lse_tol=tol)
+
+
+def test_decode_paged_fp8_workload_full_size():
+    x = wl.make("decode_fp8_paged_b8_h32x8_n32768_d128_p16", device="cuda")
+    w = x["w"]
+    o, lse = bw.attn_decode_paged_fp8(x["q"], x["k_pages"], x["v_pages"], x["k_scale"], x["v_scale"],
+                                      x["block_table"], x["nk"].cuda(), num_splits=w.num_splits)
+    torch.cuda.synchronize()
+    b = w.B - 1
+    used = x["block_table"][b].long()
+    # gather the sequence's pages back into a contiguous [1, Hkv, Nk, d] cache (data movement only)
+    kc = x["k_pages"].index_select(0, used).reshape(1, w.Nk, w.Hkv, w.d).permute(0, 2, 1, 3).contiguous()
+    vc = x["v_pages"].index_select(0, used).reshape(1, w.Nk, w.Hkv, w.d).permute(0, 2, 1, 3).contiguous()
+    o_ref, lse_ref, tol = fp8_ref(x["q"][b:b + 1], kc, vc, x["k_scale"], x["v_scale"], [w.Nk], w.num_splits)
+    check_bf16(o[b:b + 1], o_ref, lse[b:b + 1], lse_ref, what="fp8 paged full size", lse_tol=tol)
 
 
 # ------------------------------------------------------------------ varlen
