@@ -42,6 +42,13 @@ constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kRowsPerGroup = 16;
 constexpr int kKeysPerStep = 16;
+// FP8 cache: each thread's 16-byte chunks of a step (4 of K, 4 of V) go through a ring of
+// kFp8Stages shared-memory slots with cp.async, so that the bytes in flight are bounded by
+// shared memory rather than registers
+constexpr int kFp8Stages = 4;
+constexpr int kFp8Chunks = 8;
+constexpr uint32_t kFp8StageBytes = kWarps * kFp8Chunks * 32 * 16;
+constexpr uint32_t kFp8SmemBytes = kFp8Stages * kFp8StageBytes;
 constexpr int kMergeThreads = 256;
 
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
@@ -50,6 +57,17 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(p));
   return r;
+}
+
+// 16-byte asynchronous copy global -> shared (L2 only); `bytes` = 0 writes zeros and reads
+// nothing from src.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -91,11 +109,12 @@ __device__ __forceinline__ void mma_f16_top(float& d0, float& d1, uint32_t a0, u
       : "r"(a0), "r"(a2), "r"(b0), "r"(b1));
 }
 
-// Two E4M3 codes (low byte -> low half) to an f16 pair; exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes16) {
-  uint32_t r;
-  asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}\n" : "=r"(r) : "r"(codes16));
-  return r;
+// Four E4M3 codes (bytes 0..3) to two f16 pairs: bytes 0,1 -> lo, bytes 2,3 -> hi; exact.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t codes, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}\n"
+      : "=r"(lo), "=r"(hi)
+      : "r"(codes));
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
@@ -172,7 +191,8 @@ __device__ __forceinline__ size_t ws_ml_index(const SplitKArgs& a, int unit, int
 // window (a separate instance, so the plain causal and paged paths carry no window registers);
 // kFp8: FP8 E4M3 cache with per-channel scales (k8, v8, k_scale, v_scale).
 template <int NH, bool kPaged, bool kWindow, bool kFp8>
-__global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(SplitKArgs a) {
+__global__ void __launch_bounds__(kThreads, (NH == 1 && !kFp8) ? 4 : 3) splitk_kernel(SplitKArgs a) {
+  extern __shared__ __align__(16) uint8_t dsm[];  // FP8: the load ring, then the combine buffer
   const int split = blockIdx.x;
   const int hkv = blockIdx.y % a.Hkv;
   const int grp = blockIdx.y / a.Hkv;
@@ -292,78 +312,9 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
   const uint8_t* vbase8 = a.v8 + u.kv0;
   const int64_t ks = a.kv_key_stride;
 
-  for (int kb = kstart + warp * kKeysPerStep; kb < kend; kb += kWarps * kKeysPerStep) {
-    // ---- loads: K rows kb + nt*8 + gr (chunks t + 4s); V rows kb + {2t, 2t+1, 2t+8, 2t+9}
-    const int64_t so = step_offset<kPaged>(a, seq, kb);
-    float sacc[2][4];
-    uint4 va[4], vb[4];  // FP8: va only (16 codes of chunk gr per key)
-    if constexpr (!kFp8) {
-      uint4 kk[2][4];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const int key = kb + nt * 8 + gr;
-        const uint16_t* kr = kbase + so + static_cast<int64_t>(nt * 8 + gr) * ks;
-#pragma unroll
-        for (int s = 0; s < 4; ++s)
-          kk[nt][s] = (key < kend) ? ld_stream(kr + 8 * (t + 4 * s)) : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const int key = kb + 2 * t + (x & 1) + 8 * (x >> 1);
-        const uint16_t* vr = vbase + so + static_cast<int64_t>(key - kb) * ks;
-        va[x] = (key < kend) ? ld_stream(vr + 8 * gr) : make_uint4(0, 0, 0, 0);
-        vb[x] = (key < kend) ? ld_stream(vr + 64 + 8 * gr) : make_uint4(0, 0, 0, 0);
-      }
-      // ---- S = Q K^T for 16 keys: two n8 tiles, 8 k16 steps over the head dim
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
-#pragma unroll
-        for (int kst = 0; kst < 8; ++kst) {
-          const uint4& c = kk[nt][kst >> 1];
-          const uint32_t b0 = (kst & 1) ? c.z : c.x;
-          const uint32_t b1 = (kst & 1) ? c.w : c.y;
-          if constexpr (NH == 2)
-            mma_bf16(sacc[nt], qa[kst], b0, b1);
-          else
-            mma_bf16_top(sacc[nt][0], sacc[nt][1], qa[kst][0], qa[kst][2], b0, b1);
-        }
-      }
-    } else {
-      // K: codes of chunks t and t + 4 of rows kb + nt*8 + gr; V: chunk gr of 4 key rows
-      uint4 kk[2][2];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const int key = kb + nt * 8 + gr;
-        const uint8_t* kr = kbase8 + so + static_cast<int64_t>(nt * 8 + gr) * ks;
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf)
-          kk[nt][hf] = (key < kend) ? ld_stream(kr + 16 * (t + 4 * hf)) : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const int key = kb + 2 * t + (x & 1) + 8 * (x >> 1);
-        const uint8_t* vr = vbase8 + so + static_cast<int64_t>(key - kb) * ks;
-        va[x] = (key < kend) ? ld_stream(vr + 16 * gr) : make_uint4(0, 0, 0, 0);
-      }
-      // k-step kst takes word kst & 3 of chunk kst >> 2: codes (c0, c1) -> k = 2t, 2t+1 and
-      // (c2, c3) -> k = 2t+8, 2t+9, the channel order Q was packed in
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
-#pragma unroll
-        for (int kst = 0; kst < 8; ++kst) {
-          const uint32_t w = word(kk[nt][kst >> 2], kst & 3);
-          const uint32_t b0 = e4m3x2_to_f16x2(w & 0xFFFFu);
-          const uint32_t b1 = e4m3x2_to_f16x2(w >> 16);
-          if constexpr (NH == 2)
-            mma_f16(sacc[nt], qa[kst], b0, b1);
-          else
-            mma_f16_top(sacc[nt][0], sacc[nt][1], qa[kst][0], qa[kst][2], b0, b1);
-        }
-      }
-    }
-    // ---- scale (log2 units), mask, row max over the quad
+  // ---- scale (log2 units), mask, row max over the quad, online-softmax update of one 16-key
+  // step starting at key kb; returns the A fragment of P (rows x 16 keys)
+  auto softmax_step = [&](int kb, float (&sacc)[2][4], uint32_t (&pa)[4]) {
     bool need_mask = kb + kKeysPerStep > min_lim;
     if constexpr (kWindow) need_mask = need_mask || kb < max_lo;
     float mx[2] = {-INFINITY, -INFINITY};
@@ -385,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
       mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
       mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
     }
-    // ---- online-softmax update; O is rescaled only when some row's max grew
+    // O is rescaled only when some row's max grew
     float mnew[2], muse[2];
     bool grow = false;
 #pragma unroll
@@ -408,39 +359,64 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
     }
 #pragma unroll
     for (int rr = 0; rr < NH; ++rr) m_run[rr] = mnew[rr];
-    uint32_t pa[4];
-    {
-      float p[2][4];
+    float p[2][4];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int c = 0; c < 2 * NH; ++c) {
-          p[nt][c] = ex2(sacc[nt][c] - muse[c >> 1]);
-          l_part[c >> 1] += p[nt][c];
-        }
-      // A fragment of P (rows x 16 keys): k positions 2t,2t+1 from tile 0, 2t+8,2t+9 from tile 1
-      if constexpr (!kFp8) {
-        pa[0] = pack_bf16x2(p[0][0], p[0][1]);
-        pa[2] = pack_bf16x2(p[1][0], p[1][1]);
-        if constexpr (NH == 2) {
-          pa[1] = pack_bf16x2(p[0][2], p[0][3]);
-          pa[3] = pack_bf16x2(p[1][2], p[1][3]);
-        } else {
-          pa[1] = pa[3] = 0u;
-        }
-      } else {
-        pa[0] = pack_f16x2(p[0][0], p[0][1]);
-        pa[2] = pack_f16x2(p[1][0], p[1][1]);
-        if constexpr (NH == 2) {
-          pa[1] = pack_f16x2(p[0][2], p[0][3]);
-          pa[3] = pack_f16x2(p[1][2], p[1][3]);
-        } else {
-          pa[1] = pa[3] = 0u;
+      for (int c = 0; c < 2 * NH; ++c) {
+        p[nt][c] = ex2(sacc[nt][c] - muse[c >> 1]);
+        l_part[c >> 1] += p[nt][c];
+      }
+    // k positions 2t,2t+1 from tile 0, 2t+8,2t+9 from tile 1 (f16 for the FP8 cache)
+    pa[0] = kFp8 ? pack_f16x2(p[0][0], p[0][1]) : pack_bf16x2(p[0][0], p[0][1]);
+    pa[2] = kFp8 ? pack_f16x2(p[1][0], p[1][1]) : pack_bf16x2(p[1][0], p[1][1]);
+    if constexpr (NH == 2) {
+      pa[1] = kFp8 ? pack_f16x2(p[0][2], p[0][3]) : pack_bf16x2(p[0][2], p[0][3]);
+      pa[3] = kFp8 ? pack_f16x2(p[1][2], p[1][3]) : pack_bf16x2(p[1][2], p[1][3]);
+    } else {
+      pa[1] = pa[3] = 0u;
+    }
+  };
+
+  if constexpr (!kFp8) {
+    for (int kb = kstart + warp * kKeysPerStep; kb < kend; kb += kWarps * kKeysPerStep) {
+      // ---- loads: K rows kb + nt*8 + gr (chunks t + 4s); V rows kb + {2t, 2t+1, 2t+8, 2t+9}
+      const int64_t so = step_offset<kPaged>(a, seq, kb);
+      uint4 kk[2][4], va[4], vb[4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int key = kb + nt * 8 + gr;
+        const uint16_t* kr = kbase + so + static_cast<int64_t>(nt * 8 + gr) * ks;
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          kk[nt][s] = (key < kend) ? ld_stream(kr + 8 * (t + 4 * s)) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const int key = kb + 2 * t + (x & 1) + 8 * (x >> 1);
+        const uint16_t* vr = vbase + so + static_cast<int64_t>(key - kb) * ks;
+        va[x] = (key < kend) ? ld_stream(vr + 8 * gr) : make_uint4(0, 0, 0, 0);
+        vb[x] = (key < kend) ? ld_stream(vr + 64 + 8 * gr) : make_uint4(0, 0, 0, 0);
+      }
+      // ---- S = Q K^T for 16 keys: two n8 tiles, 8 k16 steps over the head dim
+      float sacc[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+#pragma unroll
+        for (int kst = 0; kst < 8; ++kst) {
+          const uint4& c = kk[nt][kst >> 1];
+          const uint32_t b0 = (kst & 1) ? c.z : c.x;
+          const uint32_t b1 = (kst & 1) ? c.w : c.y;
+          if constexpr (NH == 2)
+            mma_bf16(sacc[nt], qa[kst], b0, b1);
+          else
+            mma_bf16_top(sacc[nt][0], sacc[nt][1], qa[kst][0], qa[kst][2], b0, b1);
         }
       }
-    }
-    // ---- O += P V over 16 output n-tiles
-    if constexpr (!kFp8) {
+      uint32_t pa[4];
+      softmax_step(kb, sacc, pa);
+      // ---- O += P V over 16 output n-tiles
 #pragma unroll
       for (int nu = 0; nu < 16; ++nu) {
         const int e = nu & 7;
@@ -455,19 +431,93 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
           mma_bf16_top(oacc[nu][0], oacc[nu][1], pa[0], pa[2], __byte_perm(w0, w1, sel), __byte_perm(w2, w3, sel));
         }
       }
-    } else {
+    }
+  } else {
+    // FP8: the step's chunks are copied asynchronously into this thread's slots of a
+    // kFp8Stages-deep ring (slot = stage, chunk, lane), kFp8Stages - 1 steps ahead of the one
+    // being computed. Each thread reads back only what it copied, so no barrier is needed.
+    const uint32_t pipe = smem_u32(dsm) + static_cast<uint32_t>((warp * kFp8Chunks * 32 + lane) * 16);
+    auto slot = [&](int st, int c) { return pipe + st * kFp8StageBytes + c * 32 * 16; };
+    auto issue = [&](int kb, int st) {
+      if (kb < kend) {
+        const int64_t so = step_offset<kPaged>(a, seq, kb);
+        // K: codes of chunks t and t + 4 of rows kb + nt*8 + gr; V: chunk gr of 4 key rows
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const int key = kb + nt * 8 + gr;
+          const uint8_t* kr = kbase8 + so + static_cast<int64_t>(nt * 8 + gr) * ks;
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf)
+            cp_async16(slot(st, 2 * nt + hf), (key < kend) ? kr + 16 * (t + 4 * hf) : kbase8,
+                       (key < kend) ? 16u : 0u);
+        }
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const int key = kb + 2 * t + (x & 1) + 8 * (x >> 1);
+          const uint8_t* vr = vbase8 + so + static_cast<int64_t>(key - kb) * ks;
+          cp_async16(slot(st, 4 + x), (key < kend) ? vr + 16 * gr : vbase8, (key < kend) ? 16u : 0u);
+        }
+      }
+      cp_async_commit();  // one group per step, empty past the slice
+    };
+    auto ld_slot = [&](int st, int c) {
+      uint4 r;
+      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                   : "r"(slot(st, c)));
+      return r;
+    };
+    constexpr int kStride = kWarps * kKeysPerStep;
+    int kb_next = kstart + warp * kKeysPerStep;
+#pragma unroll
+    for (int st = 0; st < kFp8Stages - 1; ++st) {
+      issue(kb_next, st);
+      kb_next += kStride;
+    }
+    int st = 0;
+    for (int kb = kstart + warp * kKeysPerStep; kb < kend; kb += kStride) {
+      issue(kb_next, st == 0 ? kFp8Stages - 1 : st - 1);  // the slot read one step ago
+      kb_next += kStride;
+      cp_async_wait<kFp8Stages - 1>();  // this step's group has landed
+      uint4 kk[2][2], va[4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        kk[nt][0] = ld_slot(st, 2 * nt);
+        kk[nt][1] = ld_slot(st, 2 * nt + 1);
+      }
+#pragma unroll
+      for (int x = 0; x < 4; ++x) va[x] = ld_slot(st, 4 + x);
+      st = (st + 1 == kFp8Stages) ? 0 : st + 1;
+      // k-step kst takes word kst & 3 of chunk kst >> 2: codes (c0, c1) -> k = 2t, 2t+1 and
+      // (c2, c3) -> k = 2t+8, 2t+9, the channel order Q was packed in
+      float sacc[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+#pragma unroll
+        for (int kst = 0; kst < 8; ++kst) {
+          uint32_t b0, b1;
+          e4m3x4_to_f16x2x2(word(kk[nt][kst >> 2], kst & 3), b0, b1);
+          if constexpr (NH == 2)
+            mma_f16(sacc[nt], qa[kst], b0, b1);
+          else
+            mma_f16_top(sacc[nt][0], sacc[nt][1], qa[kst][0], qa[kst][2], b0, b1);
+        }
+      }
+      uint32_t pa[4];
+      softmax_step(kb, sacc, pa);
       // n-tile nu, column gr = channel 16 gr + nu: code nu of each key's chunk. One byte
       // permute pairs keys (2t, 2t+1) for channels nu and nu + 1 at once; likewise (2t+8, 2t+9).
 #pragma unroll
       for (int nu = 0; nu < 16; nu += 2) {
         const int w = nu >> 2, k = nu & 3;
         const uint32_t sel = k | ((4 + k) << 4) | ((k + 1) << 8) | ((5 + k) << 12);
-        const uint32_t lo2 = __byte_perm(word(va[0], w), word(va[1], w), sel);
-        const uint32_t hi2 = __byte_perm(word(va[2], w), word(va[3], w), sel);
+        uint32_t b0v[2], b1v[2];
+        e4m3x4_to_f16x2x2(__byte_perm(word(va[0], w), word(va[1], w), sel), b0v[0], b0v[1]);
+        e4m3x4_to_f16x2x2(__byte_perm(word(va[2], w), word(va[3], w), sel), b1v[0], b1v[1]);
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
-          const uint32_t b0 = e4m3x2_to_f16x2(h2 ? (lo2 >> 16) : (lo2 & 0xFFFFu));
-          const uint32_t b1 = e4m3x2_to_f16x2(h2 ? (hi2 >> 16) : (hi2 & 0xFFFFu));
+          const uint32_t b0 = b0v[h2], b1 = b1v[h2];
           if constexpr (NH == 2) {
             float(&acc)[4] = *reinterpret_cast<float(*)[4]>(&oacc[nu + h2][0]);
             mma_f16(acc, pa, b0, b1);
@@ -477,12 +527,21 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
         }
       }
     }
+    cp_async_wait<0>();  // nothing in flight once the ring is reused for the combine below
   }
 
   // ---- combine the warps' states in shared memory, write this split's partials
   __shared__ float sm_m[kWarps][kRowsPerGroup];
   __shared__ float sm_l[kWarps][kRowsPerGroup];
-  __shared__ float sm_o[kWarps][kRowsPerGroup][D + 4];
+  float (*sm_o)[kRowsPerGroup][D + 4];
+  if constexpr (kFp8) {
+    // the FP8 ring is free now: every warp must be past its last read before it is reused
+    __syncthreads();
+    sm_o = reinterpret_cast<float (*)[kRowsPerGroup][D + 4]>(dsm);
+  } else {
+    __shared__ float sm_o_static[kWarps][kRowsPerGroup][D + 4];
+    sm_o = sm_o_static;
+  }
 #pragma unroll
   for (int rr = 0; rr < NH; ++rr) {
     float l = l_part[rr];
@@ -705,12 +764,13 @@ cudaError_t launch_splitk(const SplitKArgs& a, cudaStream_t stream) {
   const bool fp8 = a.k8 != nullptr;
   if ((paged || fp8) && window) return cudaErrorInvalidValue;  // no entry point pairs them
   if (fp8) {
-    if (half)
-      paged ? splitk_kernel<1, true, false, true><<<grid, kThreads, 0, stream>>>(a)
-            : splitk_kernel<1, false, false, true><<<grid, kThreads, 0, stream>>>(a);
-    else
-      paged ? splitk_kernel<2, true, false, true><<<grid, kThreads, 0, stream>>>(a)
-            : splitk_kernel<2, false, false, true><<<grid, kThreads, 0, stream>>>(a);
+    static_assert(kFp8SmemBytes >= sizeof(float) * kWarps * kRowsPerGroup * (D + 4), "combine buffer");
+    auto k = half ? (paged ? splitk_kernel<1, true, false, true> : splitk_kernel<1, false, false, true>)
+                  : (paged ? splitk_kernel<2, true, false, true> : splitk_kernel<2, false, false, true>);
+    const cudaError_t e =
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kFp8SmemBytes));
+    if (e != cudaSuccess) return e;
+    k<<<grid, kThreads, kFp8SmemBytes, stream>>>(a);
   } else if (window) {
     if (half)
       splitk_kernel<1, false, true, false><<<grid, kThreads, 0, stream>>>(a);
