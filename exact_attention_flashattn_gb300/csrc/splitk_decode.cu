@@ -17,8 +17,10 @@
 // fragment layout without shared memory, the head-dim index is permuted identically on Q
 // and K (a permutation of the contraction index leaves the dot product unchanged), and the
 // output-channel index of the P V product is permuted and undone at the write. When a row
-// group has at most 8 rows (GQA groups of up to 8 heads) the padding half of the MMA rows is
-// fed zeros and its accumulators are not kept, which frees registers for more warps per SM.
+// group has at most 8 rows (GQA groups of up to 8 heads) the products are taken transposed:
+// S^T = K Q^T with the 16 keys of a step as the MMA rows and the group's heads as the 8 columns,
+// then O^T += V^T P^T with 16 head-dim channels as the rows; P^T reaches the operand layout by an
+// in-register 8x8 transpose (movmatrix). Half the MMAs of the 16-row form, none of them padding.
 //
 // FP8 KV cache ("Attention from the kernel's side", Why a quantised cache needs a fused kernel:
 // the codes are turned into values inside the tile load, so HBM carries only the codes): the
@@ -78,17 +80,6 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Rows 8..15 are padding: A rows 8..15 are zero and their accumulators are discarded.
-__device__ __forceinline__ void mma_bf16_top(float& d0, float& d1, uint32_t a0, uint32_t a2, uint32_t b0,
-                                             uint32_t b1) {
-  float x2, x3;
-  asm volatile(
-      "{\n\t.reg .b32 z;\n\tmov.b32 z, 0;\n\t"
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, z, %5, z}, {%6, %7}, "
-      "{%0, %1, z, z};\n\t}\n"
-      : "+f"(d0), "+f"(d1), "=f"(x2), "=f"(x3)
-      : "r"(a0), "r"(a2), "r"(b0), "r"(b1));
-}
 
 __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -98,16 +89,6 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], u
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ void mma_f16_top(float& d0, float& d1, uint32_t a0, uint32_t a2, uint32_t b0,
-                                            uint32_t b1) {
-  float x2, x3;
-  asm volatile(
-      "{\n\t.reg .b32 z;\n\tmov.b32 z, 0;\n\t"
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, z, %5, z}, {%6, %7}, "
-      "{%0, %1, z, z};\n\t}\n"
-      : "+f"(d0), "+f"(d1), "=f"(x2), "=f"(x3)
-      : "r"(a0), "r"(a2), "r"(b0), "r"(b1));
-}
 
 // Four E4M3 codes (bytes 0..3) to two f16 pairs: bytes 0,1 -> lo, bytes 2,3 -> hi; exact.
 __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t codes, uint32_t& lo, uint32_t& hi) {
@@ -120,6 +101,13 @@ __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t codes, uint32_t& lo, 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// 8x8 transpose of a b16 matrix held one row pair per thread (mma accumulator layout).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t r;
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
   return r;
 }
 
@@ -285,6 +273,21 @@ __global__ void __launch_bounds__(kThreads, (NH == 1 && !kFp8) ? 4 : 3) splitk_k
       }
     }
   }
+  // transposed form (NH == 1): this thread's scores belong to rows 2t and 2t+1 of the group
+  int limT[2], loT[2];
+  float sl2T[2];
+  if constexpr (NH == 1) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int r = row0 + 2 * t + j;
+      const bool ok = r < R;
+      const int i = ok ? r / a.g : 0;
+      limT[j] = ok ? (a.causal ? min(kend, u.nk - u.nq + i + 1) : kend) : kend;
+      loT[j] = (ok && kWindow) ? u.nk - u.nq + i + 1 - a.window : 0;
+      // FP8: row 2t+j's Q was normalised by the lanes holding that row (gr = 2t + j)
+      sl2T[j] = kFp8 ? __shfl_sync(0xffffffffu, sl2[0], (2 * t + j) * 4) : a.scale_log2;
+    }
+  }
   // lowest key limit over the CTA's rows: steps ending at or below it need no mask
   int min_lim = kend;
   if (a.causal) min_lim = min(kend, u.nk - u.nq + row0 / a.g + 1);
@@ -378,6 +381,61 @@ __global__ void __launch_bounds__(kThreads, (NH == 1 && !kFp8) ? 4 : 3) splitk_k
     }
   };
 
+  // Transposed form: scores st = S^T (c0: key gr, row 2t; c1: key gr, row 2t+1; c2, c3: key
+  // gr + 8); the row max runs over the 8 lanes of equal t. Returns the B fragment of P^T.
+  auto softmax_stepT = [&](int kb, float (&st)[4], uint32_t& b0, uint32_t& b1) {
+    bool need_mask = kb + kKeysPerStep > min_lim;
+    if constexpr (kWindow) need_mask = need_mask || kb < max_lo;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int j = c & 1;
+      float s = st[c] * sl2T[j];
+      if (need_mask) {
+        const int key = kb + gr + 8 * (c >> 1);
+        if (key >= limT[j] || (kWindow && key < loT[j])) s = -INFINITY;
+      }
+      st[c] = s;
+    }
+    float mx[2] = {fmaxf(st[0], st[2]), fmaxf(st[1], st[3])};
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 4));
+      mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 8));
+      mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 16));
+    }
+    float mnew[2], muse[2];
+    bool grow = false;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      mnew[j] = fmaxf(m_run[j], mx[j]);
+      grow |= mnew[j] > m_run[j];
+      muse[j] = (mnew[j] == -INFINITY) ? 0.f : mnew[j];
+    }
+    if (__any_sync(0xffffffffu, grow)) {
+      float al[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        al[j] = (m_run[j] == -INFINITY) ? 0.f : ex2(m_run[j] - muse[j]);
+        l_part[j] *= al[j];
+      }
+#pragma unroll
+      for (int nu = 0; nu < 16; ++nu)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) oacc[nu][c] *= al[c];
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) m_run[j] = mnew[j];
+    float p[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      p[c] = ex2(st[c] - muse[c & 1]);
+      l_part[c & 1] += p[c];
+    }
+    // P^T of keys gr (and gr + 8) for rows 2t, 2t+1 -> transposed: row gr, keys 2t, 2t+1 (2t+8, 2t+9)
+    b0 = movmatrix_trans(kFp8 ? pack_f16x2(p[0], p[1]) : pack_bf16x2(p[0], p[1]));
+    b1 = movmatrix_trans(kFp8 ? pack_f16x2(p[2], p[3]) : pack_bf16x2(p[2], p[3]));
+  };
+
   if constexpr (!kFp8) {
     for (int kb = kstart + warp * kKeysPerStep; kb < kend; kb += kWarps * kKeysPerStep) {
       // ---- loads: K rows kb + nt*8 + gr (chunks t + 4s); V rows kb + {2t, 2t+1, 2t+8, 2t+9}
@@ -398,37 +456,59 @@ __global__ void __launch_bounds__(kThreads, (NH == 1 && !kFp8) ? 4 : 3) splitk_k
         va[x] = (key < kend) ? ld_stream(vr + 8 * gr) : make_uint4(0, 0, 0, 0);
         vb[x] = (key < kend) ? ld_stream(vr + 64 + 8 * gr) : make_uint4(0, 0, 0, 0);
       }
-      // ---- S = Q K^T for 16 keys: two n8 tiles, 8 k16 steps over the head dim
-      float sacc[2][4];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+      if constexpr (NH == 1) {
+        // ---- S^T = K Q^T: rows = keys gr / gr + 8 (the two K rows this thread loaded), 8 k16
+        // steps over the head dim; Q is the B operand (row gr of the group)
+        float st[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int kst = 0; kst < 8; ++kst) {
-          const uint4& c = kk[nt][kst >> 1];
-          const uint32_t b0 = (kst & 1) ? c.z : c.x;
-          const uint32_t b1 = (kst & 1) ? c.w : c.y;
-          if constexpr (NH == 2)
-            mma_bf16(sacc[nt], qa[kst], b0, b1);
-          else
-            mma_bf16_top(sacc[nt][0], sacc[nt][1], qa[kst][0], qa[kst][2], b0, b1);
+          const uint4& r0 = kk[0][kst >> 1];
+          const uint4& r1 = kk[1][kst >> 1];
+          const uint32_t af[4] = {(kst & 1) ? r0.z : r0.x, (kst & 1) ? r1.z : r1.x, (kst & 1) ? r0.w : r0.y,
+                                  (kst & 1) ? r1.w : r1.y};
+          mma_bf16(st, af, qa[kst][0], qa[kst][2]);
         }
-      }
-      uint32_t pa[4];
-      softmax_step(kb, sacc, pa);
-      // ---- O += P V over 16 output n-tiles
+        uint32_t b0, b1;
+        softmax_stepT(kb, st, b0, b1);
+        // ---- O^T += V^T P^T over 8 channel tiles: tile mu, row gr = channel 8 gr + mu (va),
+        // row gr + 8 = channel 64 + 8 gr + mu (vb); keys 2t, 2t+1 | 2t+8, 2t+9
 #pragma unroll
-      for (int nu = 0; nu < 16; ++nu) {
-        const int e = nu & 7;
-        const int w = e >> 1;
-        const uint32_t sel = (e & 1) ? 0x7632u : 0x5410u;
-        const uint32_t w0 = word((nu < 8) ? va[0] : vb[0], w), w1 = word((nu < 8) ? va[1] : vb[1], w);
-        const uint32_t w2 = word((nu < 8) ? va[2] : vb[2], w), w3 = word((nu < 8) ? va[3] : vb[3], w);
-        if constexpr (NH == 2) {
+        for (int mu = 0; mu < 8; ++mu) {
+          const int w = mu >> 1;
+          const uint32_t sel = (mu & 1) ? 0x7632u : 0x5410u;
+          const uint32_t af[4] = {__byte_perm(word(va[0], w), word(va[1], w), sel),
+                                  __byte_perm(word(vb[0], w), word(vb[1], w), sel),
+                                  __byte_perm(word(va[2], w), word(va[3], w), sel),
+                                  __byte_perm(word(vb[2], w), word(vb[3], w), sel)};
+          float(&acc)[4] = *reinterpret_cast<float(*)[4]>(&oacc[2 * mu][0]);
+          mma_bf16(acc, af, b0, b1);
+        }
+      } else {
+        // ---- S = Q K^T for 16 keys: two n8 tiles, 8 k16 steps over the head dim
+        float sacc[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+#pragma unroll
+          for (int kst = 0; kst < 8; ++kst) {
+            const uint4& c = kk[nt][kst >> 1];
+            const uint32_t b0 = (kst & 1) ? c.z : c.x;
+            const uint32_t b1 = (kst & 1) ? c.w : c.y;
+            mma_bf16(sacc[nt], qa[kst], b0, b1);
+          }
+        }
+        uint32_t pa[4];
+        softmax_step(kb, sacc, pa);
+        // ---- O += P V over 16 output n-tiles
+#pragma unroll
+        for (int nu = 0; nu < 16; ++nu) {
+          const int e = nu & 7;
+          const int w = e >> 1;
+          const uint32_t sel = (e & 1) ? 0x7632u : 0x5410u;
+          const uint32_t w0 = word((nu < 8) ? va[0] : vb[0], w), w1 = word((nu < 8) ? va[1] : vb[1], w);
+          const uint32_t w2 = word((nu < 8) ? va[2] : vb[2], w), w3 = word((nu < 8) ? va[3] : vb[3], w);
           float(&acc)[4] = *reinterpret_cast<float(*)[4]>(&oacc[nu][0]);
           mma_bf16(acc, pa, __byte_perm(w0, w1, sel), __byte_perm(w2, w3, sel));
-        } else {
-          mma_bf16_top(oacc[nu][0], oacc[nu][1], pa[0], pa[2], __byte_perm(w0, w1, sel), __byte_perm(w2, w3, sel));
         }
       }
     }
@@ -490,39 +570,62 @@ __global__ void __launch_bounds__(kThreads, (NH == 1 && !kFp8) ? 4 : 3) splitk_k
       st = (st + 1 == kFp8Stages) ? 0 : st + 1;
       // k-step kst takes word kst & 3 of chunk kst >> 2: codes (c0, c1) -> k = 2t, 2t+1 and
       // (c2, c3) -> k = 2t+8, 2t+9, the channel order Q was packed in
-      float sacc[2][4];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+      if constexpr (NH == 1) {
+        float st4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int kst = 0; kst < 8; ++kst) {
-          uint32_t b0, b1;
-          e4m3x4_to_f16x2x2(word(kk[nt][kst >> 2], kst & 3), b0, b1);
-          if constexpr (NH == 2)
-            mma_f16(sacc[nt], qa[kst], b0, b1);
-          else
-            mma_f16_top(sacc[nt][0], sacc[nt][1], qa[kst][0], qa[kst][2], b0, b1);
+          uint32_t af[4];
+          e4m3x4_to_f16x2x2(word(kk[0][kst >> 2], kst & 3), af[0], af[2]);
+          e4m3x4_to_f16x2x2(word(kk[1][kst >> 2], kst & 3), af[1], af[3]);
+          mma_f16(st4, af, qa[kst][0], qa[kst][2]);
         }
-      }
-      uint32_t pa[4];
-      softmax_step(kb, sacc, pa);
-      // n-tile nu, column gr = channel 16 gr + nu: code nu of each key's chunk. One byte
-      // permute pairs keys (2t, 2t+1) for channels nu and nu + 1 at once; likewise (2t+8, 2t+9).
+        uint32_t b0, b1;
+        softmax_stepT(kb, st4, b0, b1);
+        // tile mu, row gr = channel 16 gr + mu, row gr + 8 = channel 16 gr + 8 + mu: codes mu and
+        // 8 + mu of each key's chunk; one byte permute pairs keys (2t, 2t+1) for tiles mu, mu + 1
 #pragma unroll
-      for (int nu = 0; nu < 16; nu += 2) {
-        const int w = nu >> 2, k = nu & 3;
-        const uint32_t sel = k | ((4 + k) << 4) | ((k + 1) << 8) | ((5 + k) << 12);
-        uint32_t b0v[2], b1v[2];
-        e4m3x4_to_f16x2x2(__byte_perm(word(va[0], w), word(va[1], w), sel), b0v[0], b0v[1]);
-        e4m3x4_to_f16x2x2(__byte_perm(word(va[2], w), word(va[3], w), sel), b1v[0], b1v[1]);
+        for (int mu = 0; mu < 8; mu += 2) {
+          const int w = mu >> 2, k = mu & 3;
+          const uint32_t sel = k | ((4 + k) << 4) | ((k + 1) << 8) | ((5 + k) << 12);
+          uint32_t a0[2], a1[2], a2[2], a3[2];
+          e4m3x4_to_f16x2x2(__byte_perm(word(va[0], w), word(va[1], w), sel), a0[0], a0[1]);
+          e4m3x4_to_f16x2x2(__byte_perm(word(va[0], w + 2), word(va[1], w + 2), sel), a1[0], a1[1]);
+          e4m3x4_to_f16x2x2(__byte_perm(word(va[2], w), word(va[3], w), sel), a2[0], a2[1]);
+          e4m3x4_to_f16x2x2(__byte_perm(word(va[2], w + 2), word(va[3], w + 2), sel), a3[0], a3[1]);
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          const uint32_t b0 = b0v[h2], b1 = b1v[h2];
-          if constexpr (NH == 2) {
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const uint32_t af[4] = {a0[h2], a1[h2], a2[h2], a3[h2]};
+            float(&acc)[4] = *reinterpret_cast<float(*)[4]>(&oacc[2 * (mu + h2)][0]);
+            mma_f16(acc, af, b0, b1);
+          }
+        }
+      } else {
+        float sacc[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+#pragma unroll
+          for (int kst = 0; kst < 8; ++kst) {
+            uint32_t b0, b1;
+            e4m3x4_to_f16x2x2(word(kk[nt][kst >> 2], kst & 3), b0, b1);
+            mma_f16(sacc[nt], qa[kst], b0, b1);
+          }
+        }
+        uint32_t pa[4];
+        softmax_step(kb, sacc, pa);
+        // n-tile nu, column gr = channel 16 gr + nu: code nu of each key's chunk. One byte
+        // permute pairs keys (2t, 2t+1) for channels nu and nu + 1 at once; likewise (2t+8, 2t+9).
+#pragma unroll
+        for (int nu = 0; nu < 16; nu += 2) {
+          const int w = nu >> 2, k = nu & 3;
+          const uint32_t sel = k | ((4 + k) << 4) | ((k + 1) << 8) | ((5 + k) << 12);
+          uint32_t b0v[2], b1v[2];
+          e4m3x4_to_f16x2x2(__byte_perm(word(va[0], w), word(va[1], w), sel), b0v[0], b0v[1]);
+          e4m3x4_to_f16x2x2(__byte_perm(word(va[2], w), word(va[3], w), sel), b1v[0], b1v[1]);
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
             float(&acc)[4] = *reinterpret_cast<float(*)[4]>(&oacc[nu + h2][0]);
-            mma_f16(acc, pa, b0, b1);
-          } else {
-            mma_f16_top(oacc[nu + h2][0], oacc[nu + h2][1], pa[0], pa[2], b0, b1);
+            mma_f16(acc, pa, b0v[h2], b1v[h2]);
           }
         }
       }
@@ -542,36 +645,59 @@ __global__ void __launch_bounds__(kThreads, (NH == 1 && !kFp8) ? 4 : 3) splitk_k
     __shared__ float sm_o_static[kWarps][kRowsPerGroup][D + 4];
     sm_o = sm_o_static;
   }
+  if constexpr (NH == 1) {
+    // transposed: rows 2t, 2t+1; l summed over the 8 lanes (keys) of equal t
 #pragma unroll
-  for (int rr = 0; rr < NH; ++rr) {
-    float l = l_part[rr];
-    l += __shfl_xor_sync(0xffffffffu, l, 1);
-    l += __shfl_xor_sync(0xffffffffu, l, 2);
-    if (t == 0) {
-      sm_m[warp][gr + 8 * rr] = m_run[rr];
-      sm_l[warp][gr + 8 * rr] = l;
+    for (int j = 0; j < 2; ++j) {
+      float l = l_part[j];
+      l += __shfl_xor_sync(0xffffffffu, l, 4);
+      l += __shfl_xor_sync(0xffffffffu, l, 8);
+      l += __shfl_xor_sync(0xffffffffu, l, 16);
+      if (gr == 0) {
+        sm_m[warp][2 * t + j] = m_run[j];
+        sm_l[warp][2 * t + j] = l;
+      }
     }
-  }
-  if constexpr (!kFp8) {
+    // tile mu: c0, c1 -> channel A (rows 2t, 2t+1), c2, c3 -> channel B
+    const float* vsc = kFp8 ? a.v_scale + hkv * D : nullptr;
 #pragma unroll
-    for (int nu = 0; nu < 16; ++nu) {
-      sm_o[warp][gr][dv_of(nu, 2 * t)] = oacc[nu][0];
-      sm_o[warp][gr][dv_of(nu, 2 * t + 1)] = oacc[nu][1];
-      if constexpr (NH == 2) {
+    for (int mu = 0; mu < 8; ++mu) {
+      const int chA = kFp8 ? 16 * gr + mu : 8 * gr + mu;
+      const int chB = kFp8 ? 16 * gr + 8 + mu : 64 + 8 * gr + mu;
+      const float sA = kFp8 ? vsc[chA] : 1.f, sB = kFp8 ? vsc[chB] : 1.f;
+      sm_o[warp][2 * t][chA] = oacc[2 * mu][0] * sA;
+      sm_o[warp][2 * t + 1][chA] = oacc[2 * mu][1] * sA;
+      sm_o[warp][2 * t][chB] = oacc[2 * mu + 1][0] * sB;
+      sm_o[warp][2 * t + 1][chB] = oacc[2 * mu + 1][1] * sB;
+    }
+  } else {
+#pragma unroll
+    for (int rr = 0; rr < NH; ++rr) {
+      float l = l_part[rr];
+      l += __shfl_xor_sync(0xffffffffu, l, 1);
+      l += __shfl_xor_sync(0xffffffffu, l, 2);
+      if (t == 0) {
+        sm_m[warp][gr + 8 * rr] = m_run[rr];
+        sm_l[warp][gr + 8 * rr] = l;
+      }
+    }
+    if constexpr (!kFp8) {
+#pragma unroll
+      for (int nu = 0; nu < 16; ++nu) {
+        sm_o[warp][gr][dv_of(nu, 2 * t)] = oacc[nu][0];
+        sm_o[warp][gr][dv_of(nu, 2 * t + 1)] = oacc[nu][1];
         sm_o[warp][gr + 8][dv_of(nu, 2 * t)] = oacc[nu][2];
         sm_o[warp][gr + 8][dv_of(nu, 2 * t + 1)] = oacc[nu][3];
       }
-    }
-  } else {
-    // this thread's channels are 32t .. 32t + 31: apply the V scale there
-    const float* vsc = a.v_scale + hkv * D;
+    } else {
+      // this thread's channels are 32t .. 32t + 31: apply the V scale there
+      const float* vsc = a.v_scale + hkv * D;
 #pragma unroll
-    for (int nu = 0; nu < 16; ++nu) {
-      const int c0 = dv8_of(nu, 2 * t), c1 = dv8_of(nu, 2 * t + 1);
-      const float s0 = vsc[c0], s1 = vsc[c1];
-      sm_o[warp][gr][c0] = oacc[nu][0] * s0;
-      sm_o[warp][gr][c1] = oacc[nu][1] * s1;
-      if constexpr (NH == 2) {
+      for (int nu = 0; nu < 16; ++nu) {
+        const int c0 = dv8_of(nu, 2 * t), c1 = dv8_of(nu, 2 * t + 1);
+        const float s0 = vsc[c0], s1 = vsc[c1];
+        sm_o[warp][gr][c0] = oacc[nu][0] * s0;
+        sm_o[warp][gr][c1] = oacc[nu][1] * s1;
         sm_o[warp][gr + 8][c0] = oacc[nu][2] * s0;
         sm_o[warp][gr + 8][c1] = oacc[nu][3] * s1;
       }
