@@ -47,7 +47,7 @@ constexpr int kKeysPerStep = 16;
 // FP8 cache: each thread's 16-byte chunks of a step (4 of K, 4 of V) go through a ring of
 // kFp8Stages shared-memory slots with cp.async, so that the bytes in flight are bounded by
 // shared memory rather than registers
-constexpr int kFp8Stages = 4;
+constexpr int kFp8Stages = 3;
 constexpr int kFp8Chunks = 8;
 constexpr uint32_t kFp8StageBytes = kWarps * kFp8Chunks * 32 * 16;
 constexpr uint32_t kFp8SmemBytes = kFp8Stages * kFp8StageBytes;
@@ -179,7 +179,7 @@ __device__ __forceinline__ size_t ws_ml_index(const SplitKArgs& a, int unit, int
 // window (a separate instance, so the plain causal and paged paths carry no window registers);
 // kFp8: FP8 E4M3 cache with per-channel scales (k8, v8, k_scale, v_scale).
 template <int NH, bool kPaged, bool kWindow, bool kFp8>
-__global__ void __launch_bounds__(kThreads, (NH == 1 && !kFp8) ? 4 : 3) splitk_kernel(SplitKArgs a) {
+__global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(SplitKArgs a) {
   extern __shared__ __align__(16) uint8_t dsm[];  // FP8: the load ring, then the combine buffer
   const int split = blockIdx.x;
   const int hkv = blockIdx.y % a.Hkv;
