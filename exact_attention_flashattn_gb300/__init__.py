@@ -60,6 +60,10 @@ def lib() -> ctypes.CDLL:
         L.attn_fwd.restype = ci
         L.attn_fwd_window.argtypes = [vp, vp, vp, vp, vp] + [ci] * 7 + [cf, ci, vp]
         L.attn_fwd_window.restype = ci
+        L.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp] + [ci] * 7 + [cf, ci, vp, sz, vp]
+        L.attn_fwd_host.restype = ci
+        L.attn_fwd_host_workspace_size.argtypes = [ci] * 7
+        L.attn_fwd_host_workspace_size.restype = sz
         L.attn_decode_workspace_size.argtypes = [ci, ci, ci, ci]
         L.attn_decode_workspace_size.restype = sz
         L.attn_decode.argtypes = [vp, vp, vp, vp, vp] + [ci] * 6 + [cf, vp, vp, sz, vp]
@@ -170,6 +174,49 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = T
     rc = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse_t), B, Hq, Hkv, Nq, Nk, d, int(bool(causal)),
                         _scale(scale, d), dt, _stream(stream))
     _check(rc, "attn_fwd")
+    return out, lse_t
+
+
+def fwd_host_workspace_size(B: int, Hq: int, Hkv: int, Nq: int, Nk: int, d: int, dtype=torch.bfloat16) -> int:
+    dt = DTYPE_BF16 if dtype == torch.bfloat16 else DTYPE_FP32
+    return int(lib().attn_fwd_host_workspace_size(B, Hq, Hkv, Nq, Nk, d, dt))
+
+
+def attn_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = True, scale: float | None = None,
+                  out: torch.Tensor | None = None, lse: torch.Tensor | bool | None = True,
+                  workspace: torch.Tensor | None = None, stream=None, device=None):
+    """attn_fwd on host (CPU) tensors, copies included; pinned memory lets them overlap the kernels.
+    The call is asynchronous on ``stream`` (the current stream of ``device`` by default): read
+    ``out`` after synchronising it."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        if not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous host tensor")
+    if q.dim() != 4 or k.dim() != 4 or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("q [B, Hq, Nq, d]; k, v [B, Hkv, Nk, d]")
+    B, Hq, Nq, d = q.shape
+    _, Hkv, Nk, _ = k.shape
+    if q.dtype not in (torch.bfloat16, torch.float32) or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must all be bf16 or all fp32")
+    dt = DTYPE_BF16 if q.dtype == torch.bfloat16 else DTYPE_FP32
+    if out is None:
+        out = torch.empty_like(q, pin_memory=q.is_pinned())
+    if out.is_cuda or out.dtype != q.dtype or tuple(out.shape) != tuple(q.shape) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous host tensor like q")
+    lse_t = None
+    if lse is True:
+        lse_t = torch.empty((B, Hq, Nq), dtype=torch.float32, pin_memory=q.is_pinned())
+    elif isinstance(lse, torch.Tensor):
+        lse_t = lse
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    need = int(lib().attn_fwd_host_workspace_size(B, Hq, Hkv, Nq, Nk, d, dt))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _cuda(workspace, "workspace")
+    with torch.cuda.device(dev):
+        rc = lib().attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse_t), B, Hq, Hkv, Nq, Nk, d,
+                                 int(bool(causal)), _scale(scale, d), dt, _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "attn_fwd_host")
     return out, lse_t
 
 

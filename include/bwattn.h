@@ -73,6 +73,27 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
              int Nk, int d, int causal, float scale, int dtype, void* stream);
 
 /*
+ * attn_fwd_host: attn_fwd on HOST-resident tensors (same shapes, layouts, dtypes and errors),
+ * copies included. The (sequence, KV head) units are cut into up to 8 chunks; each chunk's
+ * copies in, kernel and copies out run on library-owned streams so that transfers overlap
+ * kernels (no counterpart on the pages; it is the host-memory end of the same computation).
+ *
+ *   q, k, v, o, lse : HOST pointers in the attn_fwd layouts; page-locked memory is needed for
+ *                     the copies to overlap (pageable memory works, serialised); lse may be NULL
+ *   workspace       : DEVICE buffer, 256-byte aligned, of at least
+ *                     attn_fwd_host_workspace_size(B, Hq, Hkv, Nq, Nk, d, dtype) bytes (two
+ *                     chunks of staging); contents undefined on exit
+ *   stream          : the work starts after everything already queued on it, and work queued on
+ *                     it afterwards starts after the last copy out; the host buffers must stay
+ *                     valid until then
+ * Calls from several host threads are serialised while they enqueue (the streams are shared).
+ */
+int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+                  int Nk, int d, int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
+                  void* stream);
+size_t attn_fwd_host_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d, int dtype);
+
+/*
  * attn_fwd_window: causal prefill with a sliding window ("Attention Computation in Practice",
  * "Masking variants": sliding window i - W < j <= i). Same layouts, dtypes and errors as
  * attn_fwd with causal = 1; query i sees keys j with i' - window < j <= i', i' = i + (Nk - Nq).

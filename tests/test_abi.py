@@ -28,7 +28,7 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ("attn_fwd", "attn_fwd_window", "attn_decode", "attn_decode_paged", "attn_decode_fp8",
+    for n in ("attn_fwd", "attn_fwd_window", "attn_fwd_host", "attn_fwd_host_workspace_size", "attn_decode", "attn_decode_paged", "attn_decode_fp8",
               "attn_decode_paged_fp8", "attn_varlen", "attn_varlen_window",
               "attn_decode_workspace_size", "attn_varlen_workspace_size",
               "bwattn_get_status", "bwattn_clear_status", "bwattn_last_cuda_error", "bwattn_status_string",
@@ -173,6 +173,30 @@ def test_python_binding_fp8_checks():
     with pytest.raises(ValueError):
         bw.attn_decode_fp8(q, torch.zeros(1, 1, 4, 128, dtype=torch.uint8), torch.zeros(1, 1, 4, 128, dtype=torch.uint8),
                            torch.ones(1, 128), torch.ones(1, 128), torch.zeros(1, dtype=torch.int32), 1)
+
+
+def test_fwd_host_argument_errors(L):
+    HOSTP = 0x20000  # never dereferenced: validation fails (or the work is empty) before any copy
+
+    def fh(**kw):
+        a = dict(q=HOSTP, k=HOSTP, v=HOSTP, o=HOSTP, lse=None, B=2, Hq=4, Hkv=2, Nq=64, Nk=64, d=128, causal=1,
+                 scale=0.1, dtype=bw.DTYPE_BF16, ws=0x40000, wsb=1 << 40, stream=None)
+        a.update(kw)
+        return L.attn_fwd_host(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Hq"], a["Hkv"], a["Nq"], a["Nk"],
+                               a["d"], a["causal"], a["scale"], a["dtype"], a["ws"], a["wsb"], a["stream"])
+    need = L.attn_fwd_host_workspace_size(2, 4, 2, 64, 64, 128, bw.DTYPE_BF16)
+    # two slots of (q, k, v, o, lse) for one chunk: units = 4, one unit per chunk
+    assert need == 2 * (2 * 2 * 64 * 128 * 2 + 2 * 64 * 128 * 2 + 512)
+    assert L.attn_fwd_host_workspace_size(2, 4, 3, 64, 64, 128, bw.DTYPE_BF16) == 0
+    assert fh(ws=None) == bw.ERR_INVALID_ARG
+    assert fh(ws=0x40000 + 16) == bw.ERR_INVALID_ARG  # 256-byte alignment
+    assert fh(wsb=need - 1) == bw.ERR_INVALID_ARG
+    assert fh(q=None) == bw.ERR_INVALID_ARG
+    assert fh(d=96) == bw.ERR_UNSUPPORTED
+    assert fh(dtype=7) == bw.ERR_UNSUPPORTED
+    assert fh(scale=0.0) == bw.ERR_INVALID_ARG
+    assert fh(causal=3) == bw.ERR_INVALID_ARG
+    assert fh(B=0, q=None, k=None, v=None, o=None, ws=None) == bw.OK
 
 
 def test_python_binding_rejects_window_without_causal():

@@ -412,6 +412,42 @@ def test_varlen_workload_full_size_sampled_rows():
     assert torch.isfinite(o).all()
 
 
+# ------------------------------------------------------------------ host-buffer prefill
+# attn_fwd_host runs the same kernel on chunks of (sequence, KV head) units: every output bit
+# must equal the device call's, and the oracle's within the bf16 bars.
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d,dtype,pinned", [
+    (2, 8, 2, 700, 700, 128, torch.bfloat16, True),     # 4 units, one per chunk
+    (5, 4, 2, 300, 513, 64, torch.bfloat16, True),      # 10 units -> 5 chunks of 2
+    (3, 2, 1, 200, 333, 128, torch.bfloat16, False),    # pageable host memory
+    (1, 1, 1, 512, 512, 64, torch.float32, True),       # the fp32 path
+])
+def test_fwd_host_matches_device_call(B, Hq, Hkv, Nq, Nk, d, dtype, pinned):
+    q, k, v = wl.prefill_inputs(B, Hq, Hkv, Nq, Nk, d, dtype, seed=61 + Nq)
+    if pinned:
+        q, k, v = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    o_h, l_h = bw.attn_fwd_host(q, k, v, causal=True)
+    o_d, l_d = bw.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o_h, o_d.cpu()) and torch.equal(l_h, l_d.cpu())
+    if dtype == torch.bfloat16:
+        o_ref, lse_ref = oracle.attention(f64(q), f64(k), f64(v), True, method="tiled", block=128)
+        check_bf16(o_h, o_ref, l_h, lse_ref, what=("host", B, Hq, Hkv, Nq, Nk, d))
+
+
+def test_fwd_host_no_keys_and_no_lse():
+    q, k, v = wl.prefill_inputs(2, 4, 2, 100, 0, 128, torch.bfloat16, seed=63)
+    o, l = bw.attn_fwd_host(q.pin_memory(), k, v, causal=False)
+    torch.cuda.synchronize()
+    assert torch.all(o == 0) and torch.all(torch.isneginf(l))
+    q, k, v = wl.prefill_inputs(2, 4, 2, 100, 100, 128, torch.bfloat16, seed=64)
+    o2, l2 = bw.attn_fwd_host(q.pin_memory(), k.pin_memory(), v.pin_memory(), causal=True, lse=None)
+    o3, _ = bw.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True)
+    torch.cuda.synchronize()
+    assert l2 is None and torch.equal(o2, o3.cpu())
+
+
 # ------------------------------------------------------------------ sliding window
 # "Attention Computation in Practice", Masking variants: query i sees keys i' - W < j <= i'.
 
