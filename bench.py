@@ -9,9 +9,10 @@ gather, window, varlen dispatch).
 
 Timing: W untimed warm-up steps, then K steps bracketed by a barrier and a device synchronize,
 CUDA events on the launching stream; every workload's inputs are larger than L2 (129 MB), so no
-flush is needed between steps. ``e2e`` repeats the headline through the public API with pinned
-host buffers, host-to-device copies of the inputs and device-to-host copies of O and LSE inside
-the timed region. ``cpu_baseline`` times the fp64 oracle (as it stands) on a bounded sample.
+flush is needed between steps. ``e2e`` repeats the headline through the host-buffer entry point
+(``attn_fwd_host``) with pinned host buffers: the host-to-device copies of the inputs and the
+device-to-host copies of O and LSE are inside the timed region (chunked and overlapped with the
+kernels by the library). ``cpu_baseline`` times the fp64 oracle (as it stands) on a bounded sample.
 
 ``--impl reference`` times the oracle itself on the host cores as the reference arm (a bounded
 sample of the headline workload per step). With ``--gpus N`` under torchrun every rank runs an
