@@ -45,10 +45,10 @@ HEADLINE = "prefill_causal_b4_h32_n4096_d128"
 # only while the kernel source is the profiled one (checked by hash); otherwise reported null.
 PROFILED_TRAFFIC = {
     "kernel_source": "exact_attention_flashattn_gb300/csrc/prefill_tc.cu",
-    "sha256": "01adb089c303aeb7127082863b3f432f6e2845f0a5762d20683166a770bcd1c6",
-    # (201.49 MB read + 45.54 MB written) at B=2 (profiles/prefill_tc_b2_h32_n4096_d128.md),
+    "sha256": "346fc1a9951c6d460d15f610e48039785f8815bfc486fae2bf0adb84bebc97e2",
+    # (201.49 MB read + 45.85 MB written) at B=2 (profiles/prefill_tc_b2_h32_n4096_d128.md),
     # scaled x2 to the B=4 launch: traffic grows with the number of (batch, head) units
-    "bytes_per_launch": 494064640,
+    "bytes_per_launch": 494670336,
 }
 METRIC = "prefill TFLOP/s and decode KV GB/s, 1×GB300, as fraction of roofline"
 L2_BYTES = 129 * 1024 * 1024

@@ -49,6 +49,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max g
 constexpr int kBandUnits = 16;             // (sequence, head) units per band of the item list
 constexpr int kItemSlots = 2;              // depth of the item queue from producer to consumers
 constexpr int kItemConsumers = 1 + 8;      // MMA thread + one lane of each softmax warp
+constexpr int kEarlyLoads = 2;             // K/V loads of an item issued before its Q
 
 template <int D>
 struct Cfg {
@@ -279,14 +280,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         bar->item_q[qs] = idx;
         mbar_arrive(&bar->item_full[qs]);
         if (idx < 0) break;
-        // Q buffers are free once every S MMA of the previous item has completed
-        if (items > 0 && !(ok = mbar_wait(&bar->q_empty, (items - 1) & 1, tmo, abort))) break;
-        mbar_arrive_expect_tx(&bar->q_full, 2 * C::kQBytes);
-        for (int t = 0; t < 2; ++t)
-          for (int hf = 0; hf < C::kHalves; ++hf)
-            tma_tile(&a.tm_q, w, sQ + t * C::kQBytes + hf * (kBM * 128), &bar->q_full, hf, w.q_lo[t], true);
-        ++items;
+        // K/V loads need only ring slots: the first ones go out before the Q wait, whose
+        // buffers are free only once every S MMA of the previous item has completed
+        const int n_early = min(2 * w.nt_all, kEarlyLoads);
         for (int i = 0; i < 2 * w.nt_all; ++i, ++nload) {
+          if (i == n_early) {
+            if (items > 0 && !(ok = mbar_wait(&bar->q_empty, (items - 1) & 1, tmo, abort))) break;
+            mbar_arrive_expect_tx(&bar->q_full, 2 * C::kQBytes);
+            for (int t = 0; t < 2; ++t)
+              for (int hf = 0; hf < C::kHalves; ++hf)
+                tma_tile(&a.tm_q, w, sQ + t * C::kQBytes + hf * (kBM * 128), &bar->q_full, hf, w.q_lo[t], true);
+            ++items;
+          }
           const int slot = nload % C::kStages;
           const int round = nload / C::kStages;
           if (round > 0 && !(ok = mbar_wait(&bar->kv_empty[slot], (round - 1) & 1, tmo, abort))) break;
@@ -294,6 +299,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           for (int hf = 0; hf < C::kHalves; ++hf)
             tma_tile((i & 1) ? &a.tm_v : &a.tm_k, w, sRing + slot * C::kTileBytes + hf * (kBN * 128),
                      &bar->kv_full[slot], hf, (w.jmin + (i >> 1)) * kBN, false);
+        }
+        if (ok && n_early == 2 * w.nt_all) {  // items with no more than kEarlyLoads loads
+          if (items > 0 && !(ok = mbar_wait(&bar->q_empty, (items - 1) & 1, tmo, abort))) break;
+          mbar_arrive_expect_tx(&bar->q_full, 2 * C::kQBytes);
+          for (int t = 0; t < 2; ++t)
+            for (int hf = 0; hf < C::kHalves; ++hf)
+              tma_tile(&a.tm_q, w, sQ + t * C::kQBytes + hf * (kBM * 128), &bar->q_full, hf, w.q_lo[t], true);
+          ++items;
         }
       }
       if (!ok) raise_timeout(abort, status);
