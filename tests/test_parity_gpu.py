@@ -549,6 +549,66 @@ def test_varlen_window(W):
     check_bf16(o, o_ref, lse, lse_ref, what=("varlen window", W))
 
 
+# ------------------------------------------------------------------ CUDA graphs and streams
+# The per-launch device state (the prefill's item-counter pair, the decode's merge-ticket block)
+# is taken on the host when a call is enqueued and left reset by the kernels, so a captured
+# graph may be replayed, and calls on different streams do not share it.
+
+
+def test_graph_capture_and_replay_matches_eager():
+    qp, kp, vp = wl.prefill_inputs(1, 4, 2, 384, 384, 128, torch.bfloat16, seed=71)
+    qd, kc, vc, nk = wl.decode_inputs(2, 8, 2, 600, 128, torch.bfloat16, seed=72, nk=[600, 333])
+    qp, kp, vp, qd, kc, vc, nk = (t.cuda() for t in (qp, kp, vp, qd, kc, vc, nk))
+    o_e, l_e = bw.attn_fwd(qp, kp, vp, causal=True)
+    od_e, ld_e = bw.attn_decode(qd, kc, vc, nk, num_splits=4)
+    o, lse = torch.empty_like(o_e), torch.empty_like(l_e)
+    od, ldd = torch.empty_like(od_e), torch.empty_like(ld_e)
+    ws = torch.empty(bw.decode_workspace_size(2, 8, 128, 4), dtype=torch.uint8, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # warm the libraries' one-time setup outside the capture
+        bw.attn_fwd(qp, kp, vp, causal=True, out=o, lse=lse)
+        bw.attn_decode(qd, kc, vc, nk, num_splits=4, workspace=ws, out=od, lse=ldd)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        bw.attn_fwd(qp, kp, vp, causal=True, out=o, lse=lse)
+        bw.attn_decode(qd, kc, vc, nk, num_splits=4, workspace=ws, out=od, lse=ldd)
+    for _ in range(3):
+        o.zero_()
+        od.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(o, o_e) and torch.equal(lse, l_e)
+        assert torch.equal(od, od_e) and torch.equal(ldd, ld_e)
+
+
+def test_concurrent_calls_on_two_streams():
+    qd, kc, vc, nk = wl.decode_inputs(4, 16, 4, 1000, 128, torch.bfloat16, seed=73, nk=[1000, 999, 17, 512])
+    qd, kc, vc, nk = (t.cuda() for t in (qd, kc, vc, nk))
+    qp, kp, vp = (t.cuda() for t in wl.prefill_inputs(2, 4, 4, 640, 640, 128, torch.bfloat16, seed=74))
+    od_e, _ = bw.attn_decode(qd, kc, vc, nk, num_splits=8)
+    op_e, _ = bw.attn_fwd(qp, kp, vp, causal=True)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    ws1 = torch.empty(bw.decode_workspace_size(4, 16, 128, 8), dtype=torch.uint8, device="cuda")
+    ws2 = torch.empty_like(ws1)
+    outs = []
+    for _ in range(4):
+        with torch.cuda.stream(s1):
+            a = bw.attn_decode(qd, kc, vc, nk, num_splits=8, workspace=ws1)[0]
+            b = bw.attn_fwd(qp, kp, vp, causal=True)[0]
+        with torch.cuda.stream(s2):
+            c = bw.attn_decode(qd, kc, vc, nk, num_splits=8, workspace=ws2)[0]
+            d = bw.attn_fwd(qp, kp, vp, causal=True)[0]
+        outs.append((a, b, c, d))
+    torch.cuda.synchronize()
+    for a, b, c, d in outs:
+        assert torch.equal(a, od_e) and torch.equal(c, od_e)
+        assert torch.equal(b, op_e) and torch.equal(d, op_e)
+
+
 # ------------------------------------------------------------------ status and failure detection
 
 
