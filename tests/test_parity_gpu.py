@@ -549,6 +549,61 @@ def test_varlen_window(W):
     check_bf16(o, o_ref, lse, lse_ref, what=("varlen window", W))
 
 
+# ------------------------------------------------------------------ edge cases
+
+
+def test_varlen_with_empty_and_single_token_sequences():
+    # a sequence with no queries, one with a single query and a single key, one whose queries
+    # outnumber nothing: every path must handle them and leave other sequences exact
+    nq = [0, 1, 5, 130, 1, 0]
+    nk = [40, 1, 5, 900, 2048, 0]
+    q, k, v, cq, ck = wl.varlen_inputs(nq, nk, 8, 2, 128, torch.bfloat16, seed=81)
+    o_ref, lse_ref = oracle.varlen(f64(q), f64(k), f64(v), cq.numpy(), ck.numpy(), True, method="tiled", block=128)
+    o, lse = bw.attn_varlen(q.cuda(), k.cuda(), v.cuda(), cq.cuda(), ck.cuda(), max(nq), max(nk), causal=True)
+    torch.cuda.synchronize()
+    check_bf16(o, o_ref, lse, lse_ref, what="varlen edge")
+
+
+def test_decode_all_sequences_empty():
+    q, kc, vc, nk = wl.decode_inputs(3, 8, 2, 64, 128, torch.bfloat16, seed=82, nk=[0, 0, 0])
+    for S in (1, 5, 40):  # fused merge and separate merge
+        o, lse = bw.attn_decode(q.cuda(), kc.cuda(), vc.cuda(), nk.cuda(), num_splits=S)
+        torch.cuda.synchronize()
+        assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
+
+
+def test_prefill_single_query_long_keys():
+    # Nq = 1 against 5000 keys (bottom-right causal: the query sees every key) on both dtypes
+    for dtype, tol in ((torch.bfloat16, None), (torch.float32, TOL_FP32_MAX)):
+        q, k, v = wl.prefill_inputs(2, 4, 2, 1, 5000, 128, dtype, seed=83)
+        o_ref, lse_ref = oracle.attention(f64(q), f64(k), f64(v), True, method="tiled", block=128)
+        o, lse = bw.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True)
+        torch.cuda.synchronize()
+        if tol is None:
+            check_bf16(o, o_ref, lse, lse_ref, what="Nq=1")
+        else:
+            assert np.abs(f64(o) - o_ref).max() <= tol
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_window_head_dim_and_gqa(d):
+    q, k, v = wl.prefill_inputs(2, 8, 2, 500, 777, d, torch.bfloat16, seed=84 + d)
+    o_ref, lse_ref = oracle.attention(f64(q), f64(k), f64(v), True, method="tiled", block=128, window=300)
+    o, lse = bw.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True, window=300)
+    torch.cuda.synchronize()
+    check_bf16(o, o_ref, lse, lse_ref, what=("window d", d))
+
+
+def test_decode_large_group_and_many_heads():
+    # g = 16 (16-row MMA form) and g = 32 (two row groups) with 96 KV heads' worth of units
+    for Hq, Hkv in ((64, 4), (128, 4)):
+        q, kc, vc, nk = wl.decode_inputs(2, Hq, Hkv, 700, 128, torch.bfloat16, seed=85 + Hq, nk=[700, 301])
+        o_ref, lse_ref = oracle.decode(f64(q), f64(kc), f64(vc), nk.numpy(), method="splitk", workers=6)
+        o, lse = bw.attn_decode(q.cuda(), kc.cuda(), vc.cuda(), nk.cuda(), num_splits=6)
+        torch.cuda.synchronize()
+        check_bf16(o, o_ref, lse, lse_ref, what=("decode g", Hq // Hkv))
+
+
 # ------------------------------------------------------------------ CUDA graphs and streams
 # The per-launch device state (the prefill's item-counter pair, the decode's merge-ticket block)
 # is taken on the host when a call is enqueued and left reset by the kernels, so a captured
