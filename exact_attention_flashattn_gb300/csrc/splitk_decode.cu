@@ -181,6 +181,8 @@ __device__ __forceinline__ size_t ws_ml_index(const SplitKArgs& a, int unit, int
 template <int NH, bool kPaged, bool kWindow, bool kFp8>
 __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(SplitKArgs a) {
   extern __shared__ __align__(16) uint8_t dsm[];  // FP8: the load ring, then the combine buffer
+  // a dependent merge launch may be scheduled from now on (it waits for this grid to complete)
+  asm volatile("griddepcontrol.launch_dependents;");
   const int split = blockIdx.x;
   const int hkv = blockIdx.y % a.Hkv;
   const int grp = blockIdx.y / a.Hkv;
@@ -802,6 +804,8 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
 // first; each warp then sums its share of the splits with weights e^{m_s - M}, and the warps'
 // sums are added in shared memory.
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(MergeArgs a) {
+  // the split-K pass (the grid this launch depends on) has completed from here on
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int unit = blockIdx.x / a.rows_max;
   const int r = blockIdx.x % a.rows_max;
   const int seq = unit / a.Hkv, hkv = unit % a.Hkv;
@@ -912,10 +916,22 @@ cudaError_t launch_splitk(const SplitKArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// The merge is a programmatic dependent launch: its CTAs may be scheduled while the split-K
+// pass finishes (the split kernel signals this at its start) and wait for that grid to complete,
+// with its writes visible, before reading any partial.
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
   const long blocks = static_cast<long>(a.num_seqs) * a.Hkv * a.rows_max;
-  merge_kernel<<<static_cast<unsigned>(blocks), kMergeThreads, 0, stream>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, merge_kernel, a);
 }
 
 }  // namespace bw
