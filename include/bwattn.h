@@ -19,7 +19,8 @@
  *
  * Conventions shared by every call:
  *   - Every tensor pointer is a DEVICE pointer owned by the caller, contiguous in the layout
- *     given, 16-byte aligned. The library never allocates, frees or synchronises.
+ *     given, 16-byte aligned (attn_fwd_host alone takes host pointers). The library never
+ *     allocates or frees memory and never synchronises the host.
  *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*; NULL = the
  *     legacy default stream) and returns a status code. Argument checks happen on the host
  *     before any CUDA call, so a rejected call has no side effect.
@@ -29,8 +30,12 @@
  *     written as fp32. Passing lse = NULL skips it.
  *   - Inputs are bf16 (IEEE bfloat16) unless a dtype argument says otherwise; arithmetic is
  *     fp32 (tensor cores with fp32 accumulation for bf16 inputs, fp32 FMA for fp32 inputs).
- *   - The library keeps no state across calls except a device status word that records a
- *     timed-out internal wait (see bwattn_get_status); it is thread-safe.
+ *   - State kept across calls: a device status word that records a timed-out internal wait
+ *     (see bwattn_get_status); rings of per-launch device counters (the prefill's item
+ *     counters, the decode's merge tickets), each launch taking its share when it is enqueued
+ *     and leaving it reset; the static scratch of attn_decode_static; the streams and events
+ *     of attn_fwd_host. Calls are thread-safe and may be captured into CUDA graphs (except
+ *     attn_fwd_host).
  */
 #ifndef BWATTN_H
 #define BWATTN_H
