@@ -338,6 +338,7 @@ int run_decode(bw::SplitKArgs& a, int B, int Hq, int Hkv, int g, int num_splits,
   if (a.tickets) return BWATTN_OK;  // merged by the last CTA of each unit
   bw::MergeArgs m{};
   m.ws = a.ws;
+  m.d = a.d;
   m.o = static_cast<uint16_t*>(o);
   m.lse = lse;
   m.cu_q = m.cu_k = nullptr;
@@ -365,7 +366,7 @@ int decode_contig(const void* q, const void* kcache, const void* vcache, const f
   if (Hq % Hkv != 0 || !good_scale(scale) || num_splits < 1 || num_splits > 1024) return BWATTN_ERR_INVALID_ARG;
   if (B > 65535) return BWATTN_ERR_INVALID_ARG;
   const int g = Hq / Hkv;
-  if (d != 128 || g > 32 || Hkv > 32767) return BWATTN_ERR_UNSUPPORTED;
+  if ((d != 64 && d != 128) || (fp8 && d != 128) || g > 32 || Hkv > 32767) return BWATTN_ERR_UNSUPPORTED;
   if (B == 0) return BWATTN_OK;
   if (!q || !kcache || !vcache || !o || !nk || !workspace) return BWATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) || !aligned16(workspace) ||
@@ -375,6 +376,7 @@ int decode_contig(const void* q, const void* kcache, const void* vcache, const f
   // workspace: units = B * Hkv, rows_max = g
   if (workspace_bytes < bw::splitk_ws_bytes(B * Hkv, num_splits, g, d)) return BWATTN_ERR_INVALID_ARG;
   bw::SplitKArgs a{};
+  a.d = d;
   a.q = static_cast<const uint16_t*>(q);
   if (fp8) {
     a.k8 = static_cast<const uint8_t*>(kcache);
@@ -407,7 +409,7 @@ int decode_paged(const void* q, const void* k_pages, const void* v_pages, const 
   if (Hq % Hkv != 0 || !good_scale(scale) || num_splits < 1 || num_splits > 1024) return BWATTN_ERR_INVALID_ARG;
   if (B > 65535 || static_cast<int64_t>(max_pages_per_seq) * page_size > 0x7fffffff) return BWATTN_ERR_INVALID_ARG;
   const int g = Hq / Hkv;
-  if (d != 128 || g > 32 || Hkv > 32767) return BWATTN_ERR_UNSUPPORTED;
+  if ((d != 64 && d != 128) || (fp8 && d != 128) || g > 32 || Hkv > 32767) return BWATTN_ERR_UNSUPPORTED;
   if (B == 0) return BWATTN_OK;
   if (!q || !k_pages || !v_pages || !o || !block_table || !nk || !workspace) return BWATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o) || !aligned16(workspace) ||
@@ -416,6 +418,7 @@ int decode_paged(const void* q, const void* k_pages, const void* v_pages, const 
   if (fp8 && (!k_scale || !v_scale || !aligned16(k_scale) || !aligned16(v_scale))) return BWATTN_ERR_INVALID_ARG;
   if (workspace_bytes < bw::splitk_ws_bytes(B * Hkv, num_splits, g, d)) return BWATTN_ERR_INVALID_ARG;
   bw::SplitKArgs a{};
+  a.d = d;
   a.q = static_cast<const uint16_t*>(q);
   if (fp8) {
     a.k8 = static_cast<const uint8_t*>(k_pages);
@@ -489,7 +492,7 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
     return BWATTN_ERR_INVALID_ARG;
   if (num_seqs > 65535 || Hq > 65535) return BWATTN_ERR_INVALID_ARG;
   const int g = Hq / Hkv;
-  if (d != 128 || g > kSmallRowsLimit) return BWATTN_ERR_UNSUPPORTED;
+  if ((d != 64 && d != 128) || g > kSmallRowsLimit) return BWATTN_ERR_UNSUPPORTED;
   if (num_seqs == 0 || total_q == 0 || max_seqlen_q == 0) return BWATTN_OK;
   if (!q || !o || !cu_seqlens_q || !cu_seqlens_k || !workspace || (total_k > 0 && (!k || !v)))
     return BWATTN_ERR_INVALID_ARG;
@@ -542,6 +545,7 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
   }
   // 2) sequences with few queries: split-K kernel with the (query, head) rows packed, then merge
   bw::SplitKArgs s{};
+  s.d = d;
   s.q = static_cast<const uint16_t*>(q);
   s.k = static_cast<const uint16_t*>(k);
   s.v = static_cast<const uint16_t*>(v);
@@ -576,6 +580,7 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
   if (s.tickets) return BWATTN_OK;  // merged by the last CTA of each unit
   bw::MergeArgs m{};
   m.ws = s.ws;
+  m.d = d;
   m.o = static_cast<uint16_t*>(o);
   m.lse = lse;
   m.cu_q = cu_seqlens_q;

@@ -38,6 +38,7 @@ struct SplitKArgs {
   const int32_t* cu_q;  // varlen: [num_seqs + 1] (device), else null
   const int32_t* cu_k;
   int num_seqs, Hq, Hkv, g;
+  int d;              // head dim D: 64 or 128 (128 with an FP8 cache)
   int64_t kv_seq_stride;  // dense: elements between sequences' caches (Hkv * cap * D)
   int64_t kv_head_stride;  // elements between KV heads at the same key (dense: cap * D, varlen: D)
   int64_t kv_key_stride;   // elements between consecutive keys (dense: D, varlen: Hkv * D)
@@ -78,6 +79,7 @@ struct MergeArgs {
   const int32_t* cu_k;
   const int32_t* nk;
   int num_seqs, Hq, Hkv, g, num_splits, rows_max, small_rows_limit;
+  int d;  // head dim: 64 or 128
   int total_q;  // varlen: rows of the packed q / o (cu_seqlens_q is clamped to it)
   size_t ws_o_offset;
 };

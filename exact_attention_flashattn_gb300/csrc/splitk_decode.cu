@@ -39,7 +39,6 @@ namespace bw {
 
 namespace {
 
-constexpr int D = 128;
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kRowsPerGroup = 16;
@@ -115,8 +114,15 @@ __device__ __forceinline__ uint32_t word(const uint4& v, int w) {
   return w == 0 ? v.x : (w == 1 ? v.y : (w == 2 ? v.z : v.w));
 }
 
-// Output channel held by MMA column position p (0..7) of output n-tile nu (0..15).
+// Output channel held by MMA column position p (0..7) of output n-tile nu (0..D/8 - 1).
 __device__ __forceinline__ int dv_of(int nu, int p) { return (nu < 8) ? (8 * p + nu) : (64 + 8 * p + (nu - 8)); }
+// Transposed form: the channels held by rows gr (A) and gr + 8 (B) of output m-tile mu. d = 128:
+// va (channels 8 gr .. 8 gr + 7) feeds the A rows, vb (64 + 8 gr ..) the B rows; d = 64 has va
+// only, so its lo / hi halves feed the A / B rows: channels 8 gr + 2 mu and 8 gr + 2 mu + 1.
+template <int D>
+__device__ __forceinline__ int chA_of(int gr, int mu) { return D == 128 ? 8 * gr + mu : 8 * gr + 2 * mu; }
+template <int D>
+__device__ __forceinline__ int chB_of(int gr, int mu) { return D == 128 ? 64 + 8 * gr + mu : 8 * gr + 2 * mu + 1; }
 // The same for the FP8 cache, whose V loads are 16-channel chunks: column p of n-tile nu is
 // channel 16 p + nu.
 __device__ __forceinline__ int dv8_of(int nu, int p) { return 16 * p + nu; }
@@ -174,12 +180,17 @@ __device__ __forceinline__ size_t ws_ml_index(const SplitKArgs& a, int unit, int
   return ((static_cast<size_t>(unit) * a.num_splits + s) * a.rows_max + r) * 2;
 }
 
+// D = head dim (64 or 128; the FP8 cache is 128 only);
 // NH = number of 8-row halves of the 16-row MMA tile that carry real rows (1 or 2);
 // kPaged: keys are gathered page by page through the block table; kWindow: causal sliding
 // window (a separate instance, so the plain causal and paged paths carry no window registers);
 // kFp8: FP8 E4M3 cache with per-channel scales (k8, v8, k_scale, v_scale).
-template <int NH, bool kPaged, bool kWindow, bool kFp8>
+template <int D, int NH, bool kPaged, bool kWindow, bool kFp8>
 __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(SplitKArgs a) {
+  static_assert(D == 64 || D == 128, "head dim");
+  static_assert(!kFp8 || D == 128, "the FP8 cache layout is d = 128");
+  constexpr int kSteps = D / 16;  // k16 steps of S = Q K^T over the head dim
+  constexpr int kNT = D / 8;      // output n8 tiles of O (16-row form); 8-row pairs of them transposed
   extern __shared__ __align__(16) uint8_t dsm[];  // FP8: the load ring, then the combine buffer
   // a dependent merge launch may be scheduled from now on (it waits for this grid to complete)
   asm volatile("griddepcontrol.launch_dependents;");
@@ -204,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
 
   // Rows gr (and gr + 8) of this group: (query i, head hh) and their key limits [lo, lim).
   int lim[2], lo[2];
-  uint32_t qa[8][4];
+  uint32_t qa[kSteps][4];
   float sl2[2] = {a.scale_log2, a.scale_log2};  // FP8: the row's score scale (see below)
 #pragma unroll
   for (int rr = 0; rr < 2; ++rr) {
@@ -221,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
     const uint16_t* qrow = a.q + (static_cast<int64_t>(u.tok0 + i) * a.Hq + hkv * a.g + hh) * D;
     if constexpr (!kFp8) {
 #pragma unroll
-      for (int s = 0; s < 4; ++s) {
+      for (int s = 0; s < D / 32; ++s) {
         uint4 c = make_uint4(0, 0, 0, 0);
         if (ok) c = *reinterpret_cast<const uint4*>(qrow + 8 * (t + 4 * s));
         // k-step 2s uses words 0,1 of chunk t+4s; k-step 2s+1 words 2,3 (same permutation as K)
@@ -303,9 +314,9 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
     max_lo = u.nk - u.nq + last_r / a.g + 1 - a.window;
   }
 
-  float oacc[16][2 * NH];
+  float oacc[kNT][2 * NH];
 #pragma unroll
-  for (int nu = 0; nu < 16; ++nu)
+  for (int nu = 0; nu < kNT; ++nu)
 #pragma unroll
     for (int c = 0; c < 2 * NH; ++c) oacc[nu][c] = 0.f;
   float m_run[2] = {-INFINITY, -INFINITY};
@@ -358,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
         l_part[rr] *= al[rr];
       }
 #pragma unroll
-      for (int nu = 0; nu < 16; ++nu)
+      for (int nu = 0; nu < kNT; ++nu)
 #pragma unroll
         for (int c = 0; c < 2 * NH; ++c) oacc[nu][c] *= al[c >> 1];
     }
@@ -421,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
         l_part[j] *= al[j];
       }
 #pragma unroll
-      for (int nu = 0; nu < 16; ++nu)
+      for (int nu = 0; nu < kNT; ++nu)
 #pragma unroll
         for (int c = 0; c < 2; ++c) oacc[nu][c] *= al[c];
     }
@@ -441,14 +452,15 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
   if constexpr (!kFp8) {
     for (int kb = kstart + warp * kKeysPerStep; kb < kend; kb += kWarps * kKeysPerStep) {
       // ---- loads: K rows kb + nt*8 + gr (chunks t + 4s); V rows kb + {2t, 2t+1, 2t+8, 2t+9}
+      // (chunk gr into va; d = 128 also chunk 8 + gr into vb)
       const int64_t so = step_offset<kPaged>(a, seq, kb);
-      uint4 kk[2][4], va[4], vb[4];
+      uint4 kk[2][D / 32], va[4], vb[4];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
         const int key = kb + nt * 8 + gr;
         const uint16_t* kr = kbase + so + static_cast<int64_t>(nt * 8 + gr) * ks;
 #pragma unroll
-        for (int s = 0; s < 4; ++s)
+        for (int s = 0; s < D / 32; ++s)
           kk[nt][s] = (key < kend) ? ld_stream(kr + 8 * (t + 4 * s)) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
@@ -456,14 +468,14 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
         const int key = kb + 2 * t + (x & 1) + 8 * (x >> 1);
         const uint16_t* vr = vbase + so + static_cast<int64_t>(key - kb) * ks;
         va[x] = (key < kend) ? ld_stream(vr + 8 * gr) : make_uint4(0, 0, 0, 0);
-        vb[x] = (key < kend) ? ld_stream(vr + 64 + 8 * gr) : make_uint4(0, 0, 0, 0);
+        if constexpr (D == 128) vb[x] = (key < kend) ? ld_stream(vr + 64 + 8 * gr) : make_uint4(0, 0, 0, 0);
       }
       if constexpr (NH == 1) {
-        // ---- S^T = K Q^T: rows = keys gr / gr + 8 (the two K rows this thread loaded), 8 k16
-        // steps over the head dim; Q is the B operand (row gr of the group)
+        // ---- S^T = K Q^T: rows = keys gr / gr + 8 (the two K rows this thread loaded), D/16
+        // k16 steps over the head dim; Q is the B operand (row gr of the group)
         float st[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int kst = 0; kst < 8; ++kst) {
+        for (int kst = 0; kst < kSteps; ++kst) {
           const uint4& r0 = kk[0][kst >> 1];
           const uint4& r1 = kk[1][kst >> 1];
           const uint32_t af[4] = {(kst & 1) ? r0.z : r0.x, (kst & 1) ? r1.z : r1.x, (kst & 1) ? r0.w : r0.y,
@@ -472,27 +484,35 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
         }
         uint32_t b0, b1;
         softmax_stepT(kb, st, b0, b1);
-        // ---- O^T += V^T P^T over 8 channel tiles: tile mu, row gr = channel 8 gr + mu (va),
-        // row gr + 8 = channel 64 + 8 gr + mu (vb); keys 2t, 2t+1 | 2t+8, 2t+9
+        // ---- O^T += V^T P^T over D/16 channel tiles: tile mu, rows gr and gr + 8 = channels
+        // chA_of(gr, mu) and chB_of(gr, mu); keys 2t, 2t+1 | 2t+8, 2t+9
 #pragma unroll
-        for (int mu = 0; mu < 8; ++mu) {
-          const int w = mu >> 1;
-          const uint32_t sel = (mu & 1) ? 0x7632u : 0x5410u;
-          const uint32_t af[4] = {__byte_perm(word(va[0], w), word(va[1], w), sel),
-                                  __byte_perm(word(vb[0], w), word(vb[1], w), sel),
-                                  __byte_perm(word(va[2], w), word(va[3], w), sel),
-                                  __byte_perm(word(vb[2], w), word(vb[3], w), sel)};
+        for (int mu = 0; mu < D / 16; ++mu) {
+          uint32_t af[4];
+          if constexpr (D == 128) {
+            const int w = mu >> 1;
+            const uint32_t sel = (mu & 1) ? 0x7632u : 0x5410u;
+            af[0] = __byte_perm(word(va[0], w), word(va[1], w), sel);
+            af[1] = __byte_perm(word(vb[0], w), word(vb[1], w), sel);
+            af[2] = __byte_perm(word(va[2], w), word(va[3], w), sel);
+            af[3] = __byte_perm(word(vb[2], w), word(vb[3], w), sel);
+          } else {
+            af[0] = __byte_perm(word(va[0], mu), word(va[1], mu), 0x5410u);
+            af[1] = __byte_perm(word(va[0], mu), word(va[1], mu), 0x7632u);
+            af[2] = __byte_perm(word(va[2], mu), word(va[3], mu), 0x5410u);
+            af[3] = __byte_perm(word(va[2], mu), word(va[3], mu), 0x7632u);
+          }
           float(&acc)[4] = *reinterpret_cast<float(*)[4]>(&oacc[2 * mu][0]);
           mma_bf16(acc, af, b0, b1);
         }
       } else {
-        // ---- S = Q K^T for 16 keys: two n8 tiles, 8 k16 steps over the head dim
+        // ---- S = Q K^T for 16 keys: two n8 tiles, D/16 k16 steps over the head dim
         float sacc[2][4];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
           sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
 #pragma unroll
-          for (int kst = 0; kst < 8; ++kst) {
+          for (int kst = 0; kst < kSteps; ++kst) {
             const uint4& c = kk[nt][kst >> 1];
             const uint32_t b0 = (kst & 1) ? c.z : c.x;
             const uint32_t b1 = (kst & 1) ? c.w : c.y;
@@ -501,9 +521,9 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
         }
         uint32_t pa[4];
         softmax_step(kb, sacc, pa);
-        // ---- O += P V over 16 output n-tiles
+        // ---- O += P V over D/8 output n-tiles
 #pragma unroll
-        for (int nu = 0; nu < 16; ++nu) {
+        for (int nu = 0; nu < kNT; ++nu) {
           const int e = nu & 7;
           const int w = e >> 1;
           const uint32_t sel = (e & 1) ? 0x7632u : 0x5410u;
@@ -663,9 +683,9 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
     // tile mu: c0, c1 -> channel A (rows 2t, 2t+1), c2, c3 -> channel B
     const float* vsc = kFp8 ? a.v_scale + hkv * D : nullptr;
 #pragma unroll
-    for (int mu = 0; mu < 8; ++mu) {
-      const int chA = kFp8 ? 16 * gr + mu : 8 * gr + mu;
-      const int chB = kFp8 ? 16 * gr + 8 + mu : 64 + 8 * gr + mu;
+    for (int mu = 0; mu < D / 16; ++mu) {
+      const int chA = kFp8 ? 16 * gr + mu : chA_of<D>(gr, mu);
+      const int chB = kFp8 ? 16 * gr + 8 + mu : chB_of<D>(gr, mu);
       const float sA = kFp8 ? vsc[chA] : 1.f, sB = kFp8 ? vsc[chB] : 1.f;
       sm_o[warp][2 * t][chA] = oacc[2 * mu][0] * sA;
       sm_o[warp][2 * t + 1][chA] = oacc[2 * mu][1] * sA;
@@ -685,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
     }
     if constexpr (!kFp8) {
 #pragma unroll
-      for (int nu = 0; nu < 16; ++nu) {
+      for (int nu = 0; nu < kNT; ++nu) {
         sm_o[warp][gr][dv_of(nu, 2 * t)] = oacc[nu][0];
         sm_o[warp][gr][dv_of(nu, 2 * t + 1)] = oacc[nu][1];
         sm_o[warp][gr + 8][dv_of(nu, 2 * t)] = oacc[nu][2];
@@ -803,6 +823,7 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
 // One CTA per output row: merge the num_splits partials of (unit, row). The global max comes
 // first; each warp then sums its share of the splits with weights e^{m_s - M}, and the warps'
 // sums are added in shared memory.
+template <int D>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(MergeArgs a) {
   // the split-K pass (the grid this launch depends on) has completed from here on
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -846,6 +867,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(MergeArgs a) {
   for (int w = 1; w < kMW; ++w) M = fmaxf(M, sh_red[w]);
 
   // this warp's splits: s = warp, warp + kMW, ...; lane owns channels 4*lane .. 4*lane+3
+  // (d = 64: lanes 16..31 hold none and read channel 0 .. 3 again, their sums unused)
+  const int c4 = lane < D / 4 ? lane : 0;
   float L = 0.f;
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int s = warp; s < S; s += kMW) {
@@ -853,22 +876,22 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(MergeArgs a) {
     if (!(v.y > 0.f)) continue;
     const float f = ex2(v.x - M);
     L += f * v.y;
-    const float4 x = *reinterpret_cast<const float4*>(wo + s * o_stride + 4 * lane);
+    const float4 x = *reinterpret_cast<const float4*>(wo + s * o_stride + 4 * c4);
     o.x += f * x.x;
     o.y += f * x.y;
     o.z += f * x.z;
     o.w += f * x.w;
   }
-  sh_o[warp][lane] = o;
+  if (lane < D / 4) sh_o[warp][lane] = o;
   if (lane == 0) sh_l[warp] = L;
   __syncthreads();
-  if (warp != 0) return;
+  if (warp != 0 || lane >= D / 4) return;
   L = 0.f;
   o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
   for (int w = 0; w < kMW; ++w) {
     L += sh_l[w];
-    const float4 x = sh_o[w][lane];
+    const float4 x = sh_o[w][c4];
     o.x += x.x;
     o.y += x.y;
     o.z += x.z;
@@ -883,9 +906,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(MergeArgs a) {
   if (a.lse && lane == 0) a.lse[orow] = (L > 0.f) ? (M + log2f(L)) * kLn2 : -INFINITY;
 }
 
-}  // namespace
-
-cudaError_t launch_splitk(const SplitKArgs& a, cudaStream_t stream) {
+template <int D>
+cudaError_t launch_splitk_d(const SplitKArgs& a, cudaStream_t stream) {
   dim3 grid(a.num_splits, a.Hkv * a.row_groups, a.num_seqs);
   // every row group has at most 8 rows when the sequences' rows (n_q * g) never exceed 8
   const bool half = a.cu_q ? (a.small_rows_limit <= 8) : (a.g <= 8);
@@ -893,27 +915,41 @@ cudaError_t launch_splitk(const SplitKArgs& a, cudaStream_t stream) {
   const bool window = a.causal && a.window > 0;
   const bool fp8 = a.k8 != nullptr;
   if ((paged || fp8) && window) return cudaErrorInvalidValue;  // no entry point pairs them
-  if (fp8) {
-    static_assert(kFp8SmemBytes >= sizeof(float) * kWarps * kRowsPerGroup * (D + 4), "combine buffer");
-    auto k = half ? (paged ? splitk_kernel<1, true, false, true> : splitk_kernel<1, false, false, true>)
-                  : (paged ? splitk_kernel<2, true, false, true> : splitk_kernel<2, false, false, true>);
-    const cudaError_t e =
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kFp8SmemBytes));
-    if (e != cudaSuccess) return e;
-    k<<<grid, kThreads, kFp8SmemBytes, stream>>>(a);
-  } else if (window) {
+  if constexpr (D == 128) {
+    if (fp8) {
+      static_assert(kFp8SmemBytes >= sizeof(float) * kWarps * kRowsPerGroup * (D + 4), "combine buffer");
+      auto k = half ? (paged ? splitk_kernel<D, 1, true, false, true> : splitk_kernel<D, 1, false, false, true>)
+                    : (paged ? splitk_kernel<D, 2, true, false, true> : splitk_kernel<D, 2, false, false, true>);
+      const cudaError_t e =
+          cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kFp8SmemBytes));
+      if (e != cudaSuccess) return e;
+      k<<<grid, kThreads, kFp8SmemBytes, stream>>>(a);
+      return cudaGetLastError();
+    }
+  } else if (fp8) {
+    return cudaErrorInvalidValue;  // the FP8 cache is d = 128 only
+  }
+  if (window) {
     if (half)
-      splitk_kernel<1, false, true, false><<<grid, kThreads, 0, stream>>>(a);
+      splitk_kernel<D, 1, false, true, false><<<grid, kThreads, 0, stream>>>(a);
     else
-      splitk_kernel<2, false, true, false><<<grid, kThreads, 0, stream>>>(a);
+      splitk_kernel<D, 2, false, true, false><<<grid, kThreads, 0, stream>>>(a);
   } else if (half) {
-    paged ? splitk_kernel<1, true, false, false><<<grid, kThreads, 0, stream>>>(a)
-          : splitk_kernel<1, false, false, false><<<grid, kThreads, 0, stream>>>(a);
+    paged ? splitk_kernel<D, 1, true, false, false><<<grid, kThreads, 0, stream>>>(a)
+          : splitk_kernel<D, 1, false, false, false><<<grid, kThreads, 0, stream>>>(a);
   } else {
-    paged ? splitk_kernel<2, true, false, false><<<grid, kThreads, 0, stream>>>(a)
-          : splitk_kernel<2, false, false, false><<<grid, kThreads, 0, stream>>>(a);
+    paged ? splitk_kernel<D, 2, true, false, false><<<grid, kThreads, 0, stream>>>(a)
+          : splitk_kernel<D, 2, false, false, false><<<grid, kThreads, 0, stream>>>(a);
   }
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_splitk(const SplitKArgs& a, cudaStream_t stream) {
+  if (a.d == 64) return launch_splitk_d<64>(a, stream);
+  if (a.d == 128) return launch_splitk_d<128>(a, stream);
+  return cudaErrorInvalidValue;
 }
 
 // The merge is a programmatic dependent launch: its CTAs may be scheduled while the split-K
@@ -931,7 +967,9 @@ cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, merge_kernel, a);
+  if (a.d == 64) return cudaLaunchKernelEx(&cfg, merge_kernel<64>, a);
+  if (a.d == 128) return cudaLaunchKernelEx(&cfg, merge_kernel<128>, a);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace bw

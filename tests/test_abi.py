@@ -92,7 +92,12 @@ def test_decode_argument_errors(L):
     assert dec(L, S=0) == bw.ERR_INVALID_ARG
     assert dec(L, S=1025) == bw.ERR_INVALID_ARG
     assert dec(L, Hq=8, Hkv=3) == bw.ERR_INVALID_ARG
-    assert dec(L, d=64) == bw.ERR_UNSUPPORTED
+    assert dec(L, d=96) == bw.ERR_UNSUPPORTED
+    # d = 64 is accepted: its workspace is sized for 64 channels and checked against that
+    need64 = L.attn_decode_workspace_size(2, 8, 64, 4)
+    assert 0 < need64 < need
+    assert dec(L, d=64, wsb=need64 - 1) == bw.ERR_INVALID_ARG
+    assert dec(L, d=64, B=0, q=None) == bw.OK
     assert dec(L, Hq=66, Hkv=1) == bw.ERR_UNSUPPORTED
     assert dec(L, nk=FAKE + 2) == bw.ERR_INVALID_ARG
     assert dec(L, B=0, q=None) == bw.OK
@@ -110,7 +115,9 @@ def test_varlen_argument_errors(L):
     assert var(ws=None) == bw.ERR_INVALID_ARG
     assert var(wsb=16) == bw.ERR_INVALID_ARG
     assert var(Hq=8, Hkv=3) == bw.ERR_INVALID_ARG
-    assert var(d=64) == bw.ERR_UNSUPPORTED
+    assert var(d=96) == bw.ERR_UNSUPPORTED
+    assert var(d=64, wsb=16) == bw.ERR_INVALID_ARG
+    assert var(d=64, n=0) == bw.OK
     assert var(n=0) == bw.OK
     assert L.attn_varlen_workspace_size(3, 16, 8, 2, 128) > 0
 
@@ -227,5 +234,7 @@ def test_paged_decode_argument_errors(L):
     assert pag(npages=0) == bw.ERR_INVALID_ARG
     assert pag(table=FAKE + 2) == bw.ERR_INVALID_ARG
     assert pag(wsb=16) == bw.ERR_INVALID_ARG
-    assert pag(d=64) == bw.ERR_UNSUPPORTED
+    assert pag(d=96) == bw.ERR_UNSUPPORTED
+    assert pag(d=64, wsb=16) == bw.ERR_INVALID_ARG
+    assert pag(d=64, B=0, q=None) == bw.OK
     assert pag(B=0, q=None) == bw.OK

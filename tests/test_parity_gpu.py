@@ -549,6 +549,53 @@ def test_varlen_window(W):
     check_bf16(o, o_ref, lse, lse_ref, what=("varlen window", W))
 
 
+# ------------------------------------------------------------------ head dim 64 on the split-K paths
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,cap,nk,S", [
+    (3, 8, 2, 300, [300, 17, 0], 4),     # g = 4 (transposed form), ragged, an empty sequence
+    (1, 16, 2, 513, [513], 64),          # g = 8, 64 splits: the separate merge kernel
+    (2, 16, 1, 400, [400, 250], 3),      # g = 16 (16-row form), fused merge
+    (1, 32, 1, 200, [200], 40),          # g = 32: two row groups, separate merge
+])
+def test_decode_d64(B, Hq, Hkv, cap, nk, S):
+    q, kc, vc, nkt = wl.decode_inputs(B, Hq, Hkv, cap, 64, torch.bfloat16, seed=131 + cap, nk=nk)
+    o_ref, lse_ref = oracle.decode(f64(q), f64(kc), f64(vc), nkt.numpy(), method="splitk", workers=S)
+    o, lse = bw.attn_decode(q.cuda(), kc.cuda(), vc.cuda(), nkt.cuda(), num_splits=S)
+    torch.cuda.synchronize()
+    check_bf16(o, o_ref, lse, lse_ref, what=("d64", B, Hq, Hkv, cap, nk, S))
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,cap,nk,S,ps", [
+    (3, 8, 2, 256, [256, 17, 0], 4, 16),    # transposed form, 16-token pages
+    (2, 32, 2, 512, [512, 300], 9, 32),     # g = 16: 16-row form, 32-token pages
+])
+def test_decode_paged_d64_matches_oracle_and_contiguous(B, Hq, Hkv, cap, nk, S, ps):
+    q, kc, vc, nkt = wl.decode_inputs(B, Hq, Hkv, cap, 64, torch.bfloat16, seed=181 + cap, nk=nk)
+    kp, vp, table = wl.paged_from_dense(kc, vc, ps, seed=181)
+    o_ref, lse_ref = oracle.decode_paged(f64(q), f64(kp), f64(vp), table.numpy(), nkt.numpy(), method="splitk",
+                                         workers=S)
+    o, lse = bw.attn_decode_paged(q.cuda(), kp.cuda(), vp.cuda(), table.cuda(), nkt.cuda(), num_splits=S)
+    oc, lc = bw.attn_decode(q.cuda(), kc.cuda(), vc.cuda(), nkt.cuda(), num_splits=S)
+    torch.cuda.synchronize()
+    check_bf16(o, o_ref, lse, lse_ref, what=("paged d64", B, Hq, Hkv, cap, nk, S, ps))
+    # the same keys in the same order: the paged gather changes addresses only
+    assert torch.equal(o, oc) and torch.equal(lse, lc)
+
+
+@pytest.mark.parametrize("causal,W", [(True, 0), (False, 0), (True, 100)])
+def test_varlen_d64(causal, W):
+    nq = [1, 4, 8, 200, 300, 3, 129, 0]
+    nk = [50, 700, 8, 200, 1000, 2100, 129, 9]
+    q, k, v, cq, ck = wl.varlen_inputs(nq, nk, 8, 2, 64, torch.bfloat16, seed=151 + W + causal)
+    o_ref, lse_ref = oracle.varlen(f64(q), f64(k), f64(v), cq.numpy(), ck.numpy(), causal, method="tiled", block=128,
+                                   window=W)
+    o, lse = bw.attn_varlen(q.cuda(), k.cuda(), v.cuda(), cq.cuda(), ck.cuda(), max(nq), max(nk), causal=causal,
+                            window=W)
+    torch.cuda.synchronize()
+    check_bf16(o, o_ref, lse, lse_ref, what=("varlen d64", causal, W))
+
+
 # ------------------------------------------------------------------ edge cases
 
 

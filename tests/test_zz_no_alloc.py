@@ -59,10 +59,12 @@ def test_static_decode_matches_workspace_decode_twice(static_fn):
         dict(B=4, Hq=32, Hkv=8, cap=4096, nk=[4096, 1000, 0, 37], S=16, seed=71),
         # a different shape reusing the same array: g = 8, many small splits
         dict(B=1, Hq=64, Hkv=8, cap=20000, nk=[19999], S=96, seed=72),
+        # head dim 64 over the same array
+        dict(B=3, Hq=16, Hkv=2, cap=3000, nk=[3000, 5, 1234], S=24, seed=73, d=64),
     ]
     for c in cases:
-        q, kc, vc, nk = wl.decode_inputs(c["B"], c["Hq"], c["Hkv"], c["cap"], 128, torch.bfloat16, c["seed"],
-                                         nk=c["nk"], device="cuda")
+        q, kc, vc, nk = wl.decode_inputs(c["B"], c["Hq"], c["Hkv"], c["cap"], c.get("d", 128), torch.bfloat16,
+                                         c["seed"], nk=c["nk"], device="cuda")
         nk = nk.cuda()
         o_ref, l_ref = bw.attn_decode(q, kc, vc, nk, num_splits=c["S"])
         rc, o, lse = run_static(static_fn, q, kc, vc, nk, c["S"])
