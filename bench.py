@@ -44,11 +44,15 @@ HEADLINE = "prefill_causal_b4_h32_n4096_d128"
 # DRAM traffic of the dominant kernel from the committed ncu capture, per full launch, valid
 # only while the kernel source is the profiled one (checked by hash); otherwise reported null.
 PROFILED_TRAFFIC = {
-    "kernel_source": "exact_attention_flashattn_gb300/csrc/prefill_tc.cu",
-    "sha256": "346fc1a9951c6d460d15f610e48039785f8815bfc486fae2bf0adb84bebc97e2",
-    # (201.49 MB read + 45.85 MB written) at B=2 (profiles/prefill_tc_b2_h32_n4096_d128.md),
+    # the tcgen05 prefill kernel and the PTX wrappers it is built from, hashed in this order
+    "kernel_sources": [
+        "exact_attention_flashattn_gb300/csrc/prefill_tc.cu",
+        "exact_attention_flashattn_gb300/csrc/ptx.cuh",
+    ],
+    "sha256": "48c2ea511e2083267815557ccb330caffd33560353ab2dabdd5a46411db783e5",
+    # (201.52 MB read + 45.07 MB written) at B=2 (profiles/prefill_tc_b2_h32_n4096_d128.md),
     # scaled x2 to the B=4 launch: traffic grows with the number of (batch, head) units
-    "bytes_per_launch": 494670336,
+    "bytes_per_launch": 493168640,
 }
 METRIC = "prefill TFLOP/s and decode KV GB/s, 1×GB300, as fraction of roofline"
 L2_BYTES = 129 * 1024 * 1024
@@ -56,12 +60,14 @@ L2_BYTES = 129 * 1024 * 1024
 
 def profiled_traffic():
     import hashlib
-    p = os.path.join(ROOT, PROFILED_TRAFFIC["kernel_source"])
-    if PROFILED_TRAFFIC["sha256"] is None or not os.path.exists(p):
-        return None
-    with open(p, "rb") as f:
-        digest = hashlib.sha256(f.read()).hexdigest()
-    return PROFILED_TRAFFIC["bytes_per_launch"] if digest == PROFILED_TRAFFIC["sha256"] else None
+    h = hashlib.sha256()
+    for rel in PROFILED_TRAFFIC["kernel_sources"]:
+        p = os.path.join(ROOT, rel)
+        if not os.path.exists(p):
+            return None
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return PROFILED_TRAFFIC["bytes_per_launch"] if h.hexdigest() == PROFILED_TRAFFIC["sha256"] else None
 
 
 def load_peaks():

@@ -17,9 +17,9 @@
 //               S MMA freed them), then K_j, V_j tiles (128 keys x d, 128-byte swizzle) into a
 //               ring of shared-memory slots guarded by full/empty mbarriers; the ring runs on
 //               across items.
-//   warp 9      MMA issuer (one thread): S_w = Q_w K_j^T into TMEM (fp32, 128 columns per
-//               tile), then O_w += P_w V_j with P read from TMEM (bf16, aliased onto S_w) and V
-//               from shared memory. Issue order S0(j+1) after PV0(j), S1(j+1) after PV1(j): the
+//   warp 9      MMA issuer (the whole warp runs the loop, one elected lane issues): S_w =
+//               Q_w K_j^T into TMEM (fp32, 128 columns per tile), then O_w += P_w V_j with P read
+//               from TMEM (bf16, aliased onto S_w) and V from shared memory. Issue order S0(j+1) after PV0(j), S1(j+1) after PV1(j): the
 //               softmax of one tile overlaps tensor work on the other.
 //   warps 0-3,  softmax warpgroups, one per query tile, thread = row = TMEM lane: read the S
 //   4-7         row, apply the causal mask on diagonal tiles only ("Attention Computation in
@@ -48,7 +48,7 @@ constexpr int kMmaWarp = 9;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
 constexpr int kBandUnits = 16;             // (sequence, head) units per band of the item list
 constexpr int kItemSlots = 2;              // depth of the item queue from producer to consumers
-constexpr int kItemConsumers = 1 + 8;      // MMA thread + one lane of each softmax warp
+constexpr int kItemConsumers = 1 + 8;      // one lane of the MMA warp and of each softmax warp
 constexpr int kEarlyLoads = 2;             // K/V loads of an item issued before its Q
 
 template <int D>
@@ -319,7 +319,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this loop with identical values (waits are voted, so every lane takes
+    // the same path); the MMA and commit wrappers let one elected lane issue.
+    {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, D, 0, 1);
       // descriptor halves: K-major Q and K tiles (8-row groups 1024 B apart), MN-major V tiles
@@ -339,8 +341,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       int s_left = 0;     // S MMAs still to issue in the current item
       bool ok = true;
 
+      auto vote = [](bool x) { return __all_sync(0xffffffffu, x); };
       auto wait_load = [&](int i) -> bool {
-        const bool r = mbar_wait(&bar->kv_full[i % C::kStages], (i / C::kStages) & 1, tmo, abort);
+        const bool r =
+            __all_sync(0xffffffffu, mbar_wait(&bar->kv_full[i % C::kStages], (i / C::kStages) & 1, tmo, abort));
         tc_fence_after();
         return r;
       };
@@ -361,10 +365,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       };
 
       for (int k = 0; ok; ++k) {
-        const int idx = next_item(bar, k, true, tmo, abort, &ok);
+        const int idx = next_item(bar, k, false, tmo, abort, &ok);
+        ok = __all_sync(0xffffffffu, ok);
+        __syncwarp();
+        if (lane == 0 && ok) mbar_arrive(&bar->item_empty[k % kItemSlots]);
         if (!ok || idx < 0) break;
         const Item w = make_item<kWindow>(a, idx);
-        if (!(ok = mbar_wait(&bar->q_full, items & 1, tmo, abort))) break;
+        if (!(ok = vote(mbar_wait(&bar->q_full, items & 1, tmo, abort)))) break;
         tc_fence_after();
         ++items;
         const int nt = w.nt_all;
@@ -386,11 +393,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           // tile 0: P0 V_j, then S0 for the next K tile
           if (j >= a0 && j < e0) {
             // the first P.V of an item overwrites O: the previous item's epilogue must be done
-            if (j == a0 && ou0 > 0 && !(ok = mbar_wait(&bar->o_empty[0], (ou0 - 1) & 1, tmo, abort))) break;
-            if (!(ok = mbar_wait(&bar->p_full[0], pt0 & 1, tmo, abort))) break;
+            if (j == a0 && ou0 > 0 && !(ok = vote(mbar_wait(&bar->o_empty[0], (ou0 - 1) & 1, tmo, abort))))
+              break;
+            if (!(ok = vote(mbar_wait(&bar->p_full[0], pt0 & 1, tmo, abort)))) break;
             tc_fence_after();
             issue_pv_half(0, iv, 0, j > a0);
-            if (!(ok = mbar_wait(&bar->p2_full[0], pt0 & 1, tmo, abort))) break;
+            if (!(ok = vote(mbar_wait(&bar->p2_full[0], pt0 & 1, tmo, abort)))) break;
             ++pt0;
             tc_fence_after();
             issue_pv_half(0, iv, 1, true);
@@ -403,11 +411,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           if (j + 1 >= a0 && j + 1 < e0) issue_s(0, ik);
           // tile 1
           if (j >= a1 && j < e1) {
-            if (j == a1 && ou1 > 0 && !(ok = mbar_wait(&bar->o_empty[1], (ou1 - 1) & 1, tmo, abort))) break;
-            if (!(ok = mbar_wait(&bar->p_full[1], pt1 & 1, tmo, abort))) break;
+            if (j == a1 && ou1 > 0 && !(ok = vote(mbar_wait(&bar->o_empty[1], (ou1 - 1) & 1, tmo, abort))))
+              break;
+            if (!(ok = vote(mbar_wait(&bar->p_full[1], pt1 & 1, tmo, abort)))) break;
             tc_fence_after();
             issue_pv_half(1, iv, 0, j > a1);
-            if (!(ok = mbar_wait(&bar->p2_full[1], pt1 & 1, tmo, abort))) break;
+            if (!(ok = vote(mbar_wait(&bar->p2_full[1], pt1 & 1, tmo, abort)))) break;
             ++pt1;
             tc_fence_after();
             issue_pv_half(1, iv, 1, true);
@@ -423,8 +432,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         if (!ok) break;
         nload += 2 * nt;
       }
-      if (!ok) raise_timeout(abort, status);
-      // all MMAs issued by this thread complete before TMEM is released
+      if (!ok && lane == 0) raise_timeout(abort, status);
+      // all MMAs issued by this warp complete before TMEM is released
       const int no_abort = 0;
       umma_commit(&bar->mma_done);
       mbar_wait(&bar->mma_done, 0, tmo, &no_abort);

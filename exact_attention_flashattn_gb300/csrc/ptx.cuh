@@ -112,31 +112,15 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T-by-descriptor, kind::f16 (bf16 inputs, fp32 accumulate).
-__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                        uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem], kind::f16.
-__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                        uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Descriptor halves for sdesc_sw128: the low word carries the start address (>> 4) and the
-// leading-dimension offset; the high word the stride offset, version and swizzle mode. Within
-// one swizzle-aligned tile, moving the start address only changes the low word.
+// Shared-memory matrix descriptor (128-byte swizzle) in two halves: the low word carries the start
+// address (>> 4) and the leading-dimension offset; the high word the stride offset, version and
+// swizzle mode. Within one swizzle-aligned tile, moving the start address only changes the low word.
+//
+// The MMA and commit wrappers below are called by a whole converged warp with warp-uniform
+// operands: one lane, chosen by elect.sync (the same lane on every call of a full warp), issues
+// the instructions. Keeping the issuing warp converged keeps the descriptor arithmetic on the
+// warp-uniform datapath; issuing from a single-lane branch made every MMA about 100 cycles
+// apart, against 64 cycles of tensor work for an M128 N128 K16 MMA.
 __device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo_bytes) {
   return ((saddr & 0x3FFFFu) >> 4) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
 }
@@ -150,24 +134,24 @@ __device__ __forceinline__ uint32_t sdesc_hi(uint32_t sbo_bytes) {
 __device__ __forceinline__ void umma_ss_k128(uint32_t d_tmem, uint32_t alo, uint32_t ahi, uint32_t blo, uint32_t bhi,
                                              uint32_t idesc, uint32_t acc0) {
   asm volatile(
-      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 da, db;\n\t.reg .b32 xa, xb;\n\t"
+      "{\n\t.reg .pred p0, p1, pe;\n\t.reg .b64 da, db;\n\t.reg .b32 xa, xb;\n\telect.sync _|pe, 0xffffffff;\n\t"
       "setp.ne.b32 p0, %6, 0;\n\tsetp.eq.u32 p1, 0, 0;\n\t"
       "mov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p0;\n\t"
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p0;\n\t"
       "add.u32 xa, %1, 2;\n\tadd.u32 xb, %3, 2;\n\tmov.b64 da, {xa, %2};\n\tmov.b64 db, {xb, %4};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p1;\n\t"
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p1;\n\t"
       "add.u32 xa, %1, 4;\n\tadd.u32 xb, %3, 4;\n\tmov.b64 da, {xa, %2};\n\tmov.b64 db, {xb, %4};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p1;\n\t"
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p1;\n\t"
       "add.u32 xa, %1, 6;\n\tadd.u32 xb, %3, 6;\n\tmov.b64 da, {xa, %2};\n\tmov.b64 db, {xb, %4};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p1;\n\t"
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p1;\n\t"
       "add.u32 xa, %1, 1024;\n\tadd.u32 xb, %3, 1024;\n\tmov.b64 da, {xa, %2};\n\tmov.b64 db, {xb, %4};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p1;\n\t"
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p1;\n\t"
       "add.u32 xa, %1, 1026;\n\tadd.u32 xb, %3, 1026;\n\tmov.b64 da, {xa, %2};\n\tmov.b64 db, {xb, %4};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p1;\n\t"
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p1;\n\t"
       "add.u32 xa, %1, 1028;\n\tadd.u32 xb, %3, 1028;\n\tmov.b64 da, {xa, %2};\n\tmov.b64 db, {xb, %4};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p1;\n\t"
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p1;\n\t"
       "add.u32 xa, %1, 1030;\n\tadd.u32 xb, %3, 1030;\n\tmov.b64 da, {xa, %2};\n\tmov.b64 db, {xb, %4};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p1;\n\t}\n" ::"r"(d_tmem),
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p1;\n\t}\n" ::"r"(d_tmem),
       "r"(alo), "r"(ahi), "r"(blo), "r"(bhi), "r"(idesc), "r"(acc0)
       : "memory");
 }
@@ -176,16 +160,16 @@ __device__ __forceinline__ void umma_ss_k128(uint32_t d_tmem, uint32_t alo, uint
 __device__ __forceinline__ void umma_ss_k64(uint32_t d_tmem, uint32_t alo, uint32_t ahi, uint32_t blo, uint32_t bhi,
                                             uint32_t idesc, uint32_t acc0) {
   asm volatile(
-      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 da, db;\n\t.reg .b32 xa, xb;\n\t"
+      "{\n\t.reg .pred p0, p1, pe;\n\t.reg .b64 da, db;\n\t.reg .b32 xa, xb;\n\telect.sync _|pe, 0xffffffff;\n\t"
       "setp.ne.b32 p0, %6, 0;\n\tsetp.eq.u32 p1, 0, 0;\n\t"
       "mov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p0;\n\t"
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p0;\n\t"
       "add.u32 xa, %1, 2;\n\tadd.u32 xb, %3, 2;\n\tmov.b64 da, {xa, %2};\n\tmov.b64 db, {xb, %4};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p1;\n\t"
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p1;\n\t"
       "add.u32 xa, %1, 4;\n\tadd.u32 xb, %3, 4;\n\tmov.b64 da, {xa, %2};\n\tmov.b64 db, {xb, %4};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p1;\n\t"
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p1;\n\t"
       "add.u32 xa, %1, 6;\n\tadd.u32 xb, %3, 6;\n\tmov.b64 da, {xa, %2};\n\tmov.b64 db, {xb, %4};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p1;\n\t}\n" ::"r"(d_tmem),
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p1;\n\t}\n" ::"r"(d_tmem),
       "r"(alo), "r"(ahi), "r"(blo), "r"(bhi), "r"(idesc), "r"(acc0)
       : "memory");
 }
@@ -195,24 +179,24 @@ __device__ __forceinline__ void umma_ss_k64(uint32_t d_tmem, uint32_t alo, uint3
 __device__ __forceinline__ void umma_ts_k128(uint32_t d_tmem, uint32_t a_tmem, uint32_t blo, uint32_t bhi,
                                              uint32_t idesc, uint32_t acc0) {
   asm volatile(
-      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 db;\n\t.reg .b32 ta, xb;\n\t"
+      "{\n\t.reg .pred p0, p1, pe;\n\t.reg .b64 db;\n\t.reg .b32 ta, xb;\n\telect.sync _|pe, 0xffffffff;\n\t"
       "setp.ne.b32 p0, %5, 0;\n\tsetp.eq.u32 p1, 0, 0;\n\t"
       "mov.b64 db, {%2, %3};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p0;\n\t"
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p0;\n\t"
       "add.u32 ta, %1, 8;\n\tadd.u32 xb, %2, 128;\n\tmov.b64 db, {xb, %3};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
       "add.u32 ta, %1, 16;\n\tadd.u32 xb, %2, 256;\n\tmov.b64 db, {xb, %3};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
       "add.u32 ta, %1, 24;\n\tadd.u32 xb, %2, 384;\n\tmov.b64 db, {xb, %3};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
       "add.u32 ta, %1, 32;\n\tadd.u32 xb, %2, 512;\n\tmov.b64 db, {xb, %3};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
       "add.u32 ta, %1, 40;\n\tadd.u32 xb, %2, 640;\n\tmov.b64 db, {xb, %3};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
       "add.u32 ta, %1, 48;\n\tadd.u32 xb, %2, 768;\n\tmov.b64 db, {xb, %3};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
       "add.u32 ta, %1, 56;\n\tadd.u32 xb, %2, 896;\n\tmov.b64 db, {xb, %3};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t}\n" ::"r"(d_tmem),
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t}\n" ::"r"(d_tmem),
       "r"(a_tmem), "r"(blo), "r"(bhi), "r"(idesc), "r"(acc0)
       : "memory");
 }
@@ -222,16 +206,16 @@ __device__ __forceinline__ void umma_ts_k128(uint32_t d_tmem, uint32_t a_tmem, u
 __device__ __forceinline__ void umma_ts_k64(uint32_t d_tmem, uint32_t a_tmem, uint32_t blo, uint32_t bhi,
                                             uint32_t idesc, uint32_t acc0) {
   asm volatile(
-      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 db;\n\t.reg .b32 ta, xb;\n\t"
+      "{\n\t.reg .pred p0, p1, pe;\n\t.reg .b64 db;\n\t.reg .b32 ta, xb;\n\telect.sync _|pe, 0xffffffff;\n\t"
       "setp.ne.b32 p0, %5, 0;\n\tsetp.eq.u32 p1, 0, 0;\n\t"
       "mov.b64 db, {%2, %3};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p0;\n\t"
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p0;\n\t"
       "add.u32 ta, %1, 8;\n\tadd.u32 xb, %2, 128;\n\tmov.b64 db, {xb, %3};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
       "add.u32 ta, %1, 16;\n\tadd.u32 xb, %2, 256;\n\tmov.b64 db, {xb, %3};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
       "add.u32 ta, %1, 24;\n\tadd.u32 xb, %2, 384;\n\tmov.b64 db, {xb, %3};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t}\n" ::"r"(d_tmem),
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t}\n" ::"r"(d_tmem),
       "r"(a_tmem), "r"(blo), "r"(bhi), "r"(idesc), "r"(acc0)
       : "memory");
 }
@@ -262,9 +246,10 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
       : "memory");
 }
 
-// Arrive once on `bar` when every tcgen05 async op issued so far by this thread completes.
+// Arrive once on `bar` when every tcgen05 async op issued so far by the warp's elected lane completes.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+  asm volatile("{\n\t.reg .pred pe;\n\telect.sync _|pe, 0xffffffff;\n\t"
+               "@pe tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}\n" ::"r"(
                    smem_u32(bar))
                : "memory");
 }
