@@ -17,10 +17,12 @@
 //               S MMA freed them), then K_j, V_j tiles (128 keys x d, 128-byte swizzle) into a
 //               ring of shared-memory slots guarded by full/empty mbarriers; the ring runs on
 //               across items.
-//   warp 9      MMA issuer (the whole warp runs the loop, one elected lane issues): S_w =
-//               Q_w K_j^T into TMEM (fp32, 128 columns per tile), then O_w += P_w V_j with P read
-//               from TMEM (bf16, aliased onto S_w) and V from shared memory. Issue order S0(j+1) after PV0(j), S1(j+1) after PV1(j): the
-//               softmax of one tile overlaps tensor work on the other.
+//   warp 9      MMA issuer: S_w = Q_w K_j^T into TMEM (fp32, 128 columns per tile), then
+//               O_w += P_w V_j with P read from TMEM (bf16, aliased onto S_w) and V from shared
+//               memory. Issue order S0(j+1) after PV0(j), S1(j+1) after PV1(j): the softmax of
+//               one tile overlaps tensor work on the other. Warps 8 and 9 each run their loop
+//               converged (waits voted across the warp) and one elected lane issues each copy,
+//               MMA and commit, which keeps their address arithmetic warp-uniform.
 //   warps 0-3,  softmax warpgroups, one per query tile, thread = row = TMEM lane: read the S
 //   4-7         row, apply the causal mask on diagonal tiles only ("Attention Computation in
 //               Practice", Masking variants: skip / full / diagonal), update m and l in
@@ -66,8 +68,7 @@ struct Cfg {
 struct Barriers {
   uint64_t q_full, q_empty;
   uint64_t s_full[2];
-  uint64_t p_full[2];   // first half of P (keys 0..63) stored
-  uint64_t p2_full[2];  // second half of P (keys 64..127) stored
+  uint64_t p_full[2];  // P of the current K tile stored in TMEM
   uint64_t o_full[2];
   uint64_t o_empty[2];
   uint64_t mma_done;
@@ -230,7 +231,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar->s_full[i], 1);
       mbar_init(&bar->p_full[i], kBM);
-      mbar_init(&bar->p2_full[i], kBM);
       mbar_init(&bar->o_full[i], 1);
       mbar_init(&bar->o_empty[i], kBM);
     }
@@ -259,10 +259,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      prefetch_tmap(&a.tm_q);
-      prefetch_tmap(&a.tm_k);
-      prefetch_tmap(&a.tm_v);
+    // Like the MMA warp, the whole warp runs the loop with identical values; lane 0 takes items
+    // from the counter and publishes them, one elected lane issues each copy.
+    {
+      if (lane == 0) {
+        prefetch_tmap(&a.tm_q);
+        prefetch_tmap(&a.tm_k);
+        prefetch_tmap(&a.tm_v);
+      }
+      auto vote = [](bool x) { return __all_sync(0xffffffffu, x); };
       int nload = 0;  // K/V tiles issued by this CTA, over all items
       int items = 0;  // active items started by this CTA
       bool ok = true;
@@ -271,21 +276,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         int idx;
         Item w;
         do {
-          idx = static_cast<int>(atomicAdd(&sched[0], 1u));
+          int got = 0;
+          if (lane == 0) got = static_cast<int>(atomicAdd(&sched[0], 1u));
+          idx = __shfl_sync(0xffffffffu, got, 0);
           if (idx < total_items) w = make_item<kWindow>(a, idx);
         } while (idx < total_items && !w.active);
         if (idx >= total_items) idx = -1;
         const int qs = k % kItemSlots;
-        if (k >= kItemSlots && !(ok = mbar_wait(&bar->item_empty[qs], ((k / kItemSlots) - 1) & 1, tmo, abort))) break;
-        bar->item_q[qs] = idx;
-        mbar_arrive(&bar->item_full[qs]);
+        if (k >= kItemSlots && !(ok = vote(mbar_wait(&bar->item_empty[qs], ((k / kItemSlots) - 1) & 1, tmo, abort))))
+          break;
+        if (lane == 0) {
+          bar->item_q[qs] = idx;
+          mbar_arrive(&bar->item_full[qs]);
+        }
         if (idx < 0) break;
         // K/V loads need only ring slots: the first ones go out before the Q wait, whose
         // buffers are free only once every S MMA of the previous item has completed
         const int n_early = min(2 * w.nt_all, kEarlyLoads);
         for (int i = 0; i < 2 * w.nt_all; ++i, ++nload) {
           if (i == n_early) {
-            if (items > 0 && !(ok = mbar_wait(&bar->q_empty, (items - 1) & 1, tmo, abort))) break;
+            if (items > 0 && !(ok = vote(mbar_wait(&bar->q_empty, (items - 1) & 1, tmo, abort)))) break;
             mbar_arrive_expect_tx(&bar->q_full, 2 * C::kQBytes);
             for (int t = 0; t < 2; ++t)
               for (int hf = 0; hf < C::kHalves; ++hf)
@@ -294,14 +304,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           }
           const int slot = nload % C::kStages;
           const int round = nload / C::kStages;
-          if (round > 0 && !(ok = mbar_wait(&bar->kv_empty[slot], (round - 1) & 1, tmo, abort))) break;
+          if (round > 0 && !(ok = vote(mbar_wait(&bar->kv_empty[slot], (round - 1) & 1, tmo, abort)))) break;
           mbar_arrive_expect_tx(&bar->kv_full[slot], C::kTileBytes);
           for (int hf = 0; hf < C::kHalves; ++hf)
             tma_tile((i & 1) ? &a.tm_v : &a.tm_k, w, sRing + slot * C::kTileBytes + hf * (kBN * 128),
                      &bar->kv_full[slot], hf, (w.jmin + (i >> 1)) * kBN, false);
         }
         if (ok && n_early == 2 * w.nt_all) {  // items with no more than kEarlyLoads loads
-          if (items > 0 && !(ok = mbar_wait(&bar->q_empty, (items - 1) & 1, tmo, abort))) break;
+          if (items > 0 && !(ok = vote(mbar_wait(&bar->q_empty, (items - 1) & 1, tmo, abort)))) break;
           mbar_arrive_expect_tx(&bar->q_full, 2 * C::kQBytes);
           for (int t = 0; t < 2; ++t)
             for (int hf = 0; hf < C::kHalves; ++hf)
@@ -309,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           ++items;
         }
       }
-      if (!ok) raise_timeout(abort, status);
+      if (!ok && lane == 0) raise_timeout(abort, status);
       // every copy this CTA issued must have landed before the CTA may exit (bounded, and
       // not cut short by the abort flag)
       const int no_abort = 0;
@@ -357,11 +367,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         umma_commit(&bar->s_full[t]);
         if (--s_left == 0) umma_commit(&bar->q_empty);  // last read of the Q tiles issued
       };
-      // O_t += P_t V with V in the load slot of load i, one half of the keys at a time: the
-      // softmax releases P in two halves so that the first half's MMAs overlap the rest of it
-      auto issue_pv_half = [&](int t, int i, int half, bool accumulate) {
-        umma_ts_k64(t ? tO1 : tO0, (t ? tS1 : tS0) + half * 32, v_lo + (i % C::kStages) * slot_step + half * 512, hi,
-                    idesc_pv, accumulate ? 1u : 0u);
+      // O_t += P_t V with V in the load slot of load i: 8 MMAs of K = 16 over the tile's keys
+      auto issue_pv = [&](int t, int i, bool accumulate) {
+        umma_ts_k128(t ? tO1 : tO0, t ? tS1 : tS0, v_lo + (i % C::kStages) * slot_step, hi, idesc_pv,
+                     accumulate ? 1u : 0u);
       };
 
       for (int k = 0; ok; ++k) {
@@ -396,12 +405,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             if (j == a0 && ou0 > 0 && !(ok = vote(mbar_wait(&bar->o_empty[0], (ou0 - 1) & 1, tmo, abort))))
               break;
             if (!(ok = vote(mbar_wait(&bar->p_full[0], pt0 & 1, tmo, abort)))) break;
-            tc_fence_after();
-            issue_pv_half(0, iv, 0, j > a0);
-            if (!(ok = vote(mbar_wait(&bar->p2_full[0], pt0 & 1, tmo, abort)))) break;
             ++pt0;
             tc_fence_after();
-            issue_pv_half(0, iv, 1, true);
+            issue_pv(0, iv, j > a0);
             if (j == e0 - 1) {
               umma_commit(&bar->o_full[0]);
               ++ou0;
@@ -414,12 +420,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             if (j == a1 && ou1 > 0 && !(ok = vote(mbar_wait(&bar->o_empty[1], (ou1 - 1) & 1, tmo, abort))))
               break;
             if (!(ok = vote(mbar_wait(&bar->p_full[1], pt1 & 1, tmo, abort)))) break;
-            tc_fence_after();
-            issue_pv_half(1, iv, 0, j > a1);
-            if (!(ok = vote(mbar_wait(&bar->p2_full[1], pt1 & 1, tmo, abort)))) break;
             ++pt1;
             tc_fence_after();
-            issue_pv_half(1, iv, 1, true);
+            issue_pv(1, iv, j > a1);
             if (j == e1 - 1) {
               umma_commit(&bar->o_full[1]);
               ++ou1;
@@ -546,15 +549,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             tmem_st32(tO + c * 32, ov);
           }
         }
-        // keys 0..63 of P are in TMEM: the MMA warp may start on them
+        exp_quarter(s2, 32);
+        exp_quarter(s3, 48);
+        // all of P is in TMEM: the MMA warp may start P.V
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bar->p_full[t]);
-        exp_quarter(s2, 32);
-        exp_quarter(s3, 48);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&bar->p2_full[t]);
         l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       }
       if (!ok) break;
@@ -663,7 +663,8 @@ cudaError_t launch_d(const TcFwdArgs& a, unsigned int* status, unsigned int* sch
 
 cudaError_t launch_prefill_tc(const TcFwdArgs& a, unsigned int* status, unsigned int* sched, cudaStream_t stream) {
   const bool window = a.causal && a.window > 0;
-  if (a.d == 64) return window ? launch_d<64, true>(a, status, sched, stream) : launch_d<64, false>(a, status, sched, stream);
+  if (a.d == 64)
+    return window ? launch_d<64, true>(a, status, sched, stream) : launch_d<64, false>(a, status, sched, stream);
   return window ? launch_d<128, true>(a, status, sched, stream) : launch_d<128, false>(a, status, sched, stream);
 }
 

@@ -36,8 +36,10 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Called by a whole converged warp: one elected lane arrives (with the expected byte count).
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+  asm volatile("{\n\t.reg .pred pe;\n\telect.sync _|pe, 0xffffffff;\n\t"
+               "@pe mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;\n\t}\n" ::"r"(smem_u32(bar)),
                "r"(bytes)
                : "memory");
 }
@@ -83,11 +85,13 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
 }
 
 // 3-D tiled bulk tensor load global -> shared, completion counted in bytes on `bar`.
+// Called by a whole converged warp: one elected lane issues the copy.
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
                                             int c2) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
-      "[%2];" ::"r"(smem_u32(dst)),
+      "{\n\t.reg .pred pe;\n\telect.sync _|pe, 0xffffffff;\n\t"
+      "@pe cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
+      "[%2];\n\t}\n" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
@@ -196,25 +200,6 @@ __device__ __forceinline__ void umma_ts_k128(uint32_t d_tmem, uint32_t a_tmem, u
       "add.u32 ta, %1, 48;\n\tadd.u32 xb, %2, 768;\n\tmov.b64 db, {xb, %3};\n\t"
       "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
       "add.u32 ta, %1, 56;\n\tadd.u32 xb, %2, 896;\n\tmov.b64 db, {xb, %3};\n\t"
-      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "r"(blo), "r"(bhi), "r"(idesc), "r"(acc0)
-      : "memory");
-}
-
-// Four K=16 steps of D[tmem] (+)= A[tmem] B[smem] (one half of a 128-key P.V): A advances 8
-// columns per step, B (MN-major, 128-byte rows) 2048 B per step. acc0 = 0 overwrites D.
-__device__ __forceinline__ void umma_ts_k64(uint32_t d_tmem, uint32_t a_tmem, uint32_t blo, uint32_t bhi,
-                                            uint32_t idesc, uint32_t acc0) {
-  asm volatile(
-      "{\n\t.reg .pred p0, p1, pe;\n\t.reg .b64 db;\n\t.reg .b32 ta, xb;\n\telect.sync _|pe, 0xffffffff;\n\t"
-      "setp.ne.b32 p0, %5, 0;\n\tsetp.eq.u32 p1, 0, 0;\n\t"
-      "mov.b64 db, {%2, %3};\n\t"
-      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p0;\n\t"
-      "add.u32 ta, %1, 8;\n\tadd.u32 xb, %2, 128;\n\tmov.b64 db, {xb, %3};\n\t"
-      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
-      "add.u32 ta, %1, 16;\n\tadd.u32 xb, %2, 256;\n\tmov.b64 db, {xb, %3};\n\t"
-      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
-      "add.u32 ta, %1, 24;\n\tadd.u32 xb, %2, 384;\n\tmov.b64 db, {xb, %3};\n\t"
       "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t}\n" ::"r"(d_tmem),
       "r"(a_tmem), "r"(blo), "r"(bhi), "r"(idesc), "r"(acc0)
       : "memory");
