@@ -540,9 +540,8 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
     // being computed. Each thread reads back only what it copied, so no barrier is needed.
     const uint32_t pipe = smem_u32(dsm) + static_cast<uint32_t>((warp * kFp8Chunks * 32 + lane) * 16);
     auto slot = [&](int st, int c) { return pipe + st * kFp8StageBytes + c * 32 * 16; };
-    auto issue = [&](int kb, int st) {
+    auto issue = [&](int kb, int64_t so, int st) {
       if (kb < kend) {
-        const int64_t so = step_offset<kPaged>(a, seq, kb);
         // K: codes of chunks t and t + 4 of rows kb + nt*8 + gr; V: chunk gr of 4 key rows
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
@@ -571,15 +570,21 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
     };
     constexpr int kStride = kWarps * kKeysPerStep;
     int kb_next = kstart + warp * kKeysPerStep;
+    // paged: the block-table entry of the next step to issue is read one step before its copies
+    int64_t so_next = (kb_next < kend) ? step_offset<kPaged>(a, seq, kb_next) : 0;
+    auto advance = [&]() {
+      kb_next += kStride;
+      if (kb_next < kend) so_next = step_offset<kPaged>(a, seq, kb_next);
+    };
 #pragma unroll
     for (int st = 0; st < kFp8Stages - 1; ++st) {
-      issue(kb_next, st);
-      kb_next += kStride;
+      issue(kb_next, so_next, st);
+      advance();
     }
     int st = 0;
     for (int kb = kstart + warp * kKeysPerStep; kb < kend; kb += kStride) {
-      issue(kb_next, st == 0 ? kFp8Stages - 1 : st - 1);  // the slot read one step ago
-      kb_next += kStride;
+      issue(kb_next, so_next, st == 0 ? kFp8Stages - 1 : st - 1);  // the slot read one step ago
+      advance();
       cp_async_wait<kFp8Stages - 1>();  // this step's group has landed
       uint4 kk[2][2], va[4];
 #pragma unroll
