@@ -49,10 +49,10 @@ PROFILED_TRAFFIC = {
         "exact_attention_flashattn_gb300/csrc/prefill_tc.cu",
         "exact_attention_flashattn_gb300/csrc/ptx.cuh",
     ],
-    "sha256": "edcb02d077753245226adb206425652971308df35e13bf6c8ed2f0f3d4f82f34",
-    # (201.53 MB read + 45.35 MB written) at B=2 (profiles/prefill_tc_b2_h32_n4096_d128.md),
+    "sha256": "e1c2470662d100a5a38a328385bb4b7a302bb6a0730b752556d27ce7016b732e",
+    # (201.59 MB read + 45.47 MB written) at B=2 (profiles/prefill_tc_b2_h32_n4096_d128.md),
     # scaled x2 to the B=4 launch: traffic grows with the number of (batch, head) units
-    "bytes_per_launch": 493755392,
+    "bytes_per_launch": 494109696,
 }
 METRIC = "prefill TFLOP/s and decode KV GB/s, 1×GB300, as fraction of roofline"
 L2_BYTES = 129 * 1024 * 1024

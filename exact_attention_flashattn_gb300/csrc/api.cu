@@ -5,6 +5,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -121,6 +122,16 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int d, int64_t dim1, int6
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// Units per band of the prefill item list: as many (sequence, head) units as keep their K and V
+// (one KV head serves g consecutive query heads) within 16 MB, between 16 and 64. Wider bands
+// help short sequences, whose items are many and short (32 units: +5.6 % at 1024 keys, d = 128);
+// from 2048 keys on (d = 128) the band stays at 16, where wider ones measured 1-2 % slower.
+int band_units_for(int64_t nk, int d, int g) {
+  const int64_t unit_bytes = std::max<int64_t>(1, nk * d * 4 / std::max(g, 1));
+  const int64_t b = (static_cast<int64_t>(16) << 20) / unit_bytes;
+  return static_cast<int>(std::min<int64_t>(64, std::max<int64_t>(16, b)));
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -275,6 +286,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   a.num_seqs = B;
   a.small_rows_limit = 0;
   a.max_pairs = (Nq + 255) / 256;
+  a.band_units = band_units_for(Nk, d, Hq / Hkv);
   a.window = window;
   a.scale_log2 = sl2;
   a.timeout_ns = g_timeout_ns.load();
@@ -533,6 +545,7 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
     a.num_seqs = num_seqs;
     a.small_rows_limit = kSmallRowsLimit;
     a.max_pairs = (max_seqlen_q + 255) / 256;
+    a.band_units = band_units_for(max_seqlen_k, d, g);
     a.window = window;
     a.scale_log2 = sl2;
     a.timeout_ns = g_timeout_ns.load();

@@ -97,6 +97,7 @@ struct TcFwdArgs {
   int small_rows_limit;  // varlen: sequences with n_q * g <= this are skipped here
   int max_pairs;         // grid.x: pairs of 128-row query tiles per (sequence, head)
   int window;            // > 0: sliding window of that many keys ending at the causal limit
+  int band_units;        // (sequence, head) units per band of the item list (at least 1)
   float scale_log2;
   uint64_t timeout_ns;
 };

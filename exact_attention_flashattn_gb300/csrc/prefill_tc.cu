@@ -8,10 +8,10 @@
 //
 // GB300 mapping. A work item is two 128-row query tiles of one (sequence, head). The kernel is
 // persistent: one CTA per SM takes items from a list in order through an atomic counter
-// (dynamic, so long and short items balance). The list is cut into bands of 16 (sequence,
-// head) units and, inside a band, ordered longest first: the items in flight at any time
-// then belong to one or two bands, whose K/V (a few tens of MB) stay in L2 while every query
-// tile of those heads reads them. 10 warps per CTA:
+// (dynamic, so long and short items balance). The list is cut into bands of (sequence, head)
+// units and, inside a band, ordered longest first: the items in flight at any time then belong
+// to one or two bands, whose K/V stay in L2 while every query tile of those heads reads them.
+// The host sizes the band from the K/V bytes of a unit (16 to 64 units). 10 warps per CTA:
 //   warp 8      TMA producer: takes the next item and hands it to the other roles through a
 //               small shared-memory queue; per item, both Q tiles once (after the previous item's last
 //               S MMA freed them), then K_j, V_j tiles (128 keys x d, 128-byte swizzle) into a
@@ -48,7 +48,6 @@ constexpr int kThreads = 320;
 constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
-constexpr int kBandUnits = 16;             // (sequence, head) units per band of the item list
 constexpr int kItemSlots = 2;              // depth of the item queue from producer to consumers
 constexpr int kItemConsumers = 1 + 8;      // one lane of the MMA warp and of each softmax warp
 constexpr int kEarlyLoads = 2;             // K/V loads of an item issued before its Q
@@ -97,19 +96,20 @@ struct Item {
   int64_t out_row_stride;
 };
 
-// Item numbering: bands of kBandUnits (sequence, head) units; inside a band all units of the
+// Item numbering: bands of a.band_units (sequence, head) units; inside a band all units of the
 // last query-tile pair come first, then those of the pair before, and so on (with a causal
 // mask later pairs see more keys).
 template <bool kWindow>
 __device__ __forceinline__ Item make_item(const TcFwdArgs& a, int idx) {
   Item w;
   const int units = a.num_seqs * a.Hq;
-  const int per_band = kBandUnits * a.max_pairs;
+  const int bu = a.band_units;
+  const int per_band = bu * a.max_pairs;
   const int band = idx / per_band;
   const int within = idx % per_band;
-  const int band_units = min(kBandUnits, units - band * kBandUnits);
+  const int band_units = min(bu, units - band * bu);
   const int pair = a.max_pairs - 1 - within / band_units;
-  const int unit = band * kBandUnits + within % band_units;
+  const int unit = band * bu + within % band_units;
   const int s = unit / a.Hq;
   const int h = unit % a.Hq;
   const int g = a.Hq / a.Hkv;
