@@ -50,6 +50,7 @@ struct SplitKArgs {
   int causal;         // varlen: causal aligned to each sequence's end
   int window;         // varlen: > 0 adds a sliding window of that many keys
   int small_rows_limit;  // varlen: a sequence takes this path iff n_q * g <= this
+  int min_chunk;         // varlen: a split takes at least this many keys (a multiple of 16; 0: none)
   size_t ws_o_offset;    // splitk_o_offset(num_seqs * Hkv, num_splits, rows_max)
   float scale_log2;
   // paged KV cache (decode only) when block_table is non-null: k, v are [num_pages, page_size,

@@ -207,9 +207,10 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int t = lane & 3, gr = lane >> 2;
 
-  // Key slice of this split: whole 16-key steps.
+  // Key slice of this split: whole 16-key steps, at least min_chunk keys (varlen: the splits of a
+  // short sequence past its last key are empty partials)
   const int per = (u.nk + a.num_splits - 1) / a.num_splits;
-  const int chunk = (per + kKeysPerStep - 1) / kKeysPerStep * kKeysPerStep;
+  const int chunk = max((per + kKeysPerStep - 1) / kKeysPerStep * kKeysPerStep, a.min_chunk);
   const int kbeg = min(u.nk, split * chunk);
   const int kend = min(u.nk, kbeg + chunk);
 
