@@ -49,10 +49,10 @@ PROFILED_TRAFFIC = {
         "exact_attention_flashattn_gb300/csrc/prefill_tc.cu",
         "exact_attention_flashattn_gb300/csrc/ptx.cuh",
     ],
-    "sha256": "e1c2470662d100a5a38a328385bb4b7a302bb6a0730b752556d27ce7016b732e",
-    # (201.59 MB read + 45.47 MB written) at B=2 (profiles/prefill_tc_b2_h32_n4096_d128.md),
+    "sha256": "c4ff20d4fed3c25cc0dd97c0bc039b0b5451149a0004d2f6c2f5fda2c7e7e230",
+    # (201.54 MB read + 45.60 MB written) at B=2 (profiles/prefill_tc_b2_h32_n4096_d128.md),
     # scaled x2 to the B=4 launch: traffic grows with the number of (batch, head) units
-    "bytes_per_launch": 494109696,
+    "bytes_per_launch": 494269440,
 }
 METRIC = "prefill TFLOP/s and decode KV GB/s, 1×GB300, as fraction of roofline"
 L2_BYTES = 129 * 1024 * 1024

@@ -485,14 +485,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         tmem_reg_fence(s2);
         tmem_reg_fence(s3);
         const int kv0 = (jfirst + j) * kBN;
-        if (kv0 + kBN > lim || (kWindow && kv0 < lo)) {
-          const uint32_t ninf = __float_as_uint(-INFINITY);
+        // masks: keys at or past the causal limit (diagonal tiles), and with a window keys below
+        // its start (window-edge tiles); each kind of tile tests its own bound only
+        const uint32_t ninf = __float_as_uint(-INFINITY);
+        if (kv0 + kBN > lim) {
+          const int n = lim - kv0;  // keys of this tile the row sees from below
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            if (kv0 + e >= lim || (kWindow && kv0 + e < lo)) s0[e] = ninf;
-            if (kv0 + 32 + e >= lim || (kWindow && kv0 + 32 + e < lo)) s1[e] = ninf;
-            if (kv0 + 64 + e >= lim || (kWindow && kv0 + 64 + e < lo)) s2[e] = ninf;
-            if (kv0 + 96 + e >= lim || (kWindow && kv0 + 96 + e < lo)) s3[e] = ninf;
+            if (e >= n) s0[e] = ninf;
+            if (32 + e >= n) s1[e] = ninf;
+            if (64 + e >= n) s2[e] = ninf;
+            if (96 + e >= n) s3[e] = ninf;
+          }
+        }
+        if (kWindow && kv0 < lo) {
+          const int n = lo - kv0;  // keys of this tile below the window
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            if (e < n) s0[e] = ninf;
+            if (32 + e < n) s1[e] = ninf;
+            if (64 + e < n) s2[e] = ninf;
+            if (96 + e < n) s3[e] = ninf;
           }
         }
         // row max: four chains of 3-input max (a single 128-long chain is pure latency)
