@@ -7,10 +7,15 @@ if the library is missing or a call fails, a ``RuntimeError`` is raised.
 
 Calls (see ``include/bwattn.h`` for the full contract):
 
-* ``attn_fwd(q, k, v, causal, scale)``: prefill / cross attention, q [B, Hq, Nq, d],
-  k, v [B, Hkv, Nk, d]; bf16 (tcgen05 kernel) or fp32 (fp32 FMA kernel).
+* ``attn_fwd(q, k, v, causal, scale, window=0)``: prefill / cross attention, q [B, Hq, Nq, d],
+  k, v [B, Hkv, Nk, d]; bf16 (tcgen05 kernel) or fp32 (fp32 FMA kernel); ``window`` > 0 adds a
+  causal sliding window.
+* ``attn_fwd_host(...)``: the same prefill from host tensors, with the copies overlapping the
+  kernels (workspace from ``fwd_host_workspace_size``).
 * ``attn_decode(q, kcache, vcache, nk, num_splits)``: single-query split-K decode,
-  q [B, Hq, d], caches [B, Hkv, cap, d] bf16, nk [B] int32 on the device.
+  q [B, Hq, d], caches [B, Hkv, cap, d] bf16, nk [B] int32 on the device;
+  ``attn_decode_paged`` over a paged cache and a block table; ``attn_decode_fp8`` /
+  ``attn_decode_paged_fp8`` over E4M3 caches with per-channel scales.
 * ``attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, causal)``:
   packed sequences, q [total_q, Hq, d], k, v [total_k, Hkv, d] bf16.
 """
@@ -24,9 +29,10 @@ import threading
 import torch
 
 __all__ = [
-    "attn_fwd", "attn_decode", "attn_decode_paged", "attn_varlen", "decode_workspace_size", "varlen_workspace_size",
+    "attn_fwd", "attn_fwd_host", "attn_decode", "attn_decode_paged", "attn_decode_fp8", "attn_decode_paged_fp8",
+    "attn_varlen", "fwd_host_workspace_size", "decode_workspace_size", "varlen_workspace_size",
     "get_status", "clear_status", "set_wait_timeout_ns", "test_wait_timeout", "launch_count", "lib",
-    "BwattnError", "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_TIMEOUT",
+    "status_string", "BwattnError", "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_TIMEOUT",
 ]
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
