@@ -128,6 +128,16 @@ def test_bf16_prefill_mask_is_exact_and_deterministic():
     assert torch.equal(o1[:, :, :256], o3[:, :, :256]) and torch.equal(l1[:, :, :256], l3[:, :, :256])
 
 
+def test_prefill_several_item_bands():
+    # 72 (sequence, head) units at 1024 keys: the item list is cut into bands of 32 units (the
+    # last one ragged, 8 units); every unit must be computed exactly once, whatever its band
+    q, k, v = wl.prefill_inputs(3, 24, 24, 1024, 1024, 128, torch.bfloat16, seed=61)
+    o_ref, lse_ref = oracle.attention(f64(q), f64(k), f64(v), True, method="tiled", block=128)
+    o, lse = bw.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True)
+    torch.cuda.synchronize()
+    check_bf16(o, o_ref, lse, lse_ref, what="several item bands")
+
+
 def test_prefill_workload_full_size_sampled_rows():
     x = wl.make("prefill_causal_b4_h32_n4096_d128", device="cuda")
     w = x["w"]
@@ -609,6 +619,19 @@ def test_varlen_with_empty_and_single_token_sequences():
     o, lse = bw.attn_varlen(q.cuda(), k.cuda(), v.cuda(), cq.cuda(), ck.cuda(), max(nq), max(nk), causal=True)
     torch.cuda.synchronize()
     check_bf16(o, o_ref, lse, lse_ref, what="varlen edge")
+
+
+def test_varlen_short_queries_around_the_minimum_split():
+    # the longest sequence asks for 5 splits, and every split takes at least 2048 keys: the
+    # short-query sequences (1 .. 4100 keys) leave their later splits empty, and the 2047 / 2048 /
+    # 2049-key ones sit on a split boundary
+    nq = [1, 4, 8, 1, 4, 8, 2, 300]
+    nk = [1, 17, 2047, 2048, 2049, 4100, 700, 10000]
+    q, k, v, cq, ck = wl.varlen_inputs(nq, nk, 8, 2, 128, torch.bfloat16, seed=83)
+    o_ref, lse_ref = oracle.varlen(f64(q), f64(k), f64(v), cq.numpy(), ck.numpy(), True, method="tiled", block=128)
+    o, lse = bw.attn_varlen(q.cuda(), k.cuda(), v.cuda(), cq.cuda(), ck.cuda(), max(nq), max(nk), causal=True)
+    torch.cuda.synchronize()
+    check_bf16(o, o_ref, lse, lse_ref, what="varlen minimum split")
 
 
 def test_decode_all_sequences_empty():
