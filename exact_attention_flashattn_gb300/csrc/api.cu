@@ -378,7 +378,7 @@ int decode_contig(const void* q, const void* kcache, const void* vcache, const f
   if (Hq % Hkv != 0 || !good_scale(scale) || num_splits < 1 || num_splits > 1024) return BWATTN_ERR_INVALID_ARG;
   if (B > 65535) return BWATTN_ERR_INVALID_ARG;
   const int g = Hq / Hkv;
-  if ((d != 64 && d != 128) || (fp8 && d != 128) || g > 32 || Hkv > 32767) return BWATTN_ERR_UNSUPPORTED;
+  if ((d != 64 && d != 128 && d != 256) || (fp8 && d != 128) || g > 32 || Hkv > 32767) return BWATTN_ERR_UNSUPPORTED;
   if (B == 0) return BWATTN_OK;
   if (!q || !kcache || !vcache || !o || !nk || !workspace) return BWATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) || !aligned16(workspace) ||
@@ -421,7 +421,7 @@ int decode_paged(const void* q, const void* k_pages, const void* v_pages, const 
   if (Hq % Hkv != 0 || !good_scale(scale) || num_splits < 1 || num_splits > 1024) return BWATTN_ERR_INVALID_ARG;
   if (B > 65535 || static_cast<int64_t>(max_pages_per_seq) * page_size > 0x7fffffff) return BWATTN_ERR_INVALID_ARG;
   const int g = Hq / Hkv;
-  if ((d != 64 && d != 128) || (fp8 && d != 128) || g > 32 || Hkv > 32767) return BWATTN_ERR_UNSUPPORTED;
+  if ((d != 64 && d != 128 && d != 256) || (fp8 && d != 128) || g > 32 || Hkv > 32767) return BWATTN_ERR_UNSUPPORTED;
   if (B == 0) return BWATTN_OK;
   if (!q || !k_pages || !v_pages || !o || !block_table || !nk || !workspace) return BWATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o) || !aligned16(workspace) ||

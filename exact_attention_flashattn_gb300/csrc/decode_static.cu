@@ -61,7 +61,7 @@ extern "C" int attn_decode_static(const void* q, const void* kcache, const void*
     return BWATTN_ERR_INVALID_ARG;
   if (B > 65535) return BWATTN_ERR_INVALID_ARG;
   const int g = Hq / Hkv;
-  if ((d != 64 && d != 128) || g > 32 || Hkv > 32767) return BWATTN_ERR_UNSUPPORTED;
+  if ((d != 64 && d != 128 && d != 256) || g > 32 || Hkv > 32767) return BWATTN_ERR_UNSUPPORTED;
   if (B == 0) return BWATTN_OK;
   if (!q || !kcache || !vcache || !o || !nk) return BWATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) || !aligned4(nk) ||

@@ -180,17 +180,48 @@ __device__ __forceinline__ size_t ws_ml_index(const SplitKArgs& a, int unit, int
   return ((static_cast<size_t>(unit) * a.num_splits + s) * a.rows_max + r) * 2;
 }
 
-// D = head dim (64 or 128; the FP8 cache is 128 only);
+// d = 256: the two warps of a pair (key group kg = 0 or 1) add their partial score tiles, 4 * NH
+// scores per lane. Each warp writes its values into its half of the step's slot, meets its
+// partner at the pair's named barrier (id 1 + kg, 64 threads) and adds the partner's values; a + b is the
+// same float in both warps, so both take the same softmax. The slots alternate with the step
+// parity: a warp rewrites a slot two steps later, after the barrier of the step in between,
+// which its partner reaches only once it has read that slot.
+template <int NH>
+__device__ __forceinline__ void pair_sum(float4 (&slot)[2][32][NH], int half, int lane, int kg,
+                                         float (&v)[4 * NH]) {
+#pragma unroll
+  for (int i = 0; i < NH; ++i) slot[half][lane][i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  if (kg == 0)
+    asm volatile("bar.sync 1, 64;" ::: "memory");
+  else
+    asm volatile("bar.sync 2, 64;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < NH; ++i) {
+    const float4 o = slot[half ^ 1][lane][i];
+    v[4 * i] += o.x;
+    v[4 * i + 1] += o.y;
+    v[4 * i + 2] += o.z;
+    v[4 * i + 3] += o.w;
+  }
+}
+
+// D = head dim (64, 128 or 256; the FP8 cache is 128 only);
 // NH = number of 8-row halves of the 16-row MMA tile that carry real rows (1 or 2);
 // kPaged: keys are gathered page by page through the block table; kWindow: causal sliding
 // window (a separate instance, so the plain causal and paged paths carry no window registers);
 // kFp8: FP8 E4M3 cache with per-channel scales (k8, v8, k_scale, v_scale).
 template <int D, int NH, bool kPaged, bool kWindow, bool kFp8>
 __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(SplitKArgs a) {
-  static_assert(D == 64 || D == 128, "head dim");
+  static_assert(D == 64 || D == 128 || D == 256, "head dim");
   static_assert(!kFp8 || D == 128, "the FP8 cache layout is d = 128");
-  constexpr int kSteps = D / 16;  // k16 steps of S = Q K^T over the head dim
-  constexpr int kNT = D / 8;      // output n8 tiles of O (16-row form); 8-row pairs of them transposed
+  // d = 256: the warps work in pairs on the same 16-key steps, each warp holding 128 of the
+  // channels of Q, K, V and O; the pair adds its two partial score tiles through shared memory,
+  // so both warps take the same softmax and each accumulates its own half of O
+  constexpr bool kPair = D == 256;
+  constexpr int DW = kPair ? 128 : D;       // channels per warp
+  constexpr int kKG = kPair ? kWarps / 2 : kWarps;  // key groups (warps or warp pairs) per CTA
+  constexpr int kSteps = DW / 16;  // k16 steps of S = Q K^T over the warp's channels
+  constexpr int kNT = DW / 8;      // output n8 tiles of O (16-row form); 8-row pairs of them transposed
   extern __shared__ __align__(16) uint8_t dsm[];  // FP8: the load ring, then the combine buffer
   // a dependent merge launch may be scheduled from now on (it waits for this grid to complete)
   asm volatile("griddepcontrol.launch_dependents;");
@@ -206,6 +237,8 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int t = lane & 3, gr = lane >> 2;
+  const int kg = kPair ? warp >> 1 : warp;           // this warp's key group
+  const int hoff = kPair ? 128 * (warp & 1) : 0;     // first channel this warp holds
 
   // Key slice of this split: whole 16-key steps, at least min_chunk keys (varlen: the splits of a
   // short sequence past its last key are empty partials)
@@ -230,10 +263,10 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
       lim[rr] = kend;
       lo[rr] = 0;
     }
-    const uint16_t* qrow = a.q + (static_cast<int64_t>(u.tok0 + i) * a.Hq + hkv * a.g + hh) * D;
+    const uint16_t* qrow = a.q + (static_cast<int64_t>(u.tok0 + i) * a.Hq + hkv * a.g + hh) * D + hoff;
     if constexpr (!kFp8) {
 #pragma unroll
-      for (int s = 0; s < D / 32; ++s) {
+      for (int s = 0; s < DW / 32; ++s) {
         uint4 c = make_uint4(0, 0, 0, 0);
         if (ok) c = *reinterpret_cast<const uint4*>(qrow + 8 * (t + 4 * s));
         // k-step 2s uses words 0,1 of chunk t+4s; k-step 2s+1 words 2,3 (same permutation as K)
@@ -451,17 +484,20 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
   };
 
   if constexpr (!kFp8) {
-    for (int kb = kstart + warp * kKeysPerStep; kb < kend; kb += kWarps * kKeysPerStep) {
+    // d = 256: the pairs' exchange slots [key group][step parity][warp of the pair][lane]
+    __shared__ float4 xch[kKG][2][2][32][NH];
+    int step = 0;
+    for (int kb = kstart + kg * kKeysPerStep; kb < kend; kb += kKG * kKeysPerStep, ++step) {
       // ---- loads: K rows kb + nt*8 + gr (chunks t + 4s); V rows kb + {2t, 2t+1, 2t+8, 2t+9}
-      // (chunk gr into va; d = 128 also chunk 8 + gr into vb)
-      const int64_t so = step_offset<kPaged>(a, seq, kb);
-      uint4 kk[2][D / 32], va[4], vb[4];
+      // (chunk gr into va; 128 channels per warp also chunk 8 + gr into vb); all from channel hoff
+      const int64_t so = step_offset<kPaged>(a, seq, kb) + hoff;
+      uint4 kk[2][DW / 32], va[4], vb[4];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
         const int key = kb + nt * 8 + gr;
         const uint16_t* kr = kbase + so + static_cast<int64_t>(nt * 8 + gr) * ks;
 #pragma unroll
-        for (int s = 0; s < D / 32; ++s)
+        for (int s = 0; s < DW / 32; ++s)
           kk[nt][s] = (key < kend) ? ld_stream(kr + 8 * (t + 4 * s)) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
@@ -469,11 +505,11 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
         const int key = kb + 2 * t + (x & 1) + 8 * (x >> 1);
         const uint16_t* vr = vbase + so + static_cast<int64_t>(key - kb) * ks;
         va[x] = (key < kend) ? ld_stream(vr + 8 * gr) : make_uint4(0, 0, 0, 0);
-        if constexpr (D == 128) vb[x] = (key < kend) ? ld_stream(vr + 64 + 8 * gr) : make_uint4(0, 0, 0, 0);
+        if constexpr (DW == 128) vb[x] = (key < kend) ? ld_stream(vr + 64 + 8 * gr) : make_uint4(0, 0, 0, 0);
       }
       if constexpr (NH == 1) {
-        // ---- S^T = K Q^T: rows = keys gr / gr + 8 (the two K rows this thread loaded), D/16
-        // k16 steps over the head dim; Q is the B operand (row gr of the group)
+        // ---- S^T = K Q^T: rows = keys gr / gr + 8 (the two K rows this thread loaded), DW/16
+        // k16 steps over the warp's channels; Q is the B operand (row gr of the group)
         float st[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int kst = 0; kst < kSteps; ++kst) {
@@ -483,14 +519,15 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
                                   (kst & 1) ? r1.w : r1.y};
           mma_bf16(st, af, qa[kst][0], qa[kst][2]);
         }
+        if constexpr (kPair) pair_sum<NH>(xch[kg][step & 1], warp & 1, lane, kg, st);
         uint32_t b0, b1;
         softmax_stepT(kb, st, b0, b1);
-        // ---- O^T += V^T P^T over D/16 channel tiles: tile mu, rows gr and gr + 8 = channels
-        // chA_of(gr, mu) and chB_of(gr, mu); keys 2t, 2t+1 | 2t+8, 2t+9
+        // ---- O^T += V^T P^T over DW/16 channel tiles: tile mu, rows gr and gr + 8 = channels
+        // hoff + chA_of(gr, mu) and hoff + chB_of(gr, mu); keys 2t, 2t+1 | 2t+8, 2t+9
 #pragma unroll
-        for (int mu = 0; mu < D / 16; ++mu) {
+        for (int mu = 0; mu < DW / 16; ++mu) {
           uint32_t af[4];
-          if constexpr (D == 128) {
+          if constexpr (DW == 128) {
             const int w = mu >> 1;
             const uint32_t sel = (mu & 1) ? 0x7632u : 0x5410u;
             af[0] = __byte_perm(word(va[0], w), word(va[1], w), sel);
@@ -520,9 +557,10 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
             mma_bf16(sacc[nt], qa[kst], b0, b1);
           }
         }
+        if constexpr (kPair) pair_sum<NH>(xch[kg][step & 1], warp & 1, lane, kg, *reinterpret_cast<float(*)[8]>(&sacc[0][0]));
         uint32_t pa[4];
         softmax_step(kb, sacc, pa);
-        // ---- O += P V over D/8 output n-tiles
+        // ---- O += P V over DW/8 output n-tiles
 #pragma unroll
         for (int nu = 0; nu < kNT; ++nu) {
           const int e = nu & 7;
@@ -661,16 +699,17 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
     cp_async_wait<0>();  // nothing in flight once the ring is reused for the combine below
   }
 
-  // ---- combine the warps' states in shared memory, write this split's partials
-  __shared__ float sm_m[kWarps][kRowsPerGroup];
-  __shared__ float sm_l[kWarps][kRowsPerGroup];
+  // ---- combine the key groups' states in shared memory, write this split's partials (d = 256:
+  // the two warps of a pair hold the same m and l and one half of the channels each)
+  __shared__ float sm_m[kKG][kRowsPerGroup];
+  __shared__ float sm_l[kKG][kRowsPerGroup];
   float (*sm_o)[kRowsPerGroup][D + 4];
   if constexpr (kFp8) {
     // the FP8 ring is free now: every warp must be past its last read before it is reused
     __syncthreads();
     sm_o = reinterpret_cast<float (*)[kRowsPerGroup][D + 4]>(dsm);
   } else {
-    __shared__ float sm_o_static[kWarps][kRowsPerGroup][D + 4];
+    __shared__ float sm_o_static[kKG][kRowsPerGroup][D + 4];
     sm_o = sm_o_static;
   }
   if constexpr (NH == 1) {
@@ -681,22 +720,22 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
       l += __shfl_xor_sync(0xffffffffu, l, 4);
       l += __shfl_xor_sync(0xffffffffu, l, 8);
       l += __shfl_xor_sync(0xffffffffu, l, 16);
-      if (gr == 0) {
-        sm_m[warp][2 * t + j] = m_run[j];
-        sm_l[warp][2 * t + j] = l;
+      if (gr == 0 && hoff == 0) {
+        sm_m[kg][2 * t + j] = m_run[j];
+        sm_l[kg][2 * t + j] = l;
       }
     }
     // tile mu: c0, c1 -> channel A (rows 2t, 2t+1), c2, c3 -> channel B
     const float* vsc = kFp8 ? a.v_scale + hkv * D : nullptr;
 #pragma unroll
-    for (int mu = 0; mu < D / 16; ++mu) {
-      const int chA = kFp8 ? 16 * gr + mu : chA_of<D>(gr, mu);
-      const int chB = kFp8 ? 16 * gr + 8 + mu : chB_of<D>(gr, mu);
+    for (int mu = 0; mu < DW / 16; ++mu) {
+      const int chA = kFp8 ? 16 * gr + mu : hoff + chA_of<DW>(gr, mu);
+      const int chB = kFp8 ? 16 * gr + 8 + mu : hoff + chB_of<DW>(gr, mu);
       const float sA = kFp8 ? vsc[chA] : 1.f, sB = kFp8 ? vsc[chB] : 1.f;
-      sm_o[warp][2 * t][chA] = oacc[2 * mu][0] * sA;
-      sm_o[warp][2 * t + 1][chA] = oacc[2 * mu][1] * sA;
-      sm_o[warp][2 * t][chB] = oacc[2 * mu + 1][0] * sB;
-      sm_o[warp][2 * t + 1][chB] = oacc[2 * mu + 1][1] * sB;
+      sm_o[kg][2 * t][chA] = oacc[2 * mu][0] * sA;
+      sm_o[kg][2 * t + 1][chA] = oacc[2 * mu][1] * sA;
+      sm_o[kg][2 * t][chB] = oacc[2 * mu + 1][0] * sB;
+      sm_o[kg][2 * t + 1][chB] = oacc[2 * mu + 1][1] * sB;
     }
   } else {
 #pragma unroll
@@ -704,18 +743,18 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
       float l = l_part[rr];
       l += __shfl_xor_sync(0xffffffffu, l, 1);
       l += __shfl_xor_sync(0xffffffffu, l, 2);
-      if (t == 0) {
-        sm_m[warp][gr + 8 * rr] = m_run[rr];
-        sm_l[warp][gr + 8 * rr] = l;
+      if (t == 0 && hoff == 0) {
+        sm_m[kg][gr + 8 * rr] = m_run[rr];
+        sm_l[kg][gr + 8 * rr] = l;
       }
     }
     if constexpr (!kFp8) {
 #pragma unroll
       for (int nu = 0; nu < kNT; ++nu) {
-        sm_o[warp][gr][dv_of(nu, 2 * t)] = oacc[nu][0];
-        sm_o[warp][gr][dv_of(nu, 2 * t + 1)] = oacc[nu][1];
-        sm_o[warp][gr + 8][dv_of(nu, 2 * t)] = oacc[nu][2];
-        sm_o[warp][gr + 8][dv_of(nu, 2 * t + 1)] = oacc[nu][3];
+        sm_o[kg][gr][hoff + dv_of(nu, 2 * t)] = oacc[nu][0];
+        sm_o[kg][gr][hoff + dv_of(nu, 2 * t + 1)] = oacc[nu][1];
+        sm_o[kg][gr + 8][hoff + dv_of(nu, 2 * t)] = oacc[nu][2];
+        sm_o[kg][gr + 8][hoff + dv_of(nu, 2 * t + 1)] = oacc[nu][3];
       }
     } else {
       // this thread's channels are 32t .. 32t + 31: apply the V scale there
@@ -724,10 +763,10 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
       for (int nu = 0; nu < 16; ++nu) {
         const int c0 = dv8_of(nu, 2 * t), c1 = dv8_of(nu, 2 * t + 1);
         const float s0 = vsc[c0], s1 = vsc[c1];
-        sm_o[warp][gr][c0] = oacc[nu][0] * s0;
-        sm_o[warp][gr][c1] = oacc[nu][1] * s1;
-        sm_o[warp][gr + 8][c0] = oacc[nu][2] * s0;
-        sm_o[warp][gr + 8][c1] = oacc[nu][3] * s1;
+        sm_o[kg][gr][c0] = oacc[nu][0] * s0;
+        sm_o[kg][gr][c1] = oacc[nu][1] * s1;
+        sm_o[kg][gr + 8][c0] = oacc[nu][2] * s0;
+        sm_o[kg][gr + 8][c1] = oacc[nu][3] * s1;
       }
     }
   }
@@ -742,12 +781,12 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
     if (r >= nrows) continue;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w)
+    for (int w = 0; w < kKG; ++w)
       if (sm_l[w][r] > 0.f) M = fmaxf(M, sm_m[w][r]);
     float L = 0.f;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
+    for (int w = 0; w < kKG; ++w) {
       if (!(sm_l[w][r] > 0.f)) continue;
       const float f = ex2(sm_m[w][r] - M);
       L += f * sm_l[w][r];
@@ -872,43 +911,58 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(MergeArgs a) {
 #pragma unroll
   for (int w = 1; w < kMW; ++w) M = fmaxf(M, sh_red[w]);
 
-  // this warp's splits: s = warp, warp + kMW, ...; lane owns channels 4*lane .. 4*lane+3
-  // (d = 64: lanes 16..31 hold none and read channel 0 .. 3 again, their sums unused)
-  const int c4 = lane < D / 4 ? lane : 0;
+  // this warp's splits: s = warp, warp + kMW, ...; lane owns the channel quads lane + 32 j
+  // (d = 64: lanes 16..31 hold none and read quad 0 again, their sums unused; d = 256: two each)
+  constexpr int kC4 = D / 4;
+  constexpr int kPL = (kC4 + 31) / 32;
   float L = 0.f;
-  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 o[kPL];
+#pragma unroll
+  for (int j = 0; j < kPL; ++j) o[j] = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int s = warp; s < S; s += kMW) {
     const float2 v = *reinterpret_cast<const float2*>(ml + s * ml_stride);
     if (!(v.y > 0.f)) continue;
     const float f = ex2(v.x - M);
     L += f * v.y;
-    const float4 x = *reinterpret_cast<const float4*>(wo + s * o_stride + 4 * c4);
-    o.x += f * x.x;
-    o.y += f * x.y;
-    o.z += f * x.z;
-    o.w += f * x.w;
+#pragma unroll
+    for (int j = 0; j < kPL; ++j) {
+      const int c4 = lane + 32 * j < kC4 ? lane + 32 * j : 0;
+      const float4 x = *reinterpret_cast<const float4*>(wo + s * o_stride + 4 * c4);
+      o[j].x += f * x.x;
+      o[j].y += f * x.y;
+      o[j].z += f * x.z;
+      o[j].w += f * x.w;
+    }
   }
-  if (lane < D / 4) sh_o[warp][lane] = o;
+#pragma unroll
+  for (int j = 0; j < kPL; ++j)
+    if (lane + 32 * j < kC4) sh_o[warp][lane + 32 * j] = o[j];
   if (lane == 0) sh_l[warp] = L;
   __syncthreads();
-  if (warp != 0 || lane >= D / 4) return;
+  if (warp != 0 || lane >= kC4) return;
   L = 0.f;
-  o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-  for (int w = 0; w < kMW; ++w) {
-    L += sh_l[w];
-    const float4 x = sh_o[w][c4];
-    o.x += x.x;
-    o.y += x.y;
-    o.z += x.z;
-    o.w += x.w;
-  }
+  for (int w = 0; w < kMW; ++w) L += sh_l[w];
   const float inv = (L > 0.f) ? 1.f / L : 0.f;
   const int64_t orow = (static_cast<int64_t>(tok0 + i) * a.Hq + hkv * a.g + hh);
-  uint2 packed;
-  packed.x = pack_bf16x2(o.x * inv, o.y * inv);
-  packed.y = pack_bf16x2(o.z * inv, o.w * inv);
-  *reinterpret_cast<uint2*>(a.o + orow * D + 4 * lane) = packed;
+#pragma unroll
+  for (int j = 0; j < kPL; ++j) {
+    const int c4 = lane + 32 * j;
+    if (c4 >= kC4) break;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < kMW; ++w) {
+      const float4 x = sh_o[w][c4];
+      acc.x += x.x;
+      acc.y += x.y;
+      acc.z += x.z;
+      acc.w += x.w;
+    }
+    uint2 packed;
+    packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+    packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(a.o + orow * D + 4 * c4) = packed;
+  }
   if (a.lse && lane == 0) a.lse[orow] = (L > 0.f) ? (M + log2f(L)) * kLn2 : -INFINITY;
 }
 
@@ -955,6 +1009,7 @@ cudaError_t launch_splitk_d(const SplitKArgs& a, cudaStream_t stream) {
 cudaError_t launch_splitk(const SplitKArgs& a, cudaStream_t stream) {
   if (a.d == 64) return launch_splitk_d<64>(a, stream);
   if (a.d == 128) return launch_splitk_d<128>(a, stream);
+  if (a.d == 256) return launch_splitk_d<256>(a, stream);
   return cudaErrorInvalidValue;
 }
 
@@ -975,6 +1030,7 @@ cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
   cfg.numAttrs = 1;
   if (a.d == 64) return cudaLaunchKernelEx(&cfg, merge_kernel<64>, a);
   if (a.d == 128) return cudaLaunchKernelEx(&cfg, merge_kernel<128>, a);
+  if (a.d == 256) return cudaLaunchKernelEx(&cfg, merge_kernel<256>, a);
   return cudaErrorInvalidValue;
 }
 

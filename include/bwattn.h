@@ -133,8 +133,9 @@ size_t attn_decode_workspace_size(int B, int Hq, int d, int num_splits);
  *              bytes; contents on entry are ignored, on exit undefined. Must not be shared
  *              by calls that may overlap on the GPU.
  * The g = Hq / Hkv query heads of a group are packed against each K/V tile, so every cache
- * byte is read once. Supported: d in {64, 128}, 1 <= g <= 32. Errors as for attn_fwd, plus
- * INVALID_ARG when the workspace is NULL or too small.
+ * byte is read once. Supported: d in {64, 128, 256} ("Production implications": the fast
+ * kernels' head dims), 1 <= g <= 32. Errors as for attn_fwd, plus INVALID_ARG when the
+ * workspace is NULL or too small.
  */
 int attn_decode(const void* q, const void* kcache, const void* vcache, void* o, const int32_t* nk, int B, int Hq,
                 int Hkv, int nk_cap, int d, int num_splits, float scale, float* lse, void* workspace,
@@ -157,7 +158,7 @@ int attn_decode(const void* q, const void* kcache, const void* vcache, void* o, 
  *   nk          : [B] int32 DEVICE array, 0 <= nk[b] <= max_pages_per_seq * page_size
  *   page_size   : a multiple of 16, 16..1024
  *   workspace   : at least attn_decode_workspace_size(B, Hq, d, num_splits) bytes
- * Supported: d in {64, 128}, 1 <= g <= 32. Errors as for attn_decode.
+ * Supported: d in {64, 128, 256}, 1 <= g <= 32. Errors as for attn_decode.
  */
 int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages, void* o, const int32_t* block_table,
                       const int32_t* nk, int B, int Hq, int Hkv, int page_size, int num_pages, int max_pages_per_seq,

@@ -98,6 +98,12 @@ def test_decode_argument_errors(L):
     assert 0 < need64 < need
     assert dec(L, d=64, wsb=need64 - 1) == bw.ERR_INVALID_ARG
     assert dec(L, d=64, B=0, q=None) == bw.OK
+    # d = 256 likewise (bf16 caches; the FP8 cache stays d = 128)
+    need256 = L.attn_decode_workspace_size(2, 8, 256, 4)
+    assert need256 > need
+    assert dec(L, d=256, wsb=need256 - 1) == bw.ERR_INVALID_ARG
+    assert dec(L, d=256, B=0, q=None) == bw.OK
+    assert dec(L, d=192) == bw.ERR_UNSUPPORTED
     assert dec(L, Hq=66, Hkv=1) == bw.ERR_UNSUPPORTED
     assert dec(L, nk=FAKE + 2) == bw.ERR_INVALID_ARG
     assert dec(L, B=0, q=None) == bw.OK
@@ -169,6 +175,7 @@ def test_fp8_decode_argument_errors(L):
         assert f(k=FAKE + 8) == bw.ERR_INVALID_ARG
         assert f(ws=None) == bw.ERR_INVALID_ARG
         assert f(d=64) == bw.ERR_UNSUPPORTED
+        assert f(d=256) == bw.ERR_UNSUPPORTED
         assert f(Hq=8, Hkv=3) == bw.ERR_INVALID_ARG
         assert f(B=0, q=None) == bw.OK
     assert p8(ps=24) == bw.ERR_INVALID_ARG

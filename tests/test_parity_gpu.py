@@ -593,6 +593,71 @@ def test_decode_paged_d64_matches_oracle_and_contiguous(B, Hq, Hkv, cap, nk, S, 
     assert torch.equal(o, oc) and torch.equal(lse, lc)
 
 
+# ------------------------------------------------------------------ head dim 256 on the split-K paths
+# Each warp pair shares a 16-key step, one warp per 128 channels; the pair adds its partial
+# scores in shared memory before the softmax.
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,cap,nk,S", [
+    (3, 8, 2, 300, [300, 17, 0], 4),     # g = 4 (transposed form), ragged, an empty sequence
+    (2, 8, 8, 1000, [1000, 999], 7),     # g = 1
+    (1, 16, 2, 513, [513], 64),          # g = 8, 64 splits: the separate merge kernel
+    (2, 16, 1, 400, [400, 250], 3),      # g = 16 (16-row form), fused merge
+    (1, 32, 1, 200, [200], 40),          # g = 32: two row groups, separate merge
+])
+def test_decode_d256(B, Hq, Hkv, cap, nk, S):
+    q, kc, vc, nkt = wl.decode_inputs(B, Hq, Hkv, cap, 256, torch.bfloat16, seed=231 + cap, nk=nk)
+    o_ref, lse_ref = oracle.decode(f64(q), f64(kc), f64(vc), nkt.numpy(), method="splitk", workers=S)
+    o, lse = bw.attn_decode(q.cuda(), kc.cuda(), vc.cuda(), nkt.cuda(), num_splits=S)
+    torch.cuda.synchronize()
+    check_bf16(o, o_ref, lse, lse_ref, what=("d256", B, Hq, Hkv, cap, nk, S))
+
+
+def test_decode_d256_channel_halves_are_not_swapped():
+    # V nonzero in one channel of each half only: a half written to the other's channels, or
+    # one warp's partial scores dropped, moves or changes these columns
+    q, kc, vc, nkt = wl.decode_inputs(2, 8, 2, 400, 256, torch.bfloat16, seed=241, nk=[400, 123])
+    vc.zero_()
+    vc[..., 5] = 1.0
+    vc[..., 200] = torch.linspace(-1, 1, 400, dtype=torch.bfloat16)
+    kc[..., 128:] *= 4  # the scores depend mostly on the second half of the channels
+    o_ref, lse_ref = oracle.decode(f64(q), f64(kc), f64(vc), nkt.numpy(), method="splitk", workers=3)
+    o, lse = bw.attn_decode(q.cuda(), kc.cuda(), vc.cuda(), nkt.cuda(), num_splits=3)
+    torch.cuda.synchronize()
+    check_bf16(o, o_ref, lse, lse_ref, what="d256 halves")
+    other = [c for c in range(256) if c not in (5, 200)]
+    assert torch.count_nonzero(o[..., other]) == 0
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,cap,nk,S,ps", [
+    (3, 8, 2, 256, [256, 17, 0], 4, 16),    # transposed form, 16-token pages
+    (2, 32, 2, 512, [512, 300], 9, 32),     # g = 16: 16-row form, 32-token pages
+])
+def test_decode_paged_d256_matches_oracle_and_contiguous(B, Hq, Hkv, cap, nk, S, ps):
+    q, kc, vc, nkt = wl.decode_inputs(B, Hq, Hkv, cap, 256, torch.bfloat16, seed=281 + cap, nk=nk)
+    kp, vp, table = wl.paged_from_dense(kc, vc, ps, seed=281)
+    o_ref, lse_ref = oracle.decode_paged(f64(q), f64(kp), f64(vp), table.numpy(), nkt.numpy(), method="splitk",
+                                         workers=S)
+    o, lse = bw.attn_decode_paged(q.cuda(), kp.cuda(), vp.cuda(), table.cuda(), nkt.cuda(), num_splits=S)
+    oc, lc = bw.attn_decode(q.cuda(), kc.cuda(), vc.cuda(), nkt.cuda(), num_splits=S)
+    torch.cuda.synchronize()
+    check_bf16(o, o_ref, lse, lse_ref, what=("paged d256", B, Hq, Hkv, cap, nk, S, ps))
+    assert torch.equal(o, oc) and torch.equal(lse, lc)
+
+
+def test_decode_d256_long_context_sampled():
+    # 4 sequences x 8 KV heads x 32768 keys x 256 channels (1.07 GB of cache), 16 splits; the
+    # oracle takes every query head of the first and the last sequence
+    B, Hq, Hkv, N, S = 4, 32, 8, 32768, 16
+    q, kc, vc, nkt = wl.decode_inputs(B, Hq, Hkv, N, 256, torch.bfloat16, seed=251, nk=[N, 30001, 17, N], device="cuda")
+    o, lse = bw.attn_decode(q, kc, vc, nkt.cuda(), num_splits=S)
+    torch.cuda.synchronize()
+    for b, n in ((0, N), (3, N)):
+        o_ref, lse_ref = oracle.decode(f64(q[b:b + 1]), f64(kc[b:b + 1]), f64(vc[b:b + 1]), [n], method="splitk",
+                                       workers=S)
+        check_bf16(o[b:b + 1], o_ref, lse[b:b + 1], lse_ref, what=("d256 long", b))
+
+
 @pytest.mark.parametrize("causal,W", [(True, 0), (False, 0), (True, 100)])
 def test_varlen_d64(causal, W):
     nq = [1, 4, 8, 200, 300, 3, 129, 0]
