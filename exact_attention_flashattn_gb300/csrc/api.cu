@@ -243,7 +243,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (Hq % Hkv != 0 || !good_scale(scale) || (causal != 0 && causal != 1)) return BWATTN_ERR_INVALID_ARG;
   if (B > 65535 || Hq > 65535) return BWATTN_ERR_INVALID_ARG;
   if (dtype != BWATTN_DTYPE_FP32 && dtype != BWATTN_DTYPE_BF16) return BWATTN_ERR_UNSUPPORTED;
-  if (d != 64 && d != 128) return BWATTN_ERR_UNSUPPORTED;
+  if ((d != 64 && d != 128 && d != 256) || (d == 256 && dtype == BWATTN_DTYPE_FP32)) return BWATTN_ERR_UNSUPPORTED;
   if (B == 0 || Nq == 0) return BWATTN_OK;
   if (!q || !o || ((!k || !v) && Nk > 0)) return BWATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(o) || (Nk > 0 && (!aligned16(k) || !aligned16(v)))) return BWATTN_ERR_INVALID_ARG;
@@ -267,10 +267,11 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     return cuda_fail(e);
   const int64_t kv_heads_map = Nk > 0 ? static_cast<int64_t>(B) * Hkv : static_cast<int64_t>(B) * Hq;
   const int nk_rows = Nk > 0 ? nk_map : Nq;
-  if ((e = make_map(&a.tm_k, kp, d, nk_rows, kv_heads_map, d, static_cast<int64_t>(nk_rows) * d, 128, 1)) !=
+  const int kv_box = d == 256 ? 64 : 128;  // keys per K/V tile
+  if ((e = make_map(&a.tm_k, kp, d, nk_rows, kv_heads_map, d, static_cast<int64_t>(nk_rows) * d, kv_box, 1)) !=
       cudaSuccess)
     return cuda_fail(e);
-  if ((e = make_map(&a.tm_v, vp, d, nk_rows, kv_heads_map, d, static_cast<int64_t>(nk_rows) * d, 128, 1)) !=
+  if ((e = make_map(&a.tm_v, vp, d, nk_rows, kv_heads_map, d, static_cast<int64_t>(nk_rows) * d, kv_box, 1)) !=
       cudaSuccess)
     return cuda_fail(e);
   a.o = static_cast<uint16_t*>(o);
@@ -285,7 +286,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   a.causal = causal;
   a.num_seqs = B;
   a.small_rows_limit = 0;
-  a.max_pairs = (Nq + 255) / 256;
+  a.max_pairs = d == 256 ? (Nq + 127) / 128 : (Nq + 255) / 256;  // items per (sequence, head)
   a.band_units = band_units_for(Nk, d, Hq / Hkv);
   a.window = window;
   a.scale_log2 = sl2;
@@ -294,7 +295,9 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   unsigned int* sc = nullptr;
   if ((e = status_ptr(&sp)) != cudaSuccess) return cuda_fail(e);
   if ((e = sched_ptr(&sc)) != cudaSuccess) return cuda_fail(e);
-  if ((e = bw::launch_prefill_tc(a, sp, sc, st)) != cudaSuccess) return cuda_fail(e);
+  if ((e = (d == 256 ? bw::launch_prefill_tc256(a, sp, sc, st) : bw::launch_prefill_tc(a, sp, sc, st))) !=
+      cudaSuccess)
+    return cuda_fail(e);
   g_launches.fetch_add(1);
   return BWATTN_OK;
 }
@@ -504,7 +507,7 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
     return BWATTN_ERR_INVALID_ARG;
   if (num_seqs > 65535 || Hq > 65535) return BWATTN_ERR_INVALID_ARG;
   const int g = Hq / Hkv;
-  if ((d != 64 && d != 128) || g > kSmallRowsLimit) return BWATTN_ERR_UNSUPPORTED;
+  if ((d != 64 && d != 128 && d != 256) || g > kSmallRowsLimit) return BWATTN_ERR_UNSUPPORTED;
   if (num_seqs == 0 || total_q == 0 || max_seqlen_q == 0) return BWATTN_OK;
   if (!q || !o || !cu_seqlens_q || !cu_seqlens_k || !workspace || (total_k > 0 && (!k || !v)))
     return BWATTN_ERR_INVALID_ARG;
@@ -527,9 +530,12 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
     const int tk_map = total_k > 0 ? total_k : total_q;
     if ((e = make_map(&a.tm_q, q, d, Hq, total_q, d, static_cast<int64_t>(Hq) * d, 1, 128)) != cudaSuccess)
       return cuda_fail(e);
-    if ((e = make_map(&a.tm_k, kp, d, hk_map, tk_map, d, static_cast<int64_t>(hk_map) * d, 1, 128)) != cudaSuccess)
+    const int kv_box = d == 256 ? 64 : 128;  // keys per K/V tile
+    if ((e = make_map(&a.tm_k, kp, d, hk_map, tk_map, d, static_cast<int64_t>(hk_map) * d, 1, kv_box)) !=
+        cudaSuccess)
       return cuda_fail(e);
-    if ((e = make_map(&a.tm_v, vp, d, hk_map, tk_map, d, static_cast<int64_t>(hk_map) * d, 1, 128)) != cudaSuccess)
+    if ((e = make_map(&a.tm_v, vp, d, hk_map, tk_map, d, static_cast<int64_t>(hk_map) * d, 1, kv_box)) !=
+        cudaSuccess)
       return cuda_fail(e);
     a.o = static_cast<uint16_t*>(o);
     a.lse = lse;
@@ -544,7 +550,7 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
     a.causal = causal;
     a.num_seqs = num_seqs;
     a.small_rows_limit = kSmallRowsLimit;
-    a.max_pairs = (max_seqlen_q + 255) / 256;
+    a.max_pairs = d == 256 ? (max_seqlen_q + 127) / 128 : (max_seqlen_q + 255) / 256;
     a.band_units = band_units_for(max_seqlen_k, d, g);
     a.window = window;
     a.scale_log2 = sl2;
@@ -553,7 +559,9 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
     unsigned int* sc = nullptr;
     if ((e = status_ptr(&sp)) != cudaSuccess) return cuda_fail(e);
     if ((e = sched_ptr(&sc)) != cudaSuccess) return cuda_fail(e);
-    if ((e = bw::launch_prefill_tc(a, sp, sc, st)) != cudaSuccess) return cuda_fail(e);
+    if ((e = (d == 256 ? bw::launch_prefill_tc256(a, sp, sc, st) : bw::launch_prefill_tc(a, sp, sc, st))) !=
+        cudaSuccess)
+      return cuda_fail(e);
     g_launches.fetch_add(1);
   }
   // 2) sequences with few queries: split-K kernel with the (query, head) rows packed, then merge

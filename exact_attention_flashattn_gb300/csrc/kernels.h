@@ -105,6 +105,9 @@ struct TcFwdArgs {
 // `sched`: two zeroed device counters (next item, CTAs finished) owned by this launch alone;
 // the kernel leaves them zeroed again when it completes.
 cudaError_t launch_prefill_tc(const TcFwdArgs& a, unsigned int* status, unsigned int* sched, cudaStream_t stream);
+// Head dim 256: one 128-row query tile per item, 64-key K/V tiles (the K/V maps' box is 64 rows
+// or tokens high), a.max_pairs = query tiles per (sequence, head).
+cudaError_t launch_prefill_tc256(const TcFwdArgs& a, unsigned int* status, unsigned int* sched, cudaStream_t stream);
 
 // Timeout self-test: one CTA waits on a barrier that is never arrived at.
 cudaError_t launch_wait_timeout_probe(uint64_t timeout_ns, unsigned int* status, cudaStream_t stream);

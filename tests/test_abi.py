@@ -70,6 +70,8 @@ def test_fwd_argument_errors(L):
     assert fwd(L, lse=FAKE + 2) == bw.ERR_INVALID_ARG
     assert fwd(L, d=96) == bw.ERR_UNSUPPORTED
     assert fwd(L, dtype=7) == bw.ERR_UNSUPPORTED
+    assert fwd(L, d=256, B=0) == bw.OK  # bf16 at d = 256: the tcgen05 kernel's d = 256 instance
+    assert fwd(L, d=256, dtype=bw.DTYPE_FP32) == bw.ERR_UNSUPPORTED  # the fp32 FMA kernel stops at 128
     # empty work is a valid no-op that touches nothing
     assert fwd(L, B=0, q=None, k=None, v=None, o=None) == bw.OK
     assert fwd(L, Nq=0, q=None, k=None, v=None, o=None) == bw.OK

@@ -671,6 +671,97 @@ def test_varlen_d64(causal, W):
     check_bf16(o, o_ref, lse, lse_ref, what=("varlen d64", causal, W))
 
 
+# ------------------------------------------------------------------ head dim 256 prefill
+# One 128-row query tile per CTA, 64-key K/V tiles, S double-buffered in tensor memory.
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,causal", [
+    (1, 1, 1, 128, 128, True),      # one query tile, two K/V tiles
+    (2, 4, 2, 640, 640, True),      # 5 query tiles, GQA
+    (1, 2, 2, 300, 700, False),     # ragged cross attention
+    (1, 2, 1, 333, 1000, True),     # ragged, bottom-right causal
+    (1, 2, 2, 200, 90, True),       # more queries than keys: rows with no visible key
+    (1, 1, 1, 1, 1, True),          # one query, one key
+    (1, 3, 1, 1100, 1100, True),    # several items per CTA, odd K/V tile counts
+    (1, 2, 2, 129, 65, False),      # one key past a K/V tile, one row past a query tile
+])
+def test_prefill_d256(B, Hq, Hkv, Nq, Nk, causal):
+    q, k, v = wl.prefill_inputs(B, Hq, Hkv, Nq, Nk, 256, torch.bfloat16, seed=311 + Nq + Nk)
+    o_ref, lse_ref = oracle.attention(f64(q), f64(k), f64(v), causal, method="tiled", block=128)
+    o, lse = bw.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal)
+    torch.cuda.synchronize()
+    check_bf16(o, o_ref, lse, lse_ref, what=("d256", B, Hq, Hkv, Nq, Nk, causal))
+
+
+def test_prefill_d256_growing_max_rescales_o():
+    # keys grow along the sequence, so every row's running max rises by far more than 2^8 at
+    # later K/V tiles: o is rescaled in tensor memory after the previous P.V has completed
+    q, k, v = wl.prefill_inputs(1, 2, 2, 256, 1024, 256, torch.bfloat16, seed=331)
+    q = q.abs()
+    grow = torch.linspace(0.2, 6.0, 1024, dtype=torch.float32)[None, None, :, None]
+    k = (k.float().abs() * grow).to(torch.bfloat16)
+    o_ref, lse_ref = oracle.attention(f64(q), f64(k), f64(v), False, method="tiled", block=128)
+    o, lse = bw.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=False)
+    torch.cuda.synchronize()
+    # the scores reach several hundred: the LSE carries their bf16 rounding, relative to its size
+    check_bf16(o, o_ref, lse, lse_ref, what="d256 growing max", lse_tol=2e-3 * np.maximum(1.0, np.abs(lse_ref)))
+
+
+def test_prefill_d256_masked_keys_are_never_read():
+    q, k, v = wl.prefill_inputs(1, 2, 2, 300, 300, 256, torch.bfloat16, seed=341)
+    o1, l1 = bw.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True)
+    k2, v2 = k.clone(), v.clone()
+    # rows below 150 never see keys at or above 150: large finite values there change no bit of them
+    k2[:, :, 150:] = 3.0e4
+    v2[:, :, 150:] = -3.0e4
+    o2, l2 = bw.attn_fwd(q.cuda(), k2.cuda(), v2.cuda(), causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1[:, :, :150], o2[:, :, :150]) and torch.equal(l1[:, :, :150], l2[:, :, :150])
+
+
+@pytest.mark.parametrize("W", [1, 100, 300])
+def test_window_d256(W):
+    q, k, v = wl.prefill_inputs(2, 8, 2, 500, 777, 256, torch.bfloat16, seed=351 + W)
+    o_ref, lse_ref = oracle.attention(f64(q), f64(k), f64(v), True, method="tiled", block=128, window=W)
+    o, lse = bw.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True, window=W)
+    torch.cuda.synchronize()
+    check_bf16(o, o_ref, lse, lse_ref, what=("window d256", W))
+
+
+@pytest.mark.parametrize("causal,W", [(True, 0), (False, 0), (True, 100)])
+def test_varlen_d256(causal, W):
+    nq = [1, 4, 8, 200, 300, 3, 129, 0]
+    nk = [50, 700, 8, 200, 1000, 2100, 129, 9]
+    q, k, v, cq, ck = wl.varlen_inputs(nq, nk, 8, 2, 256, torch.bfloat16, seed=361 + W + causal)
+    o_ref, lse_ref = oracle.varlen(f64(q), f64(k), f64(v), cq.numpy(), ck.numpy(), causal, method="tiled", block=128,
+                                   window=W)
+    o, lse = bw.attn_varlen(q.cuda(), k.cuda(), v.cuda(), cq.cuda(), ck.cuda(), max(nq), max(nk), causal=causal,
+                            window=W)
+    torch.cuda.synchronize()
+    check_bf16(o, o_ref, lse, lse_ref, what=("varlen d256", causal, W))
+
+
+def test_prefill_d256_long_sampled_rows():
+    # B=2, H=16, N=4096 causal (sampled rows against the oracle, one by one)
+    B, H, N = 2, 16, 4096
+    q, k, v = wl.prefill_inputs(B, H, H, N, N, 256, torch.bfloat16, seed=371, device="cuda")
+    o, lse = bw.attn_fwd(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    g = torch.Generator().manual_seed(372)
+    rows = [(0, 0, 0), (B - 1, H - 1, N - 1), (1, 5, 127), (0, 9, 128), (1, 15, 4095)]
+    rows += [(int(torch.randint(0, B, (1,), generator=g)), int(torch.randint(0, H, (1,), generator=g)),
+              int(torch.randint(0, N, (1,), generator=g))) for _ in range(30)]
+    errs = []
+    for b, h, i in rows:
+        o_ref, lse_ref = oracle.attention(f64(q[b, h, i])[None, None, None], f64(k[b, h, :i + 1])[None, None],
+                                          f64(v[b, h, :i + 1])[None, None], False, method="naive")
+        e = np.abs(f64(o[b, h, i]) - o_ref[0, 0, 0])
+        errs.append(e)
+        assert e.max() <= TOL_BF16_MAX, (b, h, i, e.max())
+        assert abs(float(lse[b, h, i]) - lse_ref[0, 0, 0]) <= TOL_LSE
+    assert np.mean(np.concatenate(errs)) <= TOL_BF16_MEAN
+
+
 # ------------------------------------------------------------------ edge cases
 
 
