@@ -10,8 +10,9 @@
 // rows x 256 channels takes 256 of them, so one query tile is in flight per CTA (not two as at
 // d <= 128) and the other 256 columns hold two 64-column S buffers:
 //   TMEM columns   0..255  O (fp32)        256..319  S buffer 0      320..383  S buffer 1
-// K/V tiles are 64 keys x 256 channels (four 128-byte swizzle atoms, 32 KB) in a 4-stage ring;
-// with the 64 KB Q tile that is 192 KB of shared memory. A work item is one 128-row query tile
+// K/V tiles are 64 keys x 256 channels (four 128-byte swizzle atoms, 32 KB) in a 5-stage ring;
+// with the 64 KB Q tile that is 224 KB of shared memory (a fourth stage fewer left the tensor
+// pipe waiting for K/V: 10-14 % slower). A work item is one 128-row query tile
 // of a (sequence, head), taken from the same banded list as the d <= 128 kernel (persistent
 // CTAs, atomic counter, longest tiles of a band first). 6 warps per CTA:
 //   warp 4      TMA producer: Q once per item, then K_j, V_j into the ring.
@@ -25,10 +26,11 @@
 //               reference max moves only when the max grows by more than 2^8), P as bf16 into
 //               the first 32 columns of the S buffer, then the item's epilogue O = o / l, LSE.
 // Ordering of a rescale: o may be rescaled in TMEM at step j only after PV(j-1) has completed.
-// Every PV is followed by a commit to one mbarrier; the softmax waits for PV(j-1) at the end of
-// every step j, before it releases P(j). PV(j) cannot complete before that release, so exactly
-// one completion is outstanding at each wait and its parity is unambiguous; a rescale at step j
-// waits for the same completion first.
+// PV n commits to pv_done[n & 1]. When the softmax sees S(j), PV(j-2) and every PV before it have
+// completed (S(j) was issued after PV(j-2), and a commit tracks every earlier MMA), and PV(j+1)
+// cannot have been issued (P(j+1) does not exist yet); on pv_done[(j-1) & 1] the only phase that
+// can still be open is PV(j-1)'s own, so a rescale waits for that parity without ambiguity and the
+// common step waits for no PV at all.
 // Every wait is bounded; a timed-out wait sets the device status word, the CTA stops producing
 // output, waits for its own copies and MMAs and frees its TMEM.
 #include <math.h>
@@ -47,7 +49,7 @@ constexpr int kAtoms = kD / 64;  // 128-byte swizzle atoms across the head dim
 constexpr int kThreads = 192;
 constexpr int kTmaWarp = 4;
 constexpr int kMmaWarp = 5;
-constexpr int kStages = 4;
+constexpr int kStages = 5;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kItemSlots = 2;
 constexpr int kItemConsumers = 1 + 4;  // one lane of the MMA warp and of each softmax warp
@@ -63,7 +65,7 @@ struct Bars {
   uint64_t q_full, q_empty;
   uint64_t s_full[2];
   uint64_t p_full[2];
-  uint64_t pv_done;  // one phase per PV, in issue order
+  uint64_t pv_done[2];  // PV n completes a phase of pv_done[n & 1]
   uint64_t o_full, o_empty;
   uint64_t mma_done;
   uint64_t kv_full[kStages];
@@ -227,7 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc256_kernel(const __grid
       mbar_init(&bar->s_full[i], 1);
       mbar_init(&bar->p_full[i], kBM);
     }
-    mbar_init(&bar->pv_done, 1);
+    mbar_init(&bar->pv_done[0], 1);
+    mbar_init(&bar->pv_done[1], 1);
     mbar_init(&bar->o_full, 1);
     mbar_init(&bar->o_empty, kBM);
     mbar_init(&bar->mma_done, 1);
@@ -368,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc256_kernel(const __grid
         if (!(ok = vote(mbar_wait(&bar->p_full[npv & 1], (npv >> 1) & 1, tmo, abort)))) break;
         tc_fence_after();
         mma_pv(tO, tbase + kColS + 64 * (npv & 1), v_lo + (iv % kStages) * slot_step, hi, idesc_pv, j > 0);
-        umma_commit(&bar->pv_done);
+        umma_commit(&bar->pv_done[npv & 1]);
         ++npv;
         umma_commit(&bar->kv_empty[iv % kStages]);
         if (j == nt - 1) {
@@ -474,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc256_kernel(const __grid
         exp_half(s1, 16);
         // o takes the new reference max before PV(j) adds to it (rare); PV(j-1) must be done
         if (__any_sync(0xffffffffu, alpha_o != 1.f)) {
-          if (!(ok = vote(mbar_wait(&bar->pv_done, (gs - 1) & 1, tmo, abort)))) break;
+          if (!(ok = vote(mbar_wait(&bar->pv_done[(gs - 1) & 1], ((gs - 1) >> 1) & 1, tmo, abort)))) break;
           tc_fence_after();
 #pragma unroll 1
           for (int c = 0; c < kD / 32; ++c) {
@@ -487,8 +490,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc256_kernel(const __grid
             tmem_st32(tO + c * 32, ov);
           }
         }
-        // PV(gs - 1) completes before P(gs) is released: one completion outstanding per wait
-        if (gs > 0 && !(ok = vote(mbar_wait(&bar->pv_done, (gs - 1) & 1, tmo, abort)))) break;
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bar->p_full[b]);
