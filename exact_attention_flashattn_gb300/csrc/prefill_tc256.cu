@@ -8,27 +8,29 @@
 //
 // GB300 mapping at d = 256. Tensor memory has 512 columns of 128 lanes; an fp32 O tile of 128
 // rows x 256 channels takes 256 of them, so one query tile is in flight per CTA (not two as at
-// d <= 128) and the other 256 columns hold two 64-column S buffers:
-//   TMEM columns   0..255  O (fp32)        256..319  S buffer 0      320..383  S buffer 1
+// d <= 128) and 192 of the other 256 columns hold three 64-column S buffers:
+//   TMEM columns   0..255  O (fp32)        256 + 64 b .. 319 + 64 b  S buffer b (b = 0, 1, 2)
 // K/V tiles are 64 keys x 256 channels (four 128-byte swizzle atoms, 32 KB) in a 5-stage ring;
 // with the 64 KB Q tile that is 224 KB of shared memory (a fourth stage fewer left the tensor
 // pipe waiting for K/V: 10-14 % slower). A work item is one 128-row query tile
 // of a (sequence, head), taken from the same banded list as the d <= 128 kernel (persistent
 // CTAs, atomic counter, longest tiles of a band first). 6 warps per CTA:
-//   warp 4      TMA producer: Q once per item, then K_j, V_j into the ring.
-//   warp 5      MMA issuer, in the order S(0), S(1), PV(0), S(2), PV(1), S(3), ...: S(j+1) is
-//               computed into the other S buffer while the softmax works on S(j), and S(j+2)
-//               reuses S(j)'s buffer only after PV(j) (the tensor pipe runs in issue order).
-//               While the softmax of step j runs, PV(j-1) and S(j+1) are queued: 1024 cycles of
-//               tensor work against the softmax of 64 keys per row.
+//   warp 4      TMA producer: Q once per item, then the K and V tiles into the ring in the
+//               order the MMA warp consumes them.
+//   warp 5      MMA issuer, in the order S(0), S(1), S(2), PV(0), S(3), PV(1), S(4), ...: S of
+//               the next two K tiles is computed into the other S buffers while the softmax
+//               works on S(j), and S(j+3) reuses S(j)'s buffer only after PV(j) (the tensor pipe
+//               runs in issue order). While the softmax of step j runs, PV(j-1), S(j+1) and
+//               S(j+2) are queued against the softmax of 64 keys per row (one S tile of
+//               lookahead measured 2 % slower).
 //   warps 0-3   softmax, thread = row = TMEM lane: S row (64 scores) from TMEM, mask on tiles
 //               that cross the causal limit or the window start, row max, lazy rescale (the
 //               reference max moves only when the max grows by more than 2^8), P as bf16 into
 //               the first 32 columns of the S buffer, then the item's epilogue O = o / l, LSE.
 // Ordering of a rescale: o may be rescaled in TMEM at step j only after PV(j-1) has completed.
-// PV n commits to pv_done[n & 1]. When the softmax sees S(j), PV(j-2) and every PV before it have
-// completed (S(j) was issued after PV(j-2), and a commit tracks every earlier MMA), and PV(j+1)
-// cannot have been issued (P(j+1) does not exist yet); on pv_done[(j-1) & 1] the only phase that
+// PV n commits to pv_done[n % 3]. When the softmax sees S(j), PV(j-3) and every PV before it have
+// completed (S(j) was issued after PV(j-3), and a commit tracks every earlier MMA), and PV(j+2)
+// cannot have been issued (P(j+2) does not exist yet); on pv_done[(j-1) % 3] the only phase that
 // can still be open is PV(j-1)'s own, so a rescale waits for that parity without ambiguity and the
 // common step waits for no PV at all.
 // Every wait is bounded; a timed-out wait sets the device status word, the CTA stops producing
@@ -50,6 +52,7 @@ constexpr int kThreads = 192;
 constexpr int kTmaWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kStages = 5;
+constexpr int kLook = 3;  // S buffers: S(j+1) .. S(j+kLook-1) are issued before PV(j)
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kItemSlots = 2;
 constexpr int kItemConsumers = 1 + 4;  // one lane of the MMA warp and of each softmax warp
@@ -63,9 +66,9 @@ constexpr uint32_t kColO = 0, kColS = 256;  // S buffer b: columns kColS + 64 b
 
 struct Bars {
   uint64_t q_full, q_empty;
-  uint64_t s_full[2];
-  uint64_t p_full[2];
-  uint64_t pv_done[2];  // PV n completes a phase of pv_done[n & 1]
+  uint64_t s_full[kLook];
+  uint64_t p_full[kLook];
+  uint64_t pv_done[kLook];  // PV n completes a phase of pv_done[n % kLook]
   uint64_t o_full, o_empty;
   uint64_t mma_done;
   uint64_t kv_full[kStages];
@@ -225,12 +228,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc256_kernel(const __grid
   if (threadIdx.x == 0) {
     mbar_init(&bar->q_full, 1);
     mbar_init(&bar->q_empty, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kLook; ++i) {
       mbar_init(&bar->s_full[i], 1);
       mbar_init(&bar->p_full[i], kBM);
+      mbar_init(&bar->pv_done[i], 1);
     }
-    mbar_init(&bar->pv_done[0], 1);
-    mbar_init(&bar->pv_done[1], 1);
     mbar_init(&bar->o_full, 1);
     mbar_init(&bar->o_empty, kBM);
     mbar_init(&bar->mma_done, 1);
@@ -294,15 +296,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc256_kernel(const __grid
       if (idx < 0) break;
       // the first K/V loads need only ring slots; Q waits until the previous item's last S MMA
       const int n_early = min(2 * w.nt, kEarlyLoads);
+      int kn = 0, vn = 0;  // K and V tiles of the item loaded so far, in the MMA warp's order
       for (int i = 0; i < 2 * w.nt; ++i, ++nload) {
         if (i == n_early && !(ok = load_q(w))) break;
+        const bool is_k = kn < w.nt && kn < vn + kLook;
         const int slot = nload % kStages;
         const int round = nload / kStages;
         if (round > 0 && !(ok = vote(mbar_wait(&bar->kv_empty[slot], (round - 1) & 1, tmo, abort)))) break;
         mbar_arrive_expect_tx(&bar->kv_full[slot], kTileBytes);
         for (int at = 0; at < kAtoms; ++at)
-          tma_tile((i & 1) ? &a.tm_v : &a.tm_k, w, sRing + slot * kTileBytes + at * (kBN * 128), &bar->kv_full[slot],
-                   at, (w.j0 + (i >> 1)) * kBN, false);
+          tma_tile(is_k ? &a.tm_k : &a.tm_v, w, sRing + slot * kTileBytes + at * (kBN * 128), &bar->kv_full[slot],
+                   at, (w.j0 + (is_k ? kn : vn)) * kBN, false);
+        if (is_k)
+          ++kn;
+        else
+          ++vn;
       }
       if (ok && n_early == 2 * w.nt) ok = load_q(w);
     }
@@ -324,8 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc256_kernel(const __grid
     const uint32_t tO = tbase + kColO;
     int nload = 0;   // K/V tiles consumed, over all items
     int items = 0;   // items started
-    int ns = 0;      // S MMAs issued, over all items (S buffer = ns & 1)
-    int npv = 0;     // PV groups issued, over all items (P of PV n is in S buffer n & 1)
+    int ns = 0;      // S MMAs issued, over all items (S buffer ns % kLook)
+    int npv = 0;     // PV groups issued, over all items (P of PV n is in S buffer n % kLook)
     int ou = 0;      // items whose O accumulator was used
     int s_left = 0;  // S MMAs still to issue in the current item
     bool ok = true;
@@ -334,9 +342,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc256_kernel(const __grid
       tc_fence_after();
       return r;
     };
-    auto issue_s = [&](int i) {  // S into buffer ns & 1 from K in the slot of load i
-      mma_s(tbase + kColS + 64 * (ns & 1), q_lo, k_lo + (i % kStages) * slot_step, hi, idesc_qk);
-      umma_commit(&bar->s_full[ns & 1]);
+    auto issue_s = [&](int i) {  // S into buffer ns % kLook from K in the slot of load i
+      mma_s(tbase + kColS + 64 * (ns % kLook), q_lo, k_lo + (i % kStages) * slot_step, hi, idesc_qk);
+      umma_commit(&bar->s_full[ns % kLook]);
       ++ns;
       if (--s_left == 0) umma_commit(&bar->q_empty);  // last read of the Q tile issued
       umma_commit(&bar->kv_empty[i % kStages]);
@@ -355,34 +363,30 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc256_kernel(const __grid
       const int base = nload;
       s_left = nt;
       if (nt == 0) umma_commit(&bar->q_empty);
-      if (nt > 0) {
-        if (!(ok = wait_load(base))) break;
-        issue_s(base);
-      }
-      if (nt > 1) {
-        if (!(ok = wait_load(base + 2))) break;
-        issue_s(base + 2);
-      }
-      for (int j = 0; j < nt; ++j) {
-        const int iv = base + 2 * j + 1;
-        if (!(ok = wait_load(iv))) break;
+      // the item's 2 nt loads in the order the producer issued them: K tile kn while
+      // kn < vn + kLook (S of the next kLook - 1 tiles ahead of each PV), else V tile vn
+      int kn = 0, vn = 0;
+      for (int p = 0; p < 2 * nt; ++p) {
+        const int i = base + p;
+        if (!(ok = wait_load(i))) break;
+        if (kn < nt && kn < vn + kLook) {
+          issue_s(i);  // into the buffer whose P the PV kLook steps back read (in-order tensor pipe)
+          ++kn;
+          continue;
+        }
         // the item's first PV overwrites O: the previous item's epilogue must have read it
-        if (j == 0 && ou > 0 && !(ok = vote(mbar_wait(&bar->o_empty, (ou - 1) & 1, tmo, abort)))) break;
-        if (!(ok = vote(mbar_wait(&bar->p_full[npv & 1], (npv >> 1) & 1, tmo, abort)))) break;
+        if (vn == 0 && ou > 0 && !(ok = vote(mbar_wait(&bar->o_empty, (ou - 1) & 1, tmo, abort)))) break;
+        if (!(ok = vote(mbar_wait(&bar->p_full[npv % kLook], (npv / kLook) & 1, tmo, abort)))) break;
         tc_fence_after();
-        mma_pv(tO, tbase + kColS + 64 * (npv & 1), v_lo + (iv % kStages) * slot_step, hi, idesc_pv, j > 0);
-        umma_commit(&bar->pv_done[npv & 1]);
+        mma_pv(tO, tbase + kColS + 64 * (npv % kLook), v_lo + (i % kStages) * slot_step, hi, idesc_pv, vn > 0);
+        umma_commit(&bar->pv_done[npv % kLook]);
         ++npv;
-        umma_commit(&bar->kv_empty[iv % kStages]);
-        if (j == nt - 1) {
+        umma_commit(&bar->kv_empty[i % kStages]);
+        if (vn == nt - 1) {
           umma_commit(&bar->o_full);
           ++ou;
         }
-        if (j + 2 < nt) {
-          const int ik = base + 2 * (j + 2);
-          if (!(ok = wait_load(ik))) break;
-          issue_s(ik);  // into the buffer PV(j) has just read (in-order tensor pipe)
-        }
+        ++vn;
       }
       if (!ok) break;
       nload += 2 * nt;
@@ -398,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc256_kernel(const __grid
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const uint32_t tO = tbase + lane_base + kColO;
     const float sl2 = a.scale_log2;
-    int gs = 0;     // key steps done by this CTA, over all items: S buffer gs & 1, PV index gs
+    int gs = 0;     // key steps done by this CTA, over all items: S buffer gs % kLook, PV index gs
     int oused = 0;  // items whose O accumulator was used
     bool ok = true;
     for (int k = 0; ok; ++k) {
@@ -414,9 +418,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc256_kernel(const __grid
       const int lo = kWindow ? q_row + (w.nk - w.nq) + 1 - a.window : 0;  // first key in the window
       float m_ref = -INFINITY, l = 0.f;
       for (int j = 0; j < w.nt; ++j) {
-        const int b = gs & 1;
+        const int b = gs % kLook;
         const uint32_t tS = tbase + lane_base + kColS + 64 * b;
-        if (!(ok = vote(mbar_wait(&bar->s_full[b], (gs >> 1) & 1, tmo, abort)))) break;
+        if (!(ok = vote(mbar_wait(&bar->s_full[b], (gs / kLook) & 1, tmo, abort)))) break;
         tc_fence_after();
         uint32_t s0[32], s1[32];
         tmem_ld32(tS, s0);
@@ -477,7 +481,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc256_kernel(const __grid
         exp_half(s1, 16);
         // o takes the new reference max before PV(j) adds to it (rare); PV(j-1) must be done
         if (__any_sync(0xffffffffu, alpha_o != 1.f)) {
-          if (!(ok = vote(mbar_wait(&bar->pv_done[(gs - 1) & 1], ((gs - 1) >> 1) & 1, tmo, abort)))) break;
+          if (!(ok = vote(mbar_wait(&bar->pv_done[(gs - 1) % kLook], ((gs - 1) / kLook) & 1, tmo, abort))))
+            break;
           tc_fence_after();
 #pragma unroll 1
           for (int c = 0; c < kD / 32; ++c) {
