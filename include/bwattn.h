@@ -68,7 +68,9 @@ extern "C" {
  *   lse  : [B, Hq, Nq] fp32, may be NULL
  *   causal: 0 = no mask (cross attention), 1 = causal aligned to the end
  *   scale: multiplies q.k before the softmax; must be finite and > 0
- *   dtype: BWATTN_DTYPE_BF16 (tcgen05 tensor-core kernel, d in {64, 128}) or
+ *   dtype: BWATTN_DTYPE_BF16 (tcgen05 tensor-core kernel, d in {64, 128, 256}: the fast
+ *          kernels' head dims, "Production implications"; d = 256 keeps one query tile per
+ *          CTA because its fp32 O tile fills half of tensor memory) or
  *          BWATTN_DTYPE_FP32 (fp32 FMA kernel, d in {64, 128})
  * Query head h reads KV head h / (Hq / Hkv). Nq = 0 or B = 0 is a valid no-op; Nk = 0 gives
  * O = 0 and LSE = -inf. Errors: INVALID_ARG for null / misaligned pointers, negative sizes,
@@ -246,7 +248,7 @@ size_t attn_varlen_workspace_size(int num_seqs, int max_seqlen_k, int Hq, int Hk
  *   workspace    : device buffer of at least attn_varlen_workspace_size(...) bytes
  * Sequences whose n_q * (Hq / Hkv) <= 32 run on the split-K decode kernel (all query heads
  * of a KV group packed in one tile); the others run on the tcgen05 prefill kernel.
- * Supported: d in {64, 128}, 1 <= g <= 32. Errors as for attn_decode.
+ * Supported: d in {64, 128, 256}, 1 <= g <= 32. Errors as for attn_decode.
  */
 int attn_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens_q,
                 const int32_t* cu_seqlens_k, int num_seqs, int total_q, int total_k, int max_seqlen_q,
