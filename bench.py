@@ -3,9 +3,9 @@
 Headline workload: causal bf16 prefill, B=4, 32 heads, Nq = Nk = 4096, d = 128 (outputs O bf16 and
 fp32 LSE), measured as prefill TFLOP/s with causal FLOPs counted as half (4*d*Nq*Nk/2 per head).
 The same line carries the decode KV-cache GB/s of the decode workloads (contiguous and paged), the
-sliding-window prefill and the varlen append workload in ``breakdown``, each with its own roofline,
-so that one run covers every step of the path (prefill tiles, split-K decode + merge, paged
-gather, window, varlen dispatch).
+sliding-window prefill, the varlen append workload and the head-dim-256 prefill and decode in
+``breakdown``, each with its own roofline, so that one run covers every step of the path (prefill
+tiles, split-K decode + merge, paged gather, window, varlen dispatch, both d = 256 kernels).
 
 Timing: W untimed warm-up steps, then K steps bracketed by a barrier and a device synchronize,
 CUDA events on the launching stream; every workload's inputs are larger than L2 (129 MB), so no
@@ -344,6 +344,17 @@ def run_case(args, world, stream, dev, peaks):
                          "launches": n}
             del x, ws
             torch.cuda.empty_cache()
+    elif args.case == "d256":
+        w = wl.WORKLOADS["prefill_causal_b4_h16_n4096_d256"]
+        B = args.batch or w.B
+        q, k, v = wl.prefill_inputs(B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, torch.bfloat16, w.seed, device=dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, w.Hq, w.Nq), dtype=torch.float32, device=dev)
+        per, n = time_steps(lambda: bw.attn_fwd(q, k, v, causal=True, out=o, lse=lse), args.steps, args.warmup,
+                            world, stream)
+        ms = statistics.mean(per)
+        out.update({"B": B, "d": w.d, "ms": ms, "tflops": rl.prefill_flops(B, w.Hq, w.Nq, w.Nk, w.d, True) / ms / 1e9,
+                    "launches": n})
     else:
         x = wl.make("varlen_append_64seq_h32x8_d128", device=dev)
         cq, ck = x["cu_q"].to(dev), x["cu_k"].to(dev)
@@ -371,7 +382,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-breakdown", action="store_true")
     ap.add_argument("--case", default="all",
-                    choices=["all", "prefill", "window", "decode", "paged", "fp8", "varlen"],
+                    choices=["all", "prefill", "window", "decode", "paged", "fp8", "varlen", "d256"],
                     help="profiling aid: run one part only (no e2e, no CPU baseline)")
     ap.add_argument("--batch", type=int, default=0, help="profiling aid: override the prefill batch size")
     args = ap.parse_args()
@@ -516,6 +527,38 @@ def main():
                          "frac": t_roof / (msv * 1e-3),
                          "note": "sum over sequences of max(FLOPs/peak_bf16, bytes/peak_hbm) over measured time"}}
         del xv, ov, lv, wsv
+        torch.cuda.empty_cache()
+        # head dim 256: its own one-tile prefill instance and the warp-pair decode
+        x2 = wl.make("prefill_causal_b4_h16_n4096_d256", device=dev)
+        w2 = x2["w"]
+        o2 = torch.empty_like(x2["q"])
+        l2 = torch.empty((w2.B, w2.Hq, w2.Nq), dtype=torch.float32, device=dev)
+        fn = lambda: bw.attn_fwd(x2["q"], x2["k"], x2["v"], causal=True, out=o2, lse=l2)  # noqa: E731
+        per2, _ = time_steps(fn, args.steps, args.warmup, world, stream)
+        ms2 = max_over_ranks(statistics.mean(per2), world)
+        f2 = rl.prefill_flops(w2.B, w2.Hq, w2.Nq, w2.Nk, w2.d, True)
+        t2 = f2 / (ms2 * 1e-3) / 1e12
+        breakdown[w2.name] = {"metric": "prefill TFLOP/s (head dim 256)", "value": t2 * world, "unit": "TFLOP/s",
+                              "ms_per_step": ms2, "flops_per_step": f2,
+                              "roofline": {"bound": "tensor", "achieved": t2, "peak": peaks["bf16_tflops"],
+                                           "unit": "TFLOP/s", "frac": t2 / peaks["bf16_tflops"], "traffic": None}}
+        del x2, o2, l2
+        torch.cuda.empty_cache()
+        x3 = wl.make("decode_gqa_b8_h32x8_n16384_d256", device=dev)
+        w3 = x3["w"]
+        nk3 = x3["nk"].to(dev)
+        ws3 = torch.empty(bw.decode_workspace_size(w3.B, w3.Hq, w3.d, w3.num_splits), dtype=torch.uint8, device=dev)
+        fn = lambda: bw.attn_decode(x3["q"], x3["kcache"], x3["vcache"], nk3, w3.num_splits,  # noqa: E731
+                                    workspace=ws3)
+        per3, _ = time_steps(fn, args.steps, args.warmup, world, stream)
+        ms3 = max_over_ranks(statistics.mean(per3), world)
+        kv3 = rl.decode_kv_bytes([w3.Nk] * w3.B, w3.Hkv, w3.d)
+        g3 = kv3 / (ms3 * 1e-3) / 1e9
+        breakdown[w3.name] = {"metric": "decode KV-cache GB/s (head dim 256)", "value": g3 * world, "unit": "GB/s",
+                              "ms_per_step": ms3, "num_splits": w3.num_splits,
+                              "roofline": {"bound": "hbm", "achieved": g3, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                           "frac": g3 / peaks["hbm_gbs"], "algorithmic_bytes": kv3, "traffic": None}}
+        del x3, nk3, ws3
         torch.cuda.empty_cache()
 
     cpu = None

@@ -24,6 +24,10 @@ Workloads (names give their sizes):
 * ``varlen_append_64seq_h32x8_d128``: 64 sequences with KV length ~ U[1024, 16384] and new
   query count uniform over {1, 4, 8, 512}, packed with cu_seqlens, 32 query heads over 8
   KV heads, d = 128, bf16 N(0, 1), causal aligned to each sequence's end.
+* ``prefill_causal_b4_h16_n4096_d256`` and ``decode_gqa_b8_h32x8_n16384_d256``: the prefill and
+  the GQA decode at head dim 256 (the pages' third fast head dim), with the same bytes as their
+  d = 128 counterparts (half the heads or half the keys); the decode takes 8 splits, 2048 keys
+  each, as the d = 128 decode does.
 """
 from __future__ import annotations
 
@@ -38,6 +42,7 @@ SEED_DECODE_LONG = 1004
 SEED_VARLEN = 1005
 SEED_FP8_GQA = 1006
 SEED_FP8_LONG = 1007
+SEED_D256 = 1008
 # FP8 caches: N(0, 1) draws are quantised with 448 / 4.5 codes per unit, so |z| up to 4.5 is
 # representable and larger draws saturate at the largest code
 FP8_SIGMAS = 4.5
@@ -108,6 +113,12 @@ WORKLOADS = {
     "varlen_append_64seq_h32x8_d128": Workload("varlen_append_64seq_h32x8_d128", "varlen", torch.bfloat16,
                                                Hq=32, Hkv=8, d=128, causal=True, seed=SEED_VARLEN,
                                                num_seqs=64, nk_range=(1024, 16384)),
+    "prefill_causal_b4_h16_n4096_d256": Workload("prefill_causal_b4_h16_n4096_d256", "fwd", torch.bfloat16,
+                                                 B=4, Hq=16, Hkv=16, Nq=4096, Nk=4096, d=256, causal=True,
+                                                 seed=SEED_D256),
+    "decode_gqa_b8_h32x8_n16384_d256": Workload("decode_gqa_b8_h32x8_n16384_d256", "decode", torch.bfloat16,
+                                                B=8, Hq=32, Hkv=8, Nq=1, Nk=16384, d=256, causal=False,
+                                                num_splits=8, seed=SEED_D256),
 }
 
 
