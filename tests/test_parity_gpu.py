@@ -432,6 +432,7 @@ def test_varlen_workload_full_size_sampled_rows():
     (5, 4, 2, 300, 513, 64, torch.bfloat16, True),      # 10 units -> 5 chunks of 2
     (3, 2, 1, 200, 333, 128, torch.bfloat16, False),    # pageable host memory
     (1, 1, 1, 512, 512, 64, torch.float32, True),       # the fp32 path
+    (3, 4, 2, 333, 700, 256, torch.bfloat16, True),     # head dim 256: 6 units, one per chunk
 ])
 def test_fwd_host_matches_device_call(B, Hq, Hkv, Nq, Nk, d, dtype, pinned):
     q, k, v = wl.prefill_inputs(B, Hq, Hkv, Nq, Nk, d, dtype, seed=61 + Nq)

@@ -61,6 +61,8 @@ def test_static_decode_matches_workspace_decode_twice(static_fn):
         dict(B=1, Hq=64, Hkv=8, cap=20000, nk=[19999], S=96, seed=72),
         # head dim 64 over the same array
         dict(B=3, Hq=16, Hkv=2, cap=3000, nk=[3000, 5, 1234], S=24, seed=73, d=64),
+        # head dim 256 (warp pairs) over the same array
+        dict(B=2, Hq=16, Hkv=4, cap=5000, nk=[5000, 777], S=12, seed=74, d=256),
     ]
     for c in cases:
         q, kc, vc, nk = wl.decode_inputs(c["B"], c["Hq"], c["Hkv"], c["cap"], c.get("d", 128), torch.bfloat16,
