@@ -49,10 +49,10 @@ PROFILED_TRAFFIC = {
         "exact_attention_flashattn_gb300/csrc/prefill_tc.cu",
         "exact_attention_flashattn_gb300/csrc/ptx.cuh",
     ],
-    "sha256": "c4ff20d4fed3c25cc0dd97c0bc039b0b5451149a0004d2f6c2f5fda2c7e7e230",
-    # (201.54 MB read + 45.60 MB written) at B=2 (profiles/prefill_tc_b2_h32_n4096_d128.md),
+    "sha256": "dc72bbaa1ef1e5d681df8034659c6f2f629b24d008fb8d9eab93f86e28956fb8",
+    # (201.56 MB read + 45.74 MB written) at B=2 (profiles/prefill_tc_b2_h32_n4096_d128.md),
     # scaled x2 to the B=4 launch: traffic grows with the number of (batch, head) units
-    "bytes_per_launch": 494269440,
+    "bytes_per_launch": 494615552,
 }
 METRIC = "prefill TFLOP/s and decode KV GB/s, 1×GB300, as fraction of roofline"
 L2_BYTES = 129 * 1024 * 1024

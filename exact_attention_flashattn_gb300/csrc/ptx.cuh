@@ -116,9 +116,11 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor (128-byte swizzle) in two halves: the low word carries the start
-// address (>> 4) and the leading-dimension offset; the high word the stride offset, version and
-// swizzle mode. Within one swizzle-aligned tile, moving the start address only changes the low word.
+// Shared-memory matrix descriptor for tcgen05.mma, 128-byte swizzle (the layout TMA writes with
+// CU_TENSOR_MAP_SWIZZLE_128B), in two 32-bit halves. Low word: start address >> 4 (bits 0-13) and
+// leading-dimension byte offset >> 4 (bits 16-29); high word: stride-dimension byte offset >> 4
+// (descriptor bits 32-45), version 1 (bits 46-47), base offset 0, swizzle mode 2 = 128B (bits
+// 61-63). Within one swizzle-aligned tile, moving the start address only changes the low word.
 //
 // The MMA and commit wrappers below are called by a whole converged warp with warp-uniform
 // operands: one lane, chosen by elect.sync (the same lane on every call of a full warp), issues
@@ -280,20 +282,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 
-// Shared-memory matrix descriptor for tcgen05.mma, 128-byte swizzle (the layout TMA writes
-// with CU_TENSOR_MAP_SWIZZLE_128B). Fields: start address >> 4 (bits 0-13), leading-dimension
-// byte offset >> 4 (bits 16-29), stride-dimension byte offset >> 4 (bits 32-45), descriptor
-// version 1 (bits 46-47), base offset 0, swizzle mode 2 = 128B (bits 61-63).
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
-  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
-  d |= static_cast<uint64_t>(1) << 46;
-  d |= static_cast<uint64_t>(2) << 61;
-  return d;
-}
-
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A bf16 (bits 7-9 = 1), B bf16
 // (bits 10-12 = 1), A major (bit 15), B major (bit 16; 1 = MN-major), N >> 3 (bits 17-22),
 // M >> 4 (bits 24-28).
@@ -322,17 +310,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
-}
-
-__device__ __forceinline__ uint32_t elect_one_sync() {
-  uint32_t pred = 0;
-  asm volatile(
-      "{\n\t.reg .b32 rx;\n\t.reg .pred px;\n\t"
-      "elect.sync rx|px, %1;\n\t"
-      "@px mov.s32 %0, 1;\n\t}\n"
-      : "+r"(pred)
-      : "r"(0xffffffffu));
-  return pred;
 }
 
 }  // namespace bw
