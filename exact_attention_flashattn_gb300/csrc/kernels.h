@@ -86,9 +86,9 @@ struct MergeArgs {
 };
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
 
-// ---- tcgen05 prefill (bf16, d in {64, 128}) ----
+// ---- tcgen05 prefill (bf16, d in {64, 128, 256}) ----
 struct TcFwdArgs {
-  CUtensorMap tm_q, tm_k, tm_v;  // 3-D maps, box {64, 1 or 128, ...}, 128-byte swizzle
+  CUtensorMap tm_q, tm_k, tm_v;  // 3-D maps, box {64, 1 or 128 (d = 256 K/V: 64), ...}, 128-byte swizzle
   uint16_t* o;
   float* lse;
   const int32_t* cu_q;  // varlen (packed) mode if non-null
@@ -96,7 +96,7 @@ struct TcFwdArgs {
   int B, Hq, Hkv, Nq, Nk, d, causal;  // packed mode: Nq, Nk = total rows of q and k
   int num_seqs;
   int small_rows_limit;  // varlen: sequences with n_q * g <= this are skipped here
-  int max_pairs;         // grid.x: pairs of 128-row query tiles per (sequence, head)
+  int max_pairs;         // work items per (sequence, head): pairs of 128-row query tiles (d = 256: tiles)
   int window;            // > 0: sliding window of that many keys ending at the causal limit
   int band_units;        // (sequence, head) units per band of the item list (at least 1)
   float scale_log2;
