@@ -355,6 +355,15 @@ def run_case(args, world, stream, dev, peaks):
         ms = statistics.mean(per)
         out.update({"B": B, "d": w.d, "ms": ms, "tflops": rl.prefill_flops(B, w.Hq, w.Nq, w.Nk, w.d, True) / ms / 1e9,
                     "launches": n})
+    elif args.case == "d256_decode":
+        x = wl.make("decode_gqa_b8_h32x8_n16384_d256", device=dev)
+        wd = x["w"]
+        nk = x["nk"].to(dev)
+        ws = torch.empty(bw.decode_workspace_size(wd.B, wd.Hq, wd.d, wd.num_splits), dtype=torch.uint8, device=dev)
+        per, n = time_steps(lambda: bw.attn_decode(x["q"], x["kcache"], x["vcache"], nk, wd.num_splits, workspace=ws),
+                            args.steps, args.warmup, world, stream)
+        ms = statistics.mean(per)
+        out[wd.name] = {"ms": ms, "GB/s": rl.decode_kv_bytes([wd.Nk] * wd.B, wd.Hkv, wd.d) / ms / 1e6, "launches": n}
     else:
         x = wl.make("varlen_append_64seq_h32x8_d128", device=dev)
         cq, ck = x["cu_q"].to(dev), x["cu_k"].to(dev)
@@ -382,7 +391,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-breakdown", action="store_true")
     ap.add_argument("--case", default="all",
-                    choices=["all", "prefill", "window", "decode", "paged", "fp8", "varlen", "d256"],
+                    choices=["all", "prefill", "window", "decode", "paged", "fp8", "varlen", "d256", "d256_decode"],
                     help="profiling aid: run one part only (no e2e, no CPU baseline)")
     ap.add_argument("--batch", type=int, default=0, help="profiling aid: override the prefill batch size")
     args = ap.parse_args()
