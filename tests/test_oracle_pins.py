@@ -181,10 +181,10 @@ def test_brute_force_rectangular_bottom_right():
 # ---------------------------------------------------------------- closed forms
 
 
+@pytest.mark.parametrize("d", [8, 256])
 @pytest.mark.parametrize("nq,nk,causal", [(8, 8, True), (5, 11, True), (8, 8, False), (1, 33, False)])
-def test_zero_queries_give_mean_of_visible_values(nq, nk, causal):
+def test_zero_queries_give_mean_of_visible_values(nq, nk, causal, d):
     r = rng(10)
-    d = 8
     q = np.zeros((1, 1, nq, d))
     k, v = randn(r, 1, 1, nk, d), randn(r, 1, 1, nk, d)
     for method, kw in (("naive", {}), ("tiled", {"block": 3}), ("splitk", {"workers": 4})):
