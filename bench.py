@@ -54,20 +54,33 @@ PROFILED_TRAFFIC = {
     # scaled x2 to the B=4 launch: traffic grows with the number of (batch, head) units
     "bytes_per_launch": 494615552,
 }
+PROFILED_TRAFFIC_D256 = {
+    # the head-dim-256 prefill kernel and its PTX wrappers, hashed in this order
+    "kernel_sources": [
+        "exact_attention_flashattn_gb300/csrc/prefill_tc256.cu",
+        "exact_attention_flashattn_gb300/csrc/ptx.cuh",
+    ],
+    "sha256": "6d5fa9d7d8a7c85ae7968d7023396663fc3c72c0aaacf79d3cd4b31df0d120ea",
+    # (282.69 MB read + 45.45 MB written) at B=2 (profiles/prefill_tc256_b2_h16_n4096_d256.md),
+    # scaled x2 to the B=4 launch of prefill_causal_b4_h16_n4096_d256
+    "bytes_per_launch": 656267264,
+}
 METRIC = "prefill TFLOP/s and decode KV GB/s, 1×GB300, as fraction of roofline"
 L2_BYTES = 129 * 1024 * 1024
 
 
-def profiled_traffic():
+def profiled_traffic(spec=None):
+    """Measured DRAM bytes per launch of a profiled kernel, or None once its sources changed."""
     import hashlib
+    spec = PROFILED_TRAFFIC if spec is None else spec
     h = hashlib.sha256()
-    for rel in PROFILED_TRAFFIC["kernel_sources"]:
+    for rel in spec["kernel_sources"]:
         p = os.path.join(ROOT, rel)
         if not os.path.exists(p):
             return None
         with open(p, "rb") as f:
             h.update(f.read())
-    return PROFILED_TRAFFIC["bytes_per_launch"] if h.hexdigest() == PROFILED_TRAFFIC["sha256"] else None
+    return spec["bytes_per_launch"] if h.hexdigest() == spec["sha256"] else None
 
 
 def load_peaks():
@@ -550,7 +563,8 @@ def main():
         breakdown[w2.name] = {"metric": "prefill TFLOP/s (head dim 256)", "value": t2 * world, "unit": "TFLOP/s",
                               "ms_per_step": ms2, "flops_per_step": f2,
                               "roofline": {"bound": "tensor", "achieved": t2, "peak": peaks["bf16_tflops"],
-                                           "unit": "TFLOP/s", "frac": t2 / peaks["bf16_tflops"], "traffic": None}}
+                                           "unit": "TFLOP/s", "frac": t2 / peaks["bf16_tflops"],
+                                           "traffic": profiled_traffic(PROFILED_TRAFFIC_D256)}}
         del x2, o2, l2
         torch.cuda.empty_cache()
         x3 = wl.make("decode_gqa_b8_h32x8_n16384_d256", device=dev)
