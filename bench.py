@@ -50,7 +50,7 @@ PROFILED_TRAFFIC = {
         "exact_attention_flashattn_gb300/csrc/ptx.cuh",
     ],
     "sha256": "dc72bbaa1ef1e5d681df8034659c6f2f629b24d008fb8d9eab93f86e28956fb8",
-    # (201.56 MB read + 45.74 MB written) at B=2 (profiles/prefill_tc_b2_h32_n4096_d128.md),
+    # (201.56 MB read + 45.74 MB written) at B=2, from the ncu capture summarised under profiles/,
     # scaled x2 to the B=4 launch: traffic grows with the number of (batch, head) units
     "bytes_per_launch": 494615552,
 }
@@ -61,7 +61,7 @@ PROFILED_TRAFFIC_D256 = {
         "exact_attention_flashattn_gb300/csrc/ptx.cuh",
     ],
     "sha256": "6d5fa9d7d8a7c85ae7968d7023396663fc3c72c0aaacf79d3cd4b31df0d120ea",
-    # (282.69 MB read + 45.45 MB written) at B=2 (profiles/prefill_tc256_b2_h16_n4096_d256.md),
+    # (282.69 MB read + 45.45 MB written) at B=2, from the ncu capture summarised under profiles/,
     # scaled x2 to the B=4 launch of prefill_causal_b4_h16_n4096_d256
     "bytes_per_launch": 656267264,
 }
