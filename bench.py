@@ -28,6 +28,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import torch
@@ -143,7 +144,8 @@ class ClockSampler:
     def __init__(self, device_index):
         self.dev = device_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
+        # raw samples go to the temp directory; the bench line carries their summary
+        self.path = os.path.join(tempfile.gettempdir(), f"bwattn_bench_clocks_rank{device_index}_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
