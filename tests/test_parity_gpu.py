@@ -694,20 +694,6 @@ def test_prefill_d256(B, Hq, Hkv, Nq, Nk, causal):
     check_bf16(o, o_ref, lse, lse_ref, what=("d256", B, Hq, Hkv, Nq, Nk, causal))
 
 
-def test_prefill_d256_growing_max_rescales_o():
-    # keys grow along the sequence, so every row's running max rises by far more than 2^8 at
-    # later K/V tiles: o is rescaled in tensor memory after the previous P.V has completed
-    q, k, v = wl.prefill_inputs(1, 2, 2, 256, 1024, 256, torch.bfloat16, seed=331)
-    q = q.abs()
-    grow = torch.linspace(0.2, 6.0, 1024, dtype=torch.float32)[None, None, :, None]
-    k = (k.float().abs() * grow).to(torch.bfloat16)
-    o_ref, lse_ref = oracle.attention(f64(q), f64(k), f64(v), False, method="tiled", block=128)
-    o, lse = bw.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=False)
-    torch.cuda.synchronize()
-    # the scores reach several hundred: the LSE carries their bf16 rounding, relative to its size
-    check_bf16(o, o_ref, lse, lse_ref, what="d256 growing max", lse_tol=2e-3 * np.maximum(1.0, np.abs(lse_ref)))
-
-
 def test_prefill_d256_masked_keys_are_never_read():
     q, k, v = wl.prefill_inputs(1, 2, 2, 300, 300, 256, torch.bfloat16, seed=341)
     o1, l1 = bw.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True)
@@ -761,6 +747,149 @@ def test_prefill_d256_long_sampled_rows():
         assert e.max() <= TOL_BF16_MAX, (b, h, i, e.max())
         assert abs(float(lse[b, h, i]) - lse_ref[0, 0, 0]) <= TOL_LSE
     assert np.mean(np.concatenate(errs)) <= TOL_BF16_MEAN
+
+
+# ------------------------------------------------------------------ growing running max
+# The recurrence rescales o by exp(m - m_new) whenever a new tile raises a row's max ("Attention
+# from the kernel's side", The online softmax; "Attention kernels", Maths). The tensor-core
+# kernels keep o in TMEM against a lazily moved reference max and rescale it only when the max
+# grows by more than 2^8 (8 log2 units), and N(0, 1) inputs never do that after a row's first
+# key tile. Here |q| and |k| times a factor that rises along each sequence's keys make later
+# key tiles raise the max: by more than 128 log2 units past a row's first visited tile, so a
+# kernel that skipped or misapplied the rescale would overflow fp32 (2^128) or lose o;
+# ``assert_max_grows`` checks that on the inputs. The key tiles are visited in ascending order.
+#
+# With the max growing this steeply the softmax is close to one-hot, so O is close to a single
+# value row: at |v| around 4 the bf16 rounding of the output alone (2^-8 relative) would nearly
+# reach the absolute bar. The values are therefore scaled by 1/4 (O is linear in V; the scores,
+# the running max and the rescale path are unchanged), so that the standard O bars apply.
+V_SCALE = 0.25
+#
+# LSE bar for these large scores (up to a few hundred): the scores are fp32 sums of d exact
+# bf16 products, so each is off by at most d * 2^-23 * scale * sum_c |q_c k_c| (the standard
+# bound for a d-term float sum, with one bit of slack for a truncating accumulator), and the
+# LSE, a 1-Lipschitz function of the scores in the max norm, by at most the largest of these
+# over the row's keys. The bar is 2e-3 plus that bound (the bound reaches about 1e-2 for the
+# d = 256 window case, whose scores reach a few hundred).
+
+KEY_TILE = 128
+LOG2E = 1.4426950408889634
+GROWTH_LOG2 = 200.0
+
+
+def growing(k, key_axis, starts=None, span=None, lo=0.05):
+    """|k| times a factor rising linearly along each sequence's keys (``starts``: packed sequence
+    offsets along ``key_axis``, else one sequence), by enough that a head-dim-d score at scale
+    1/sqrt(d) grows by about GROWTH_LOG2 log2 units over ``span`` keys (default: the sequence)."""
+    d = k.shape[-1]
+    # E[|q_c| |k_c|] = 2 / pi: the score grows by log2(e) * sqrt(d) * 2 / pi per unit of factor
+    per_span = GROWTH_LOG2 / (LOG2E * math.sqrt(d) * 2.0 / math.pi)
+    n = k.shape[key_axis]
+    f = torch.empty(n, dtype=torch.float32)
+    bounds = [0, n] if starts is None else list(starts)
+    for s0, s1 in zip(bounds[:-1], bounds[1:]):
+        m = s1 - s0
+        if m > 0:
+            f[s0:s1] = lo + per_span / (span or m) * torch.arange(m, dtype=torch.float32)
+    shape = [1] * k.dim()
+    shape[key_axis] = n
+    return (k.float().abs() * f.view(shape)).to(k.dtype)
+
+
+def assert_max_grows(q, k, causal, W, need=128.0):
+    """Some row's max over its visible keys exceeds its max over the first key tile the kernel
+    visits for its query tile by more than ``need`` log2 units (dense [B, H, N, d] layout; the
+    first row of each 128-row query tile, whose first visited tile holds its first visible key)."""
+    qd, kd = f64(q), f64(k)
+    B, Hq, Nq, d = qd.shape
+    Hkv, Nk = kd.shape[1], kd.shape[2]
+    g = Hq // Hkv
+    best = 0.0
+    for b in range(B):
+        for h in range(Hq):
+            for r in range(0, Nq, KEY_TILE):
+                hi = min(Nk, r + Nk - Nq + 1) if causal else Nk
+                lo = max(0, hi - W) if W else 0
+                if hi <= lo:
+                    continue
+                s = (kd[b, h // g, lo:hi] @ qd[b, h, r]) / math.sqrt(d)
+                first = min(hi, (lo // KEY_TILE + 1) * KEY_TILE) - lo
+                best = max(best, (s.max() - s[:first].max()) * LOG2E)
+    assert best > need, best
+
+
+def score_bound(q, k):
+    """Per row: d * 2^-23 * scale * max over keys of sum_c |q_c k_c| (dense [B, H, N, d]; all
+    keys, an upper bound of the visible ones)."""
+    qa, ka = np.abs(f64(q)), np.abs(f64(k))
+    B, Hq, Nq, d = qa.shape
+    g = Hq // ka.shape[1]
+    out = np.zeros((B, Hq, Nq))
+    for b in range(B):
+        for h in range(Hq):
+            if ka.shape[2]:
+                out[b, h] = (qa[b, h] @ ka[b, h // g].T).max(axis=1)
+    return d * 2.0 ** -23 / math.sqrt(d) * out
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,causal,W", [
+    (1, 2, 1, 1024, 1024, True, 0),     # causal, 8 query tiles (4 items at d <= 128)
+    (1, 2, 2, 300, 1000, False, 0),     # cross attention, ragged
+    (1, 2, 1, 700, 1500, True, 0),      # bottom-right causal
+    (1, 2, 1, 1024, 1024, True, 600),   # sliding window over several key tiles
+])
+def test_prefill_growing_max_rescales_o(d, B, Hq, Hkv, Nq, Nk, causal, W):
+    q, k, v = wl.prefill_inputs(B, Hq, Hkv, Nq, Nk, d, torch.bfloat16, seed=401 + d + Nq + W)
+    q, v = q.abs(), (v.float() * V_SCALE).to(v.dtype)
+    k = growing(k, 2, span=W or None)
+    assert_max_grows(q, k, causal, W)
+    o_ref, lse_ref = oracle.attention(f64(q), f64(k), f64(v), causal, method="tiled", block=128, window=W)
+    o, lse = bw.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal, window=W)
+    torch.cuda.synchronize()
+    check_bf16(o, o_ref, lse, lse_ref, what=("growing max", d, Nq, Nk, causal, W),
+               lse_tol=TOL_LSE + score_bound(q, k))
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("W", [0, 700])
+def test_varlen_growing_max_rescales_o(d, W):
+    # 300- and 600-query sequences take the packed tensor-core path, the 1..8-query ones split-K;
+    # each sequence's keys grow along its own length
+    nq = [300, 1, 600, 4, 8]
+    nk = [1000, 900, 1200, 800, 700]
+    q, k, v, cq, ck = wl.varlen_inputs(nq, nk, 8, 2, d, torch.bfloat16, seed=431 + d + W)
+    q, v = q.abs(), (v.float() * V_SCALE).to(v.dtype)
+    k = growing(k, 0, starts=ck.tolist(), span=W or None)
+    tol = np.full((q.shape[0], q.shape[1]), TOL_LSE)
+    for s in range(len(nq)):  # dense [1, H, n, d] views of each sequence
+        qs = q[cq[s]:cq[s + 1]].permute(1, 0, 2)[None]
+        ks = k[ck[s]:ck[s + 1]].permute(1, 0, 2)[None]
+        tol[cq[s]:cq[s + 1]] += score_bound(qs, ks)[0].T
+        if s == 0:  # the first long sequence's rows must outgrow the threshold
+            assert_max_grows(qs, ks, True, W)
+    o_ref, lse_ref = oracle.varlen(f64(q), f64(k), f64(v), cq.numpy(), ck.numpy(), True, method="tiled", block=128,
+                                   window=W)
+    o, lse = bw.attn_varlen(q.cuda(), k.cuda(), v.cuda(), cq.cuda(), ck.cuda(), max(nq), max(nk), causal=True,
+                            window=W)
+    torch.cuda.synchronize()
+    check_bf16(o, o_ref, lse, lse_ref, what=("varlen growing max", d, W), lse_tol=tol)
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("Hq,Hkv,S", [(8, 2, 3), (16, 2, 40), (32, 2, 5)])
+def test_decode_growing_max_rescales_o(d, Hq, Hkv, S):
+    # the split-K pass rescales its o in registers when a row's max grows within a split; g = 4
+    # and 8 take the transposed form, g = 16 the 16-row form, 40 splits the separate merge
+    nk = [3000, 1777]
+    q, kc, vc, nkt = wl.decode_inputs(2, Hq, Hkv, 3000, d, torch.bfloat16, seed=461 + d + Hq, nk=nk)
+    q, vc = q.abs(), (vc.float() * V_SCALE).to(vc.dtype)
+    kc = growing(kc, 2)
+    tol = TOL_LSE + score_bound(q[:, :, None], kc)[:, :, 0]
+    o_ref, lse_ref = oracle.decode(f64(q), f64(kc), f64(vc), nkt.numpy(), method="splitk", workers=S)
+    o, lse = bw.attn_decode(q.cuda(), kc.cuda(), vc.cuda(), nkt.cuda(), num_splits=S)
+    torch.cuda.synchronize()
+    check_bf16(o, o_ref, lse, lse_ref, what=("decode growing max", d, Hq, Hkv, S), lse_tol=tol)
 
 
 # ------------------------------------------------------------------ edge cases
