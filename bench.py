@@ -67,6 +67,9 @@ PROFILED_TRAFFIC_D256 = {
     "bytes_per_launch": 656267264,
 }
 METRIC = "prefill TFLOP/s and decode KV GB/s, 1×GB300, as fraction of roofline"
+# nominal GB300 figures, the second roofline basis: HBM3e bandwidth of about 8 TB/s and the dense
+# (no 2:4 sparsity) bf16 tensor-core peak of 2.25 PFLOP/s
+NOMINAL = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0}
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -273,35 +276,103 @@ def run_reference(args, rank, world):
 # ------------------------------------------------------------------ single-part runs (profiling aid)
 
 
-def bench_fp8(name, args, world, stream, dev, peaks):
-    """FP8 (E4M3) KV-cache decode: KV bytes are one per element (plus the [Hkv, d] scales)."""
+def r4(x):
+    """4 significant digits (keeps the bench line short)."""
+    return float(f"{x:.4g}")
+
+
+def roofline_entry(bound, achieved, peaks, unit, **extra):
+    """Roofline object on both bases: the measured peak (MEASURED_PEAKS.json, else the fallback)
+    and the nominal one (8 TB/s HBM3e; 2.25 PFLOP/s dense bf16)."""
+    key = "hbm_gbs" if bound == "hbm" else "bf16_tflops"
+    out = {"bound": bound, "achieved": r4(achieved), "peak": peaks[key], "unit": unit,
+           "frac": r4(achieved / peaks[key]), "peak_nominal": NOMINAL[key],
+           "frac_nominal": r4(achieved / NOMINAL[key])}
+    out.update(extra)
+    return out
+
+
+def decode_call(x, w, nk, ws, o, lse):
+    """The decode entry point of a workload, as a closure over its inputs and outputs."""
+    if w.kind == "decode":
+        return lambda: bw.attn_decode(x["q"], x["kcache"], x["vcache"], nk, w.num_splits, workspace=ws, out=o,
+                                      lse=lse)
+    if w.kind == "decode_paged":
+        return lambda: bw.attn_decode_paged(x["q"], x["k_pages"], x["v_pages"], x["block_table"], nk, w.num_splits,
+                                            workspace=ws, out=o, lse=lse)
+    if w.kind == "decode_fp8":
+        return lambda: bw.attn_decode_fp8(x["q"], x["kcache"], x["vcache"], x["k_scale"], x["v_scale"], nk,
+                                          w.num_splits, workspace=ws, out=o, lse=lse)
+    return lambda: bw.attn_decode_paged_fp8(x["q"], x["k_pages"], x["v_pages"], x["k_scale"], x["v_scale"],
+                                            x["block_table"], nk, w.num_splits, workspace=ws, out=o, lse=lse)
+
+
+def bench_decode(name, args, world, stream, dev, peaks):
+    """Decode KV-cache GB/s: every cached K and V element read once (bf16: 2 bytes, FP8: 1)."""
     x = wl.make(name, device=dev)
     w = x["w"]
     nk = x["nk"].to(dev)
     o = torch.empty_like(x["q"])
     lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
     ws = torch.empty(bw.decode_workspace_size(w.B, w.Hq, w.d, w.num_splits), dtype=torch.uint8, device=dev)
-    if w.kind == "decode_paged_fp8":
-        fn = lambda: bw.attn_decode_paged_fp8(x["q"], x["k_pages"], x["v_pages"], x["k_scale"],  # noqa: E731
-                                              x["v_scale"], x["block_table"], nk, w.num_splits, workspace=ws,
-                                              out=o, lse=lse)
-    else:
-        fn = lambda: bw.attn_decode_fp8(x["q"], x["kcache"], x["vcache"], x["k_scale"], x["v_scale"],  # noqa: E731
-                                        nk, w.num_splits, workspace=ws, out=o, lse=lse)
+    per, _ = time_steps(decode_call(x, w, nk, ws, o, lse), args.steps, args.warmup, world, stream)
+    ms = max_over_ranks(statistics.mean(per), world)
+    fp8 = w.kind.endswith("fp8")
+    kvb = rl.decode_kv_bytes([w.Nk] * w.B, w.Hkv, w.d, elem_bytes=1 if fp8 else 2)
+    gbs = kvb / (ms * 1e-3) / 1e9
+    out = {"GB/s": r4(gbs * world), "ms": r4(ms), "splits": w.num_splits,
+           "roofline": roofline_entry("hbm", gbs, peaks, "GB/s", bytes=kvb)}
+    del x, o, lse, ws, nk
+    torch.cuda.empty_cache()
+    return out
+
+
+def bench_prefill(name, args, world, stream, dev, peaks):
+    """Prefill TFLOP/s of a dense workload (causal counted as half; a window counts its visible
+    pairs exactly)."""
+    w = wl.WORKLOADS[name]
+    x = wl.make(name, device=dev)
+    W = w.extra.get("window", 0)
+    o = torch.empty_like(x["q"])
+    lse = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=dev)
+    fn = lambda: bw.attn_fwd(x["q"], x["k"], x["v"], causal=True, window=W, out=o, lse=lse)  # noqa: E731
     per, _ = time_steps(fn, args.steps, args.warmup, world, stream)
     ms = max_over_ranks(statistics.mean(per), world)
-    kvb = rl.decode_kv_bytes([w.Nk] * w.B, w.Hkv, w.d, elem_bytes=1)
-    gbs = kvb / (ms * 1e-3) / 1e9
-    out = {"metric": "decode KV-cache GB/s (FP8 E4M3 codes)", "value": gbs * world, "unit": "GB/s",
-           "ms_per_step": ms, "num_splits": w.num_splits,
-           "keys_per_s": float(w.Nk) * w.B * w.Hkv * world / (ms * 1e-3),
-           "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                        "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": kvb, "traffic": None,
-                        "note": "split-K pass, codes turned into f16 in registers" +
-                                (", fused merge" if w.num_splits <= 32 else ", separate merge")}}
-    if "page_size" in w.extra:
-        out["page_size"] = w.extra["page_size"]
-    del x, o, lse, ws, nk
+    f = rl.window_prefill_flops(w.B, w.Hq, w.Nq, w.Nk, w.d, W) if W else rl.prefill_flops(w.B, w.Hq, w.Nq, w.Nk,
+                                                                                          w.d, True)
+    t = f / (ms * 1e-3) / 1e12
+    traffic = profiled_traffic(PROFILED_TRAFFIC_D256) if w.d == 256 else None
+    out = {"TFLOP/s": r4(t * world), "ms": r4(ms), "roofline": roofline_entry("tensor", t, peaks, "TFLOP/s",
+                                                                             traffic=traffic)}
+    del x, o, lse
+    torch.cuda.empty_cache()
+    return out
+
+
+def bench_varlen(args, world, stream, dev, peaks):
+    """Varlen append workload: measured time against the sum over sequences of
+    max(FLOPs / bf16 peak, bytes / HBM peak), on both bases."""
+    xv = wl.make("varlen_append_64seq_h32x8_d128", device=dev)
+    wv = xv["w"]
+    cq, ck = xv["cu_q"].to(dev), xv["cu_k"].to(dev)
+    ov = torch.empty_like(xv["q"])
+    lv = torch.empty((xv["q"].shape[0], wv.Hq), dtype=torch.float32, device=dev)
+    mq, mk = max(xv["nq"]), max(xv["nk"])
+    wsv = torch.empty(bw.varlen_workspace_size(wv.num_seqs, mk, wv.Hq, wv.Hkv, wv.d), dtype=torch.uint8, device=dev)
+    fn = lambda: bw.attn_varlen(xv["q"], xv["k"], xv["v"], cq, ck, mq, mk, causal=True,  # noqa: E731
+                                workspace=wsv, out=ov, lse=lv)
+    per, _ = time_steps(fn, args.steps, args.warmup, world, stream)
+    ms = max_over_ranks(statistics.mean(per), world)
+    fv = rl.varlen_flops(xv["nq"], xv["nk"], wv.Hq, wv.d, True)
+    roof = {}
+    for tag, pk in (("", peaks), ("_nominal", NOMINAL)):
+        roof["roofline_ms" + tag] = r4(1e3 * rl.varlen_roofline_seconds(xv["nq"], xv["nk"], wv.Hq, wv.Hkv, wv.d, True,
+                                                                        pk["bf16_tflops"] * 1e12,
+                                                                        pk["hbm_gbs"] * 1e9))
+        roof["frac" + tag] = r4(roof["roofline_ms" + tag] / ms)
+    out = {"TFLOP/s": r4(fv * world / (ms * 1e-3) / 1e12), "ms": r4(ms),
+           "roofline": {"bound": "mixed", **roof}}
+    del xv, ov, lv, wsv
     torch.cuda.empty_cache()
     return out
 
@@ -333,8 +404,7 @@ def run_case(args, world, stream, dev, peaks):
     elif args.case == "fp8":
         for name in ("decode_fp8_gqa_b8_h32x8_n32768_d128", "decode_fp8_paged_b8_h32x8_n32768_d128_p16",
                      "decode_fp8_long_b1_h64x8_n262144_d128"):
-            r = bench_fp8(name, args, world, stream, dev, peaks)
-            out[name] = {"ms": r["ms_per_step"], "GB/s": r["value"], "frac": r["roofline"]["frac"]}
+            out[name] = bench_decode(name, args, world, stream, dev, peaks)
     elif args.case == "paged":
         x = wl.make("decode_paged_b8_h32x8_n32768_d128_p16", device=dev)
         wd = x["w"]
@@ -464,127 +534,21 @@ def main():
     del x, q, k, v, o, lse
     torch.cuda.empty_cache()
 
-    # ---------------- breakdown: decode and varlen workloads
+    # ---------------- breakdown: every other workload, the decode and varlen ones last so that
+    # they sit in the end of the line (compact entries, 4 significant digits)
     breakdown = {}
     if not args.no_breakdown:
-        for name in ("decode_gqa_b8_h32x8_n32768_d128", "decode_long_b1_h64x8_n262144_d128"):
-            xd = wl.make(name, device=dev)
-            wd = xd["w"]
-            nk = xd["nk"].to(dev)
-            od = torch.empty_like(xd["q"])
-            ld = torch.empty((wd.B, wd.Hq), dtype=torch.float32, device=dev)
-            wsd = torch.empty(bw.decode_workspace_size(wd.B, wd.Hq, wd.d, wd.num_splits), dtype=torch.uint8,
-                              device=dev)
-            fn = lambda: bw.attn_decode(xd["q"], xd["kcache"], xd["vcache"], nk, wd.num_splits,  # noqa: E731
-                                        workspace=wsd, out=od, lse=ld)
-            perd, _ = time_steps(fn, args.steps, args.warmup, world, stream)
-            msd = max_over_ranks(statistics.mean(perd), world)
-            kvb = rl.decode_kv_bytes([wd.Nk] * wd.B, wd.Hkv, wd.d)
-            gbs = kvb / (msd * 1e-3) / 1e9
-            breakdown[name] = {"metric": "decode KV-cache GB/s", "value": gbs * world, "unit": "GB/s",
-                               "ms_per_step": msd, "num_splits": wd.num_splits,
-                               "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
-                                            "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
-                                            "algorithmic_bytes": kvb, "traffic": None,
-                                            "note": "split-K pass with the merge fused into the last CTA of each unit"}}
-            del xd, od, ld, wsd, nk
-            torch.cuda.empty_cache()
-        xp = wl.make("decode_paged_b8_h32x8_n32768_d128_p16", device=dev)
-        wp = xp["w"]
-        nkp = xp["nk"].to(dev)
-        wsp = torch.empty(bw.decode_workspace_size(wp.B, wp.Hq, wp.d, wp.num_splits), dtype=torch.uint8, device=dev)
-        op = torch.empty_like(xp["q"])
-        lp = torch.empty((wp.B, wp.Hq), dtype=torch.float32, device=dev)
-        fn = lambda: bw.attn_decode_paged(xp["q"], xp["k_pages"], xp["v_pages"], xp["block_table"], nkp,  # noqa: E731
-                                          wp.num_splits, workspace=wsp, out=op, lse=lp)
-        perp, _ = time_steps(fn, args.steps, args.warmup, world, stream)
-        msp = max_over_ranks(statistics.mean(perp), world)
-        kvb = rl.decode_kv_bytes([wp.Nk] * wp.B, wp.Hkv, wp.d)
-        gbs = kvb / (msp * 1e-3) / 1e9
-        breakdown[wp.name] = {"metric": "decode KV-cache GB/s", "value": gbs * world, "unit": "GB/s",
-                              "ms_per_step": msp, "num_splits": wp.num_splits, "page_size": wp.extra["page_size"],
-                              "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                           "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": kvb,
-                                           "traffic": None, "note": "paged split-K pass with the fused merge"}}
-        del xp, wsp, op, lp, nkp
-        torch.cuda.empty_cache()
+        for name in ("prefill_causal_b4_h16_n4096_d256", "prefill_window_b4_h32_n4096_w1024_d128",
+                     "prefill_causal_b4_h32_n4096_d64"):
+            breakdown[name] = bench_prefill(name, args, world, stream, dev, peaks)
+        breakdown["decode_gqa_b8_h32x8_n16384_d256"] = bench_decode("decode_gqa_b8_h32x8_n16384_d256", args, world,
+                                                                    stream, dev, peaks)
         for name in ("decode_fp8_gqa_b8_h32x8_n32768_d128", "decode_fp8_paged_b8_h32x8_n32768_d128_p16",
-                     "decode_fp8_long_b1_h64x8_n262144_d128"):
-            breakdown[name] = bench_fp8(name, args, world, stream, dev, peaks)
-        xw = wl.make("prefill_window_b4_h32_n4096_w1024_d128", device=dev)
-        ww = xw["w"]
-        W = ww.extra["window"]
-        ow = torch.empty_like(xw["q"])
-        lw = torch.empty((ww.B, ww.Hq, ww.Nq), dtype=torch.float32, device=dev)
-        fn = lambda: bw.attn_fwd(xw["q"], xw["k"], xw["v"], causal=True, window=W, out=ow, lse=lw)  # noqa: E731
-        perw, _ = time_steps(fn, args.steps, args.warmup, world, stream)
-        msw = max_over_ranks(statistics.mean(perw), world)
-        fw = rl.window_prefill_flops(ww.B, ww.Hq, ww.Nq, ww.Nk, ww.d, W)
-        tw = fw / (msw * 1e-3) / 1e12
-        breakdown[ww.name] = {"metric": "window prefill TFLOP/s", "value": tw * world, "unit": "TFLOP/s",
-                              "ms_per_step": msw, "window": W, "flops_per_step": fw,
-                              "flop_convention": "visible (query, key) pairs counted exactly",
-                              "roofline": {"bound": "tensor", "achieved": tw, "peak": peaks["bf16_tflops"],
-                                           "unit": "TFLOP/s", "frac": tw / peaks["bf16_tflops"], "traffic": None}}
-        del xw, ow, lw
-        torch.cuda.empty_cache()
-        xv = wl.make("varlen_append_64seq_h32x8_d128", device=dev)
-        wv = xv["w"]
-        cq, ck = xv["cu_q"].to(dev), xv["cu_k"].to(dev)
-        ov = torch.empty_like(xv["q"])
-        lv = torch.empty((xv["q"].shape[0], wv.Hq), dtype=torch.float32, device=dev)
-        mq, mk = max(xv["nq"]), max(xv["nk"])
-        wsv = torch.empty(bw.varlen_workspace_size(wv.num_seqs, mk, wv.Hq, wv.Hkv, wv.d), dtype=torch.uint8,
-                          device=dev)
-        fn = lambda: bw.attn_varlen(xv["q"], xv["k"], xv["v"], cq, ck, mq, mk, causal=True,  # noqa: E731
-                                    workspace=wsv, out=ov, lse=lv)
-        perv, _ = time_steps(fn, args.steps, args.warmup, world, stream)
-        msv = max_over_ranks(statistics.mean(perv), world)
-        fv = rl.varlen_flops(xv["nq"], xv["nk"], wv.Hq, wv.d, True)
-        bv = rl.varlen_bytes(xv["nq"], xv["nk"], wv.Hq, wv.Hkv, wv.d)
-        t_roof = rl.varlen_roofline_seconds(xv["nq"], xv["nk"], wv.Hq, wv.Hkv, wv.d, True,
-                                            peaks["bf16_tflops"] * 1e12, peaks["hbm_gbs"] * 1e9)
-        breakdown["varlen_append_64seq_h32x8_d128"] = {
-            "metric": "varlen TFLOP/s", "value": fv * world / (msv * 1e-3) / 1e12, "unit": "TFLOP/s",
-            "ms_per_step": msv, "kv_bytes": bv,
-            "roofline": {"bound": "mixed", "achieved_s": msv * 1e-3, "roofline_s": t_roof,
-                         "frac": t_roof / (msv * 1e-3),
-                         "note": "sum over sequences of max(FLOPs/peak_bf16, bytes/peak_hbm) over measured time"}}
-        del xv, ov, lv, wsv
-        torch.cuda.empty_cache()
-        # head dim 256: its own one-tile prefill instance and the warp-pair decode
-        x2 = wl.make("prefill_causal_b4_h16_n4096_d256", device=dev)
-        w2 = x2["w"]
-        o2 = torch.empty_like(x2["q"])
-        l2 = torch.empty((w2.B, w2.Hq, w2.Nq), dtype=torch.float32, device=dev)
-        fn = lambda: bw.attn_fwd(x2["q"], x2["k"], x2["v"], causal=True, out=o2, lse=l2)  # noqa: E731
-        per2, _ = time_steps(fn, args.steps, args.warmup, world, stream)
-        ms2 = max_over_ranks(statistics.mean(per2), world)
-        f2 = rl.prefill_flops(w2.B, w2.Hq, w2.Nq, w2.Nk, w2.d, True)
-        t2 = f2 / (ms2 * 1e-3) / 1e12
-        breakdown[w2.name] = {"metric": "prefill TFLOP/s (head dim 256)", "value": t2 * world, "unit": "TFLOP/s",
-                              "ms_per_step": ms2, "flops_per_step": f2,
-                              "roofline": {"bound": "tensor", "achieved": t2, "peak": peaks["bf16_tflops"],
-                                           "unit": "TFLOP/s", "frac": t2 / peaks["bf16_tflops"],
-                                           "traffic": profiled_traffic(PROFILED_TRAFFIC_D256)}}
-        del x2, o2, l2
-        torch.cuda.empty_cache()
-        x3 = wl.make("decode_gqa_b8_h32x8_n16384_d256", device=dev)
-        w3 = x3["w"]
-        nk3 = x3["nk"].to(dev)
-        ws3 = torch.empty(bw.decode_workspace_size(w3.B, w3.Hq, w3.d, w3.num_splits), dtype=torch.uint8, device=dev)
-        fn = lambda: bw.attn_decode(x3["q"], x3["kcache"], x3["vcache"], nk3, w3.num_splits,  # noqa: E731
-                                    workspace=ws3)
-        per3, _ = time_steps(fn, args.steps, args.warmup, world, stream)
-        ms3 = max_over_ranks(statistics.mean(per3), world)
-        kv3 = rl.decode_kv_bytes([w3.Nk] * w3.B, w3.Hkv, w3.d)
-        g3 = kv3 / (ms3 * 1e-3) / 1e9
-        breakdown[w3.name] = {"metric": "decode KV-cache GB/s (head dim 256)", "value": g3 * world, "unit": "GB/s",
-                              "ms_per_step": ms3, "num_splits": w3.num_splits,
-                              "roofline": {"bound": "hbm", "achieved": g3, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                           "frac": g3 / peaks["hbm_gbs"], "algorithmic_bytes": kv3, "traffic": None}}
-        del x3, nk3, ws3
-        torch.cuda.empty_cache()
+                     "decode_fp8_long_b1_h64x8_n262144_d128", "decode_paged_b8_h32x8_n32768_d128_p16"):
+            breakdown[name] = bench_decode(name, args, world, stream, dev, peaks)
+        breakdown["varlen_append_64seq_h32x8_d128"] = bench_varlen(args, world, stream, dev, peaks)
+        for name in ("decode_long_b1_h64x8_n262144_d128", "decode_gqa_b8_h32x8_n32768_d128"):
+            breakdown[name] = bench_decode(name, args, world, stream, dev, peaks)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -601,7 +565,8 @@ def main():
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": achieved / peaks["bf16_tflops"], "traffic": profiled_traffic(),
-                         "peak_source": f"{peaks['source']} bf16 burst"},
+                         "peak_source": f"{peaks['source']} bf16 burst",
+                         "peak_nominal": NOMINAL["bf16_tflops"], "frac_nominal": achieved / NOMINAL["bf16_tflops"]},
             "e2e": e2e, "gpu_launches": launches, "clocks": clocks, "cpu_baseline": cpu, "breakdown": breakdown,
         }
         print(json.dumps(line))

@@ -16,28 +16,32 @@ namespace {
 
 __device__ unsigned int g_status_word;
 
+constexpr int kMaxDevices = 64;
+
 // Item counters of the persistent prefill kernel: one pair per launch, taken round-robin from
-// this ring, so launches in flight on different streams never share a pair; a launch leaves
-// its pair zeroed when it completes.
+// this ring (one position per device), so launches in flight on different streams never share
+// a pair unless 4096 or more prefill launches are in flight on the device at once; a launch
+// leaves its pair zeroed when it completes.
 constexpr int kSchedSlots = 4096;
 __device__ unsigned int g_sched_counters[2 * kSchedSlots];
-std::atomic<uint32_t> g_sched_next{0};
+std::atomic<uint32_t> g_sched_next[kMaxDevices];
 
 // Merge tickets of the split-K kernel: each launch takes a contiguous block (zeroed, and left
-// zeroed by the kernel) from this ring; the ring holds 2^16 tickets, so blocks are reused only
-// after many later launches.
+// zeroed by the kernel) from this ring (one position per device); the ring holds 2^16 tickets,
+// so a block is handed out again only after 2^16 more tickets have been taken on the device.
+// Launches still in flight by then (other streams, a captured graph replayed alongside) would
+// share it; the header states the limit.
 constexpr uint32_t kTicketSlots = 1u << 16;
 // With more splits than this the separate merge kernel (one CTA per output row) is faster than
 // letting one CTA per unit walk all the splits.
 constexpr int kFusedMergeMaxSplits = 32;
 __device__ unsigned int g_merge_tickets[kTicketSlots];
-uint32_t g_ticket_next = 0;
+uint32_t g_ticket_next[kMaxDevices] = {};
 
 thread_local int t_last_cuda_error = 0;
 std::atomic<uint64_t> g_launches{0};
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 
-constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 unsigned int* g_status_ptr[kMaxDevices] = {};
 unsigned int* g_sched_ptr[kMaxDevices] = {};
@@ -87,7 +91,7 @@ cudaError_t sched_ptr(unsigned int** out) {
     }
     base = g_sched_ptr[dev];
   }
-  *out = base + 2 * (g_sched_next.fetch_add(1) % kSchedSlots);
+  *out = base + 2 * (g_sched_next[dev].fetch_add(1) % kSchedSlots);
   return cudaSuccess;
 }
 
@@ -169,9 +173,9 @@ cudaError_t merge_tickets(int n, unsigned int** out) {
     if (e != cudaSuccess) return e;
     g_ticket_ptr[dev] = static_cast<unsigned int*>(p);
   }
-  uint32_t pos = g_ticket_next;
+  uint32_t pos = g_ticket_next[dev];
   if (pos + static_cast<uint32_t>(n) > kTicketSlots) pos = 0;
-  g_ticket_next = pos + static_cast<uint32_t>(n);
+  g_ticket_next[dev] = pos + static_cast<uint32_t>(n);
   *out = g_ticket_ptr[dev] + pos;
   return cudaSuccess;
 }

@@ -124,9 +124,18 @@ int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* l
     return BWATTN_ERR_CUDA;
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  auto fail = [](cudaError_t err) {
+  // On an error after work was queued, wait for this call's own streams before returning, so
+  // that no copy from or to the caller's host buffers is still running when the caller sees
+  // the error (their status is not reported again: the first error is).
+  auto drain = [&pp](int rc) {
+    for (int i = 0; i < kH2dStreams; ++i) cudaStreamSynchronize(pp.h2d[i]);
+    cudaStreamSynchronize(pp.comp);
+    cudaStreamSynchronize(pp.d2h);
+    return rc;
+  };
+  auto fail = [&drain](cudaError_t err) {
     bw::record_cuda_error(err);
-    return BWATTN_ERR_CUDA;
+    return drain(BWATTN_ERR_CUDA);
   };
   // everything starts after the work already queued on the caller's stream
   if ((e = cudaEventRecord(pp.start, st)) != cudaSuccess) return fail(e);
@@ -169,7 +178,7 @@ int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* l
       if ((e = cudaStreamWaitEvent(pp.comp, pp.h2d_done[c][i], 0)) != cudaSuccess) return fail(e);
     if (c >= kSlots && (e = cudaStreamWaitEvent(pp.comp, pp.d2h_done[c - kSlots], 0)) != cudaSuccess) return fail(e);
     const int rc = attn_fwd(dq, dk, dv, dout, lse ? dl : nullptr, n, p.g, 1, Nq, Nk, d, causal, scale, dtype, pp.comp);
-    if (rc != BWATTN_OK) return rc;
+    if (rc != BWATTN_OK) return drain(rc);
     if ((e = cudaEventRecord(pp.comp_done[c], pp.comp)) != cudaSuccess) return fail(e);
     // copies out
     if ((e = cudaStreamWaitEvent(pp.d2h, pp.comp_done[c], 0)) != cudaSuccess) return fail(e);

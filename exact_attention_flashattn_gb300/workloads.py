@@ -28,6 +28,8 @@ Workloads (names give their sizes):
   the GQA decode at head dim 256 (the pages' third fast head dim), with the same bytes as their
   d = 128 counterparts (half the heads or half the keys); the decode takes 8 splits, 2048 keys
   each, as the d = 128 decode does.
+* ``prefill_causal_b4_h32_n4096_d64``: the causal prefill workload at head dim 64 (the pages'
+  smallest fast head dim), same B, heads and lengths.
 """
 from __future__ import annotations
 
@@ -43,6 +45,7 @@ SEED_VARLEN = 1005
 SEED_FP8_GQA = 1006
 SEED_FP8_LONG = 1007
 SEED_D256 = 1008
+SEED_D64 = 1009
 # FP8 caches: N(0, 1) draws are quantised with 448 / 4.5 codes per unit, so |z| up to 4.5 is
 # representable and larger draws saturate at the largest code
 FP8_SIGMAS = 4.5
@@ -116,6 +119,9 @@ WORKLOADS = {
     "prefill_causal_b4_h16_n4096_d256": Workload("prefill_causal_b4_h16_n4096_d256", "fwd", torch.bfloat16,
                                                  B=4, Hq=16, Hkv=16, Nq=4096, Nk=4096, d=256, causal=True,
                                                  seed=SEED_D256),
+    "prefill_causal_b4_h32_n4096_d64": Workload("prefill_causal_b4_h32_n4096_d64", "fwd", torch.bfloat16,
+                                                B=4, Hq=32, Hkv=32, Nq=4096, Nk=4096, d=64, causal=True,
+                                                seed=SEED_D64),
     "decode_gqa_b8_h32x8_n16384_d256": Workload("decode_gqa_b8_h32x8_n16384_d256", "decode", torch.bfloat16,
                                                 B=8, Hq=32, Hkv=8, Nq=1, Nk=16384, d=256, causal=False,
                                                 num_splits=8, seed=SEED_D256),

@@ -36,6 +36,12 @@
  *     and leaving it reset; the static scratch of attn_decode_static; the streams and events
  *     of attn_fwd_host. Calls are thread-safe and may be captured into CUDA graphs (except
  *     attn_fwd_host).
+ *   - Limit of those rings, per device: a share is handed out again after 4096 further
+ *     prefill launches (item counters) or 65,536 further merge tickets (a fused-merge decode
+ *     takes one ticket per (sequence, KV head, row group)). Calls still running when their
+ *     share comes round again would share it and corrupt each other's scheduling or merge:
+ *     keep fewer launches than that in flight on one device at a time, counting every replay
+ *     of a captured graph that runs concurrently with other calls.
  */
 #ifndef BWATTN_H
 #define BWATTN_H
@@ -94,6 +100,9 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
  *                     it afterwards starts after the last copy out; the host buffers must stay
  *                     valid until then
  * Calls from several host threads are serialised while they enqueue (the streams are shared).
+ * On an error return after copies were queued (a CUDA error part way through), the call first
+ * waits on the host for its own streams, so no copy from or to the host buffers is still
+ * running when it returns; the outputs are then undefined.
  */
 int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
                   int Nk, int d, int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
