@@ -131,11 +131,15 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int d, int64_t dim1, int6
 // Units per band of the prefill item list: as many (sequence, head) units as keep their K and V
 // (one KV head serves g consecutive query heads) within 16 MB, between 16 and 64. Wider bands
 // help short sequences, whose items are many and short (32 units: +5.6 % at 1024 keys, d = 128);
-// from 2048 keys on (d = 128) the band stays at 16, where wider ones measured 1-2 % slower.
+// from 2048 keys on (d = 128) the band stays at 16, where wider ones measured 1-2 % slower. At
+// d = 256 the floor is 8 units: 16 units of 4096 keys hold 64 MB of K/V, and the two bands in
+// flight then no longer fit in L2 (DRAM reads 1.4x the Q, K, V bytes), while 8 units measured
+// as fast.
 int band_units_for(int64_t nk, int d, int g) {
   const int64_t unit_bytes = std::max<int64_t>(1, nk * d * 4 / std::max(g, 1));
   const int64_t b = (static_cast<int64_t>(16) << 20) / unit_bytes;
-  return static_cast<int>(std::min<int64_t>(64, std::max<int64_t>(16, b)));
+  const int64_t floor_units = d == 256 ? 8 : 16;
+  return static_cast<int>(std::min<int64_t>(64, std::max<int64_t>(floor_units, b)));
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -143,6 +147,11 @@ bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0
 bool good_scale(float s) { return isfinite(s) && s > 0.f; }
 
 constexpr int kSmallRowsLimit = 32;  // varlen: n_q * g at or below this takes the split-K path
+// varlen short-query rows are taken 16 at a time in the 16-row MMA form (168 registers, three
+// CTAs per SM). Groups of 8 in the transposed form (127 registers, four CTAs; a sequence with
+// more rows takes several row-group CTAs, which read its K/V from L2 after the first) measured
+// 1.194 against 1.093 ms on the 64-sequence append workload.
+constexpr int kVarlenGroupRows = 16;
 constexpr int kVarlenKeysPerSplit = 2048;
 constexpr int kVarlenMaxSplits = 64;
 
@@ -342,7 +351,8 @@ int run_decode(bw::SplitKArgs& a, int B, int Hq, int Hkv, int g, int num_splits,
   a.g = g;
   a.num_splits = num_splits;
   a.rows_max = g;
-  a.row_groups = (g + 15) / 16;
+  a.group_rows = g <= 8 ? 8 : 16;
+  a.row_groups = (g + a.group_rows - 1) / a.group_rows;
   a.causal = 0;
   a.small_rows_limit = g;
   a.ws_o_offset = bw::splitk_o_offset(B * Hkv, num_splits, g);
@@ -590,7 +600,8 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
   s.total_k = total_k;
   s.num_splits = splits;
   s.rows_max = kSmallRowsLimit;
-  s.row_groups = kSmallRowsLimit / 16;
+  s.group_rows = kVarlenGroupRows;
+  s.row_groups = kSmallRowsLimit / kVarlenGroupRows;
   s.causal = causal;
   s.window = window;
   s.small_rows_limit = kSmallRowsLimit;

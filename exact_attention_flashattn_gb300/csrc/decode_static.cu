@@ -96,7 +96,8 @@ extern "C" int attn_decode_static(const void* q, const void* kcache, const void*
   a.total_q = a.total_k = 0;
   a.num_splits = num_splits;
   a.rows_max = g;
-  a.row_groups = (g + 15) / 16;
+  a.group_rows = g <= 8 ? 8 : 16;
+  a.row_groups = (g + a.group_rows - 1) / a.group_rows;
   a.causal = 0;
   a.small_rows_limit = g;
   a.ws_o_offset = bw::splitk_o_offset(B * Hkv, num_splits, g);

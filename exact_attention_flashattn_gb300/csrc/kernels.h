@@ -28,7 +28,8 @@ cudaError_t launch_prefill_fp32(const Fp32FwdArgs& a, cudaStream_t stream);
 
 // ---- split-K pass over the KV axis (decode and small-n_q varlen sequences) ----
 // A "unit" is (sequence, KV head, row group); its rows are the (query, head) pairs
-// r = i * g + hh of that sequence's queries and the group's query heads, 16 per row group.
+// r = i * g + hh of that sequence's queries and the group's query heads, group_rows (8 or 16)
+// per row group.
 struct SplitKArgs {
   const uint16_t* q;  // bf16 bits; token-major [tokens, Hq, D]
   const uint16_t* k;  // bf16 bits
@@ -46,7 +47,8 @@ struct SplitKArgs {
   int total_q, total_k;  // varlen: rows of the packed tensors (cu_seqlens are clamped to them)
   int num_splits;
   int rows_max;       // workspace rows per (sequence, KV head)
-  int row_groups;     // ceil(rows_max / 16)
+  int group_rows;     // rows per row group: 8 (transposed 8-row MMA form) or 16 (16-row form)
+  int row_groups;     // ceil(rows_max / group_rows)
   int causal;         // varlen: causal aligned to each sequence's end
   int window;         // varlen: > 0 adds a sliding window of that many keys
   int small_rows_limit;  // varlen: a sequence takes this path iff n_q * g <= this

@@ -8,7 +8,8 @@
 //
 // GB300 mapping. A work item is two 128-row query tiles of one (sequence, head). The kernel is
 // persistent: one CTA per SM takes items from a list in order through an atomic counter
-// (dynamic, so long and short items balance). The list is cut into bands of (sequence, head)
+// (dynamic, so long and short items balance); the producer warp publishes each item with the
+// fields its consumers need already worked out. The list is cut into bands of (sequence, head)
 // units and, inside a band, ordered longest first: the items in flight at any time then belong
 // to one or two bands, whose K/V stay in L2 while every query tile of those heads reads them.
 // The host sizes the band from the K/V bytes of a unit (16 to 64 units). 10 warps per CTA:
@@ -59,9 +60,23 @@ struct Cfg {
   static constexpr uint32_t kTileBytes = kBN * D * 2;
   static constexpr int kStages = (D == 128) ? 4 : 6;
   static constexpr uint32_t kBarOffset = 2 * kQBytes + kStages * kTileBytes;
-  static constexpr uint32_t kSmemBytes = kBarOffset + 256 + 1024;  // + barriers, + alignment slack
+  static constexpr uint32_t kSmemBytes = kBarOffset + 512 + 1024;  // + barriers, + alignment slack
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
+};
+
+// What the consumers of an item need, computed once by the producer warp and published in the
+// item queue. Each consumer warp would otherwise redo the list arithmetic (integer divisions)
+// on a code path it runs once per item, where it delays the item's first MMA or softmax.
+struct ItemRec {
+  int idx;           // item index, -1: the list is exhausted
+  int nq, nk;        // the sequence's query and key counts
+  int q_lo[2];       // first row (within the sequence) of each query tile
+  int j0[2], j1[2];  // each query tile's K/V tiles: [j0, j1)
+  int nt[2];         // j1 - j0
+  int jmin, nt_all;  // K/V tiles the item loads: jmin .. jmin + nt_all - 1
+  int out_row_stride;
+  int64_t out_row0;  // output row index of the sequence's first query for this head
 };
 
 struct Barriers {
@@ -75,10 +90,11 @@ struct Barriers {
   uint64_t kv_empty[6];
   uint64_t item_full[kItemSlots];
   uint64_t item_empty[kItemSlots];
-  int item_q[kItemSlots];  // item index, or -1 when the list is exhausted
+  ItemRec rec[kItemSlots];  // the item queue
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(Barriers) <= 512, "barriers exceed the shared memory reserved for them");
 
 struct Item {
   bool active;
@@ -190,14 +206,16 @@ __device__ __forceinline__ Item make_item(const TcFwdArgs& a, int idx) {
   return w;
 }
 
-// Consumer side of the item queue: the k-th item this CTA runs (-1: no more items).
-__device__ __forceinline__ int next_item(Barriers* bar, int k, bool arrive, uint64_t tmo, const volatile int* abort,
-                                         bool* ok) {
+// Consumer side of the item queue, called by a converged warp: wait for the k-th item this CTA
+// runs (null: a wait gave up); the warp copies what it needs, then releases the slot.
+__device__ __forceinline__ const ItemRec* wait_item(Barriers* bar, int k, uint64_t tmo, const volatile int* abort) {
   const int slot = k % kItemSlots;
-  *ok = mbar_wait(&bar->item_full[slot], (k / kItemSlots) & 1, tmo, abort);
-  const int idx = *ok ? *reinterpret_cast<volatile int*>(&bar->item_q[slot]) : -1;
-  if (arrive && *ok) mbar_arrive(&bar->item_empty[slot]);
-  return idx;
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(&bar->item_full[slot], (k / kItemSlots) & 1, tmo, abort));
+  return ok ? &bar->rec[slot] : nullptr;
+}
+__device__ __forceinline__ void release_item(Barriers* bar, int k) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&bar->item_empty[k % kItemSlots]);
 }
 
 __device__ __forceinline__ void tma_tile(const CUtensorMap* map, const Item& w, uint8_t* dst, uint64_t* bar,
@@ -286,7 +304,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         if (k >= kItemSlots && !(ok = vote(mbar_wait(&bar->item_empty[qs], ((k / kItemSlots) - 1) & 1, tmo, abort))))
           break;
         if (lane == 0) {
-          bar->item_q[qs] = idx;
+          ItemRec& r = bar->rec[qs];
+          r.idx = idx;
+          if (idx >= 0) {
+            r.nq = w.nq;
+            r.nk = w.nk;
+            r.q_lo[0] = w.q_lo[0];
+            r.q_lo[1] = w.q_lo[1];
+            r.j0[0] = w.j0[0];
+            r.j0[1] = w.j0[1];
+            r.j1[0] = w.j1[0];
+            r.j1[1] = w.j1[1];
+            r.nt[0] = w.nt[0];
+            r.nt[1] = w.nt[1];
+            r.jmin = w.jmin;
+            r.nt_all = w.nt_all;
+            r.out_row_stride = static_cast<int>(w.out_row_stride);
+            r.out_row0 = w.out_row0;
+          }
           mbar_arrive(&bar->item_full[qs]);
         }
         if (idx < 0) break;
@@ -374,12 +409,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       };
 
       for (int k = 0; ok; ++k) {
-        const int idx = next_item(bar, k, false, tmo, abort, &ok);
-        ok = __all_sync(0xffffffffu, ok);
-        __syncwarp();
-        if (lane == 0 && ok) mbar_arrive(&bar->item_empty[k % kItemSlots]);
-        if (!ok || idx < 0) break;
-        const Item w = make_item<kWindow>(a, idx);
+        const ItemRec* rp = wait_item(bar, k, tmo, abort);
+        if (!(ok = rp != nullptr)) break;
+        if (rp->idx < 0) {
+          release_item(bar, k);
+          break;
+        }
+        struct {
+          int nt_all, jmin, j0[2], j1[2], nt[2];
+        } w;
+        w.nt_all = rp->nt_all;
+        w.jmin = rp->jmin;
+        w.j0[0] = rp->j0[0];
+        w.j0[1] = rp->j0[1];
+        w.j1[0] = rp->j1[0];
+        w.j1[1] = rp->j1[1];
+        w.nt[0] = rp->nt[0];
+        w.nt[1] = rp->nt[1];
+        release_item(bar, k);
         if (!(ok = vote(mbar_wait(&bar->q_full, items & 1, tmo, abort)))) break;
         tc_fence_after();
         ++items;
@@ -453,20 +500,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     int oused = 0;   // items whose O accumulator was used
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      const int idx = next_item(bar, k, false, tmo, abort, &ok);
-      ok = __all_sync(0xffffffffu, ok);
-      __syncwarp();
-      if (lane == 0 && ok) mbar_arrive(&bar->item_empty[k % kItemSlots]);
-      if (!ok || idx < 0) break;
-      const Item w = make_item<kWindow>(a, idx);
-      // per-tile fields by select: a runtime index would put the item in local memory
-      const int q_row = (t ? w.q_lo[1] : w.q_lo[0]) + row;
-      const bool row_ok = q_row < w.nq;
-      const int lim = a.causal ? min(w.nk, q_row + (w.nk - w.nq) + 1) : w.nk;
+      const ItemRec* rp = wait_item(bar, k, tmo, abort);
+      if (!(ok = rp != nullptr)) break;
+      if (rp->idx < 0) {
+        release_item(bar, k);
+        break;
+      }
+      // this warpgroup's query tile: the record's per-tile fields, read from shared memory
+      const int q_row = rp->q_lo[t] + row;
+      const int wnq = rp->nq, wnk = rp->nk;
+      const bool row_ok = q_row < wnq;
+      const int lim = a.causal ? min(wnk, q_row + (wnk - wnq) + 1) : wnk;
       // sliding window: keys below lo are outside this row's window
-      const int lo = kWindow ? q_row + (w.nk - w.nq) + 1 - a.window : 0;
-      const int ntile = t ? w.nt[1] : w.nt[0];
-      const int jfirst = t ? w.j0[1] : w.j0[0];
+      const int lo = kWindow ? q_row + (wnk - wnq) + 1 - a.window : 0;
+      const int ntile = rp->nt[t];
+      const int jfirst = rp->j0[t];
+      const int64_t out_idx = rp->out_row0 + static_cast<int64_t>(q_row) * rp->out_row_stride;
+      release_item(bar, k);
       float m_ref = -INFINITY, l = 0.f;
       for (int j = 0; j < ntile; ++j) {
         ok = mbar_wait(&bar->s_full[t], stiles & 1, tmo, abort);
@@ -580,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         tc_fence_after();
       }
       const float inv = (l > 0.f) ? 1.f / l : 0.f;
-      uint16_t* orow = a.o + (w.out_row0 + static_cast<int64_t>(q_row) * w.out_row_stride) * D;
+      uint16_t* orow = a.o + out_idx * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t ov[32];
@@ -611,8 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         mbar_arrive(&bar->o_empty[t]);
       }
       if (row_ok && a.lse)
-        a.lse[w.out_row0 + static_cast<int64_t>(q_row) * w.out_row_stride] =
-            (l > 0.f) ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+        a.lse[out_idx] = (l > 0.f) ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
     }
     if (!ok && lane == 0) raise_timeout(abort, status);
     tc_fence_before();

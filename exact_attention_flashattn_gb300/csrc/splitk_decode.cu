@@ -51,6 +51,7 @@ constexpr int kFp8Chunks = 8;
 constexpr uint32_t kFp8StageBytes = kWarps * kFp8Chunks * 32 * 16;
 constexpr uint32_t kFp8SmemBytes = kFp8Stages * kFp8StageBytes;
 constexpr int kMergeThreads = 256;
+constexpr int kMergeMaxSplits = 1024;  // the entry points accept at most this many splits
 
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
   uint4 r;
@@ -232,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
   const UnitGeom u = unit_geom(a, seq, hkv);
   if (!u.active) return;
   const int R = u.nq * a.g;
-  const int row0 = grp * kRowsPerGroup;
+  const int row0 = grp * 8 * NH;
   if (row0 >= R) return;
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -344,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
   int max_lo = 0;
   if constexpr (kWindow) {
     kstart = max(kbeg, (u.nk - u.nq + row0 / a.g + 1 - a.window) / kKeysPerStep * kKeysPerStep);
-    const int last_r = min(row0 + kRowsPerGroup, R) - 1;
+    const int last_r = min(row0 + 8 * NH, R) - 1;
     max_lo = u.nk - u.nq + last_r / a.g + 1 - a.window;
   }
 
@@ -869,7 +870,7 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
 // first; each warp then sums its share of the splits with weights e^{m_s - M}, and the warps'
 // sums are added in shared memory.
 template <int D>
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(MergeArgs a) {
+__global__ void __launch_bounds__(kMergeThreads, 1) merge_kernel(MergeArgs a) {
   // the split-K pass (the grid this launch depends on) has completed from here on
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int unit = blockIdx.x / a.rows_max;
@@ -893,15 +894,43 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(MergeArgs a) {
   const float* wo = a.ws + a.ws_o_offset + (static_cast<size_t>(unit) * S * a.rows_max + r) * D;
   const size_t ml_stride = static_cast<size_t>(a.rows_max) * 2;
   const size_t o_stride = static_cast<size_t>(a.rows_max) * D;
+  __shared__ float sh_f[kMergeMaxSplits];  // weight 2^(m_s - M) of split s (0 for an empty split)
   __shared__ float sh_red[kMW];
   __shared__ float4 sh_o[kMW][D / 4];
   __shared__ float sh_l[kMW];
 
-  // global max over the non-empty partials
+  // this warp's splits: s = warp, warp + kMW, ...; lane owns the channel quads lane + 32 j
+  // (d = 64: lanes 16..31 hold none and read quad 0 again, their sums unused; d = 256: two each).
+  // Every split's o row is written by the split-K pass (zeros for an empty split, whose weight
+  // is 0), so the first kUnroll rows of this warp are loaded before the weights are known: their
+  // loads overlap the (m, l) round below.
+  constexpr int kC4 = D / 4;
+  constexpr int kPL = (kC4 + 31) / 32;
+  constexpr int kUnroll = D == 256 ? 8 : 16;
+  auto load_rows = [&](int s0, float4 (&x)[kUnroll][kPL]) {
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int s = min(s0 + u * kMW, S - 1);
+#pragma unroll
+      for (int j = 0; j < kPL; ++j) {
+        const int c4 = lane + 32 * j < kC4 ? lane + 32 * j : 0;
+        x[u][j] = *reinterpret_cast<const float4*>(wo + s * o_stride + 4 * c4);
+      }
+    }
+  };
+  float4 x[kUnroll][kPL];
+  load_rows(warp, x);
+
+  // every split's (m, l) in one round of loads (a thread holds up to four), then the global max
+  // over the non-empty partials
+  constexpr int kPT = kMergeMaxSplits / kMergeThreads;
+  float2 v[kPT];
   float M = -INFINITY;
-  for (int s = threadIdx.x; s < S; s += kMergeThreads) {
-    const float2 v = *reinterpret_cast<const float2*>(ml + s * ml_stride);
-    if (v.y > 0.f) M = fmaxf(M, v.x);
+#pragma unroll
+  for (int u = 0; u < kPT; ++u) {
+    const int s = threadIdx.x + u * kMergeThreads;
+    v[u] = s < S ? *reinterpret_cast<const float2*>(ml + s * ml_stride) : make_float2(-INFINITY, 0.f);
+    if (v[u].y > 0.f) M = fmaxf(M, v[u].x);
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
@@ -910,34 +939,43 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(MergeArgs a) {
   M = sh_red[0];
 #pragma unroll
   for (int w = 1; w < kMW; ++w) M = fmaxf(M, sh_red[w]);
-
-  // this warp's splits: s = warp, warp + kMW, ...; lane owns the channel quads lane + 32 j
-  // (d = 64: lanes 16..31 hold none and read quad 0 again, their sums unused; d = 256: two each)
-  constexpr int kC4 = D / 4;
-  constexpr int kPL = (kC4 + 31) / 32;
+  // the weights and the merged sum l
   float L = 0.f;
+#pragma unroll
+  for (int u = 0; u < kPT; ++u) {
+    const int s = threadIdx.x + u * kMergeThreads;
+    const float f = v[u].y > 0.f ? ex2(v[u].x - M) : 0.f;
+    L += f * v[u].y;
+    if (s < S) sh_f[s] = f;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  if (lane == 0) sh_l[warp] = L;
+  __syncthreads();
+
   float4 o[kPL];
 #pragma unroll
   for (int j = 0; j < kPL; ++j) o[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = warp; s < S; s += kMW) {
-    const float2 v = *reinterpret_cast<const float2*>(ml + s * ml_stride);
-    if (!(v.y > 0.f)) continue;
-    const float f = ex2(v.x - M);
-    L += f * v.y;
+  for (int s0 = warp;;) {
 #pragma unroll
-    for (int j = 0; j < kPL; ++j) {
-      const int c4 = lane + 32 * j < kC4 ? lane + 32 * j : 0;
-      const float4 x = *reinterpret_cast<const float4*>(wo + s * o_stride + 4 * c4);
-      o[j].x += f * x.x;
-      o[j].y += f * x.y;
-      o[j].z += f * x.z;
-      o[j].w += f * x.w;
+    for (int u = 0; u < kUnroll; ++u) {
+      const int s = s0 + u * kMW;
+      const float f = s < S ? sh_f[s] : 0.f;
+#pragma unroll
+      for (int j = 0; j < kPL; ++j) {
+        o[j].x += f * x[u][j].x;
+        o[j].y += f * x[u][j].y;
+        o[j].z += f * x[u][j].z;
+        o[j].w += f * x[u][j].w;
+      }
     }
+    s0 += kUnroll * kMW;
+    if (s0 >= S) break;
+    load_rows(s0, x);
   }
 #pragma unroll
   for (int j = 0; j < kPL; ++j)
     if (lane + 32 * j < kC4) sh_o[warp][lane + 32 * j] = o[j];
-  if (lane == 0) sh_l[warp] = L;
   __syncthreads();
   if (warp != 0 || lane >= kC4) return;
   L = 0.f;
@@ -952,11 +990,11 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(MergeArgs a) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int w = 0; w < kMW; ++w) {
-      const float4 x = sh_o[w][c4];
-      acc.x += x.x;
-      acc.y += x.y;
-      acc.z += x.z;
-      acc.w += x.w;
+      const float4 y = sh_o[w][c4];
+      acc.x += y.x;
+      acc.y += y.y;
+      acc.z += y.z;
+      acc.w += y.w;
     }
     uint2 packed;
     packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
@@ -969,8 +1007,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(MergeArgs a) {
 template <int D>
 cudaError_t launch_splitk_d(const SplitKArgs& a, cudaStream_t stream) {
   dim3 grid(a.num_splits, a.Hkv * a.row_groups, a.num_seqs);
-  // every row group has at most 8 rows when the sequences' rows (n_q * g) never exceed 8
-  const bool half = a.cu_q ? (a.small_rows_limit <= 8) : (a.g <= 8);
+  // 8-row groups take the transposed form
+  const bool half = a.group_rows == 8;
   const bool paged = a.block_table != nullptr;
   const bool window = a.causal && a.window > 0;
   const bool fp8 = a.k8 != nullptr;
