@@ -12,18 +12,23 @@
 // fields its consumers need already worked out. The list is cut into bands of (sequence, head)
 // units and, inside a band, ordered longest first: the items in flight at any time then belong
 // to one or two bands, whose K/V stay in L2 while every query tile of those heads reads them.
-// The host sizes the band from the K/V bytes of a unit (16 to 64 units). 10 warps per CTA:
+// The host sizes the band from the K/V bytes of a unit (16 to 64 units). 11 warps per CTA:
 //   warp 8      TMA producer: takes the next item and hands it to the other roles through a
 //               small shared-memory queue; per item, both Q tiles once (after the previous item's last
 //               S MMA freed them), then K_j, V_j tiles (128 keys x d, 128-byte swizzle) into a
 //               ring of shared-memory slots guarded by full/empty mbarriers; the ring runs on
 //               across items.
-//   warp 9      MMA issuer: S_w = Q_w K_j^T into TMEM (fp32, 128 columns per tile), then
-//               O_w += P_w V_j with P read from TMEM (bf16, aliased onto S_w) and V from shared
-//               memory. Issue order S0(j+1) after PV0(j), S1(j+1) after PV1(j): the softmax of
-//               one tile overlaps tensor work on the other. Warps 8 and 9 each run their loop
-//               converged (waits voted across the warp) and one elected lane issues each copy,
-//               MMA and commit, which keeps their address arithmetic warp-uniform.
+//   warps 9,10  MMA issuers, one per query tile w: S_w = Q_w K_j^T into TMEM (fp32, 128 columns
+//               per tile), then O_w += P_w V_j with P read from TMEM (bf16, aliased onto S_w)
+//               and V from shared memory, S_w(j+1) after P_w V_j. A tcgen05.mma issue blocks at
+//               about the tensor pipe's own rate (one M128 N128 K16 MMA per ~70 cycles, even
+//               with the pipe idle), so an issuer that waits for P leaves the pipe without work;
+//               with one issuer per tile the other tile's MMAs fill that time. The window and
+//               d = 64 instances keep one issuer for both tiles (warp 9; warp 10 idles), in the
+//               order PV0(j), S0(j+1), PV1(j), S1(j+1), which makes the two tiles' softmaxes
+//               alternate. Warps 8-10 each run their loop converged (waits voted across the
+//               warp) and one elected lane issues each copy, MMA and commit, which keeps their
+//               address arithmetic warp-uniform.
 //   warps 0-3,  softmax warpgroups, one per query tile, thread = row = TMEM lane: read the S
 //   4-7         row, apply the causal mask on diagonal tiles only ("Attention Computation in
 //               Practice", Masking variants: skip / full / diagonal), update m and l in
@@ -45,12 +50,11 @@ namespace {
 
 constexpr int kBM = 128;  // rows per query tile
 constexpr int kBN = 128;  // keys per K/V tile
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kTmaWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 9;  // warps 9 (query tile 0, or both) and 10 (query tile 1)
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
 constexpr int kItemSlots = 2;              // depth of the item queue from producer to consumers
-constexpr int kItemConsumers = 1 + 8;      // one lane of the MMA warp and of each softmax warp
 constexpr int kEarlyLoads = 2;             // K/V loads of an item issued before its Q
 
 template <int D>
@@ -85,7 +89,7 @@ struct Barriers {
   uint64_t p_full[2];  // P of the current K tile stored in TMEM
   uint64_t o_full[2];
   uint64_t o_empty[2];
-  uint64_t mma_done;
+  uint64_t mma_done[2];
   uint64_t kv_full[6];
   uint64_t kv_empty[6];
   uint64_t item_full[kItemSlots];
@@ -233,6 +237,11 @@ template <int D, bool kWindow>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ TcFwdArgs a,
                                                                  unsigned int* status, unsigned int* sched) {
   using C = Cfg<D>;
+  // MMA issuers: one per query tile, except in the window and d = 64 instances (one for both;
+  // there the tiles' softmaxes do better forced to alternate by a single issue order: short,
+  // window-bounded items, or MMA groups half as long as at d = 128)
+  constexpr int kIssuers = (kWindow || D == 64) ? 1 : 2;
+  constexpr int kItemConsumers = kIssuers + 8;  // one lane of each MMA warp and of each softmax warp
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;                      // [2][halves][128 rows][128 B]
@@ -245,17 +254,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 
   if (threadIdx.x == 0) {
     mbar_init(&bar->q_full, 1);
-    mbar_init(&bar->q_empty, 1);
+    mbar_init(&bar->q_empty, kIssuers);  // one commit per MMA warp
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar->s_full[i], 1);
       mbar_init(&bar->p_full[i], kBM);
       mbar_init(&bar->o_full[i], 1);
       mbar_init(&bar->o_empty[i], kBM);
     }
-    mbar_init(&bar->mma_done, 1);
+    mbar_init(&bar->mma_done[0], 1);
+    mbar_init(&bar->mma_done[1], 1);
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&bar->kv_full[i], 1);
-      mbar_init(&bar->kv_empty[i], 1);
+      mbar_init(&bar->kv_empty[i], kIssuers);  // one commit per MMA warp
     }
     for (int i = 0; i < kItemSlots; ++i) {
       mbar_init(&bar->item_full[i], 1);
@@ -362,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       for (int i = max(0, nload - C::kStages); i < nload; ++i)
         mbar_wait(&bar->kv_full[i % C::kStages], (i / C::kStages) & 1, tmo, &no_abort);
     }
-  } else if (warp == kMmaWarp) {
+  } else if (kIssuers == 1 && warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs this loop with identical values (waits are voted, so every lane takes
     // the same path); the MMA and commit wrappers let one elected lane issue.
@@ -485,10 +495,114 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       if (!ok && lane == 0) raise_timeout(abort, status);
       // all MMAs issued by this warp complete before TMEM is released
       const int no_abort = 0;
-      umma_commit(&bar->mma_done);
-      mbar_wait(&bar->mma_done, 0, tmo, &no_abort);
+      umma_commit(&bar->mma_done[0]);
+      mbar_wait(&bar->mma_done[0], 0, tmo, &no_abort);
     }
-  } else {
+  } else if (kIssuers == 2 && (warp == kMmaWarp || warp == kMmaWarp + 1)) {
+    // ------------------------------------------------------------ MMA issuers, one per query tile
+    // tcgen05.mma issue blocks at about the tensor pipe's own rate, so a single issuing warp that
+    // waits (for P, a K/V tile or Q) leaves the pipe with nothing queued; with one issuer per
+    // query tile the other tile's MMAs keep it fed. Each warp runs its loop converged (waits
+    // are voted); the MMA and commit wrappers let one elected lane issue. Both warps release
+    // every K/V slot and the Q buffers (two-arrival barriers), each only after the slot's load
+    // has landed, so neither can arrive for a phase before the previous one has completed.
+    {
+      const int tt = warp - kMmaWarp;  // this warp's query tile
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, 0, 0);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, D, 0, 1);
+      // descriptor halves: K-major Q and K tiles (8-row groups 1024 B apart), MN-major V tiles
+      // (8-key groups 1024 B apart, the two 64-column halves kBN * 128 B apart)
+      const uint32_t hi = sdesc_hi(1024);
+      const uint32_t q_lo = sdesc_lo(smem_u32(sQ) + tt * C::kQBytes, 16);
+      const uint32_t k_lo = sdesc_lo(smem_u32(sRing), 16);
+      const uint32_t v_lo = sdesc_lo(smem_u32(sRing), kBN * 128);
+      const uint32_t slot_step = C::kTileBytes >> 4;
+      const uint32_t tS = tbase + (tt ? C::kColS1 : C::kColS0);
+      const uint32_t tO = tbase + (tt ? C::kColO1 : C::kColO0);
+      int nload = 0;  // K/V tiles consumed, over all items
+      int items = 0;  // active items
+      int pt = 0;     // p_full completions consumed
+      int ou = 0;     // items whose O accumulator was used
+      bool ok = true;
+
+      auto vote = [](bool x) { return __all_sync(0xffffffffu, x); };
+      auto wait_load = [&](int i) -> bool {
+        const bool r =
+            __all_sync(0xffffffffu, mbar_wait(&bar->kv_full[i % C::kStages], (i / C::kStages) & 1, tmo, abort));
+        tc_fence_after();
+        return r;
+      };
+      // S = Q K^T, K in the load slot of load i
+      auto issue_s = [&](int i) {
+        const uint32_t kl = k_lo + (i % C::kStages) * slot_step;
+        if constexpr (D == 128)
+          umma_ss_k128(tS, q_lo, hi, kl, hi, idesc_qk, 0);
+        else
+          umma_ss_k64(tS, q_lo, hi, kl, hi, idesc_qk, 0);
+        umma_commit(&bar->s_full[tt]);
+      };
+      // O += P V with V in the load slot of load i: 8 MMAs of K = 16 over the tile's keys
+      auto issue_pv = [&](int i, bool accumulate) {
+        umma_ts_k128(tO, tS, v_lo + (i % C::kStages) * slot_step, hi, idesc_pv, accumulate ? 1u : 0u);
+      };
+
+      for (int k = 0; ok; ++k) {
+        const ItemRec* rp = wait_item(bar, k, tmo, abort);
+        if (!(ok = rp != nullptr)) break;
+        if (rp->idx < 0) {
+          release_item(bar, k);
+          break;
+        }
+        const int nt = rp->nt_all;
+        // this tile uses the item's K/V tiles [ta, te)
+        const int ta = rp->j0[tt] - rp->jmin;
+        const int te = ta + rp->nt[tt];
+        release_item(bar, k);
+        if (!(ok = vote(mbar_wait(&bar->q_full, items & 1, tmo, abort)))) break;
+        tc_fence_after();
+        ++items;
+        const int base = nload;
+        if (te == ta) umma_commit(&bar->q_empty);  // no S MMA reads this tile's Q
+        if (te > ta) {
+          if (!(ok = wait_load(base + 2 * ta))) break;
+          issue_s(base + 2 * ta);
+          if (te == ta + 1) umma_commit(&bar->q_empty);
+        }
+        for (int j = 0; j < nt; ++j) {
+          const int ik = base + 2 * j, iv = ik + 1;
+          // K_j: read by S(j), issued already, or not read by this tile at all
+          if ((j < ta || j >= te) && !(ok = wait_load(ik))) break;
+          umma_commit(&bar->kv_empty[ik % C::kStages]);
+          if (!(ok = wait_load(iv))) break;
+          if (j >= ta && j < te) {
+            // the first P.V of an item overwrites O: the previous item's epilogue must be done
+            if (j == ta && ou > 0 && !(ok = vote(mbar_wait(&bar->o_empty[tt], (ou - 1) & 1, tmo, abort)))) break;
+            if (!(ok = vote(mbar_wait(&bar->p_full[tt], pt & 1, tmo, abort)))) break;
+            ++pt;
+            tc_fence_after();
+            issue_pv(iv, j > ta);
+            if (j == te - 1) {
+              umma_commit(&bar->o_full[tt]);
+              ++ou;
+            } else {
+              // S(j + 1) overwrites P(j): it follows this P.V in the warp's (in-order) stream
+              if (!(ok = wait_load(ik + 2))) break;
+              issue_s(ik + 2);
+              if (j + 2 == te) umma_commit(&bar->q_empty);  // the tile's last S
+            }
+          }
+          umma_commit(&bar->kv_empty[iv % C::kStages]);
+        }
+        if (!ok) break;
+        nload += 2 * nt;
+      }
+      if (!ok && lane == 0) raise_timeout(abort, status);
+      // all MMAs issued by this warp complete before TMEM is released
+      const int no_abort = 0;
+      umma_commit(&bar->mma_done[tt]);
+      mbar_wait(&bar->mma_done[tt], 0, tmo, &no_abort);
+    }
+  } else if (warp < 8) {
     // ------------------------------------------------------------ softmax warpgroups
     const int t = warp >> 2;                 // query tile of this warpgroup
     const int row = (warp & 3) * 32 + lane;  // = TMEM lane
