@@ -45,26 +45,29 @@ HEADLINE = "prefill_causal_b4_h32_n4096_d128"
 # DRAM traffic of the dominant kernel from the committed ncu capture, per full launch, valid
 # only while the kernel source is the profiled one (checked by hash); otherwise reported null.
 PROFILED_TRAFFIC = {
-    # the tcgen05 prefill kernel and the PTX wrappers it is built from, hashed in this order
+    # the tcgen05 prefill kernel, the PTX wrappers it is built from and the host code that sizes
+    # its item-list bands, hashed in this order
     "kernel_sources": [
         "exact_attention_flashattn_gb300/csrc/prefill_tc.cu",
         "exact_attention_flashattn_gb300/csrc/ptx.cuh",
+        "exact_attention_flashattn_gb300/csrc/api.cu",
     ],
-    "sha256": "dc72bbaa1ef1e5d681df8034659c6f2f629b24d008fb8d9eab93f86e28956fb8",
-    # (201.56 MB read + 45.74 MB written) at B=2, from the ncu capture summarised under profiles/,
+    "sha256": "d307c1e1cb3963cdf2bb7f059b1ef30f7f0b1578326dc1702402814512938388",
+    # (201.57 MB read + 46.59 MB written) at B=2, from the ncu capture summarised under profiles/,
     # scaled x2 to the B=4 launch: traffic grows with the number of (batch, head) units
-    "bytes_per_launch": 494615552,
+    "bytes_per_launch": 496326656,
 }
 PROFILED_TRAFFIC_D256 = {
-    # the head-dim-256 prefill kernel and its PTX wrappers, hashed in this order
+    # the head-dim-256 prefill kernel, its PTX wrappers and the band sizing, hashed in this order
     "kernel_sources": [
         "exact_attention_flashattn_gb300/csrc/prefill_tc256.cu",
         "exact_attention_flashattn_gb300/csrc/ptx.cuh",
+        "exact_attention_flashattn_gb300/csrc/api.cu",
     ],
-    "sha256": "6d5fa9d7d8a7c85ae7968d7023396663fc3c72c0aaacf79d3cd4b31df0d120ea",
-    # (282.69 MB read + 45.45 MB written) at B=2, from the ncu capture summarised under profiles/,
+    "sha256": "aeda8c1ebf803e5621be9b7ba4b614d5e988789da8d3417b2de2e8d642b00a52",
+    # (201.58 MB read + 44.71 MB written) at B=2, from the ncu capture summarised under profiles/,
     # scaled x2 to the B=4 launch of prefill_causal_b4_h16_n4096_d256
-    "bytes_per_launch": 656267264,
+    "bytes_per_launch": 492587520,
 }
 METRIC = "prefill TFLOP/s and decode KV GB/s, 1×GB300, as fraction of roofline"
 # nominal GB300 figures, the second roofline basis: HBM3e bandwidth of about 8 TB/s and the dense
