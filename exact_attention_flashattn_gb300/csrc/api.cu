@@ -128,6 +128,23 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int d, int64_t dim1, int6
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// 3-D uint8 map {128, dim1, dim2} with row strides in bytes, box {128, box1, box2}, 128-byte
+// swizzle (rows of E4M3 codes at d = 128: one swizzle atom wide), zero fill out of bounds.
+cudaError_t make_map_u8(CUtensorMap* m, const void* base, int64_t dim1, int64_t dim2, int64_t stride1_bytes,
+                        int64_t stride2_bytes, int box1, int box2) {
+  EncodeTiledFn enc = nullptr;
+  cudaError_t e = encoder(&enc);
+  if (e != cudaSuccess) return e;
+  const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(dim1), static_cast<cuuint64_t>(dim2)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(stride1_bytes), static_cast<cuuint64_t>(stride2_bytes)};
+  const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(box1), static_cast<cuuint32_t>(box2)};
+  const cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // Units per band of the prefill item list: as many (sequence, head) units as keep their K and V
 // (one KV head serves g consecutive query heads) within 16 MB, between 16 and 64. Wider bands
 // help short sequences, whose items are many and short (32 units: +5.6 % at 1024 keys, d = 128);
@@ -362,6 +379,8 @@ int run_decode(bw::SplitKArgs& a, int B, int Hq, int Hkv, int g, int num_splits,
     return cuda_fail(e);
   a.o = static_cast<uint16_t*>(o);
   a.lse = lse;
+  if ((e = status_ptr(&a.status)) != cudaSuccess) return cuda_fail(e);
+  a.timeout_ns = g_timeout_ns.load();
   if ((e = bw::launch_splitk(a, st)) != cudaSuccess) return cuda_fail(e);
   g_launches.fetch_add(1);
   if (a.tickets) return BWATTN_OK;  // merged by the last CTA of each unit
@@ -424,6 +443,15 @@ int decode_contig(const void* q, const void* kcache, const void* vcache, const f
   a.kv_cap = nk_cap;
   a.total_q = a.total_k = 0;
   a.scale_log2 = scale * bw::kLog2e;
+  if (fp8 && nk_cap > 0) {
+    // {128 codes, keys, sequence * KV head}: a box is one 16-key step of one KV head
+    cudaError_t e;
+    if ((e = make_map_u8(&a.tm_k8, kcache, nk_cap, static_cast<int64_t>(B) * Hkv, 128,
+                         static_cast<int64_t>(nk_cap) * 128, 16, 1)) != cudaSuccess ||
+        (e = make_map_u8(&a.tm_v8, vcache, nk_cap, static_cast<int64_t>(B) * Hkv, 128,
+                         static_cast<int64_t>(nk_cap) * 128, 16, 1)) != cudaSuccess)
+      return cuda_fail(e);
+  }
   return run_decode(a, B, Hq, Hkv, g, num_splits, nk, o, lse, static_cast<cudaStream_t>(stream));
 }
 
@@ -466,6 +494,14 @@ int decode_paged(const void* q, const void* k_pages, const void* v_pages, const 
   a.page_size = page_size;
   a.max_pages = max_pages_per_seq;
   a.num_pages = num_pages;
+  if (fp8) {
+    // {128 codes, KV head, page rows}: a box is 16 consecutive rows of one KV head inside a page
+    const int64_t rows = static_cast<int64_t>(num_pages) * page_size;
+    cudaError_t e;
+    if ((e = make_map_u8(&a.tm_k8, k_pages, Hkv, rows, 128, static_cast<int64_t>(Hkv) * 128, 1, 16)) != cudaSuccess ||
+        (e = make_map_u8(&a.tm_v8, v_pages, Hkv, rows, 128, static_cast<int64_t>(Hkv) * 128, 1, 16)) != cudaSuccess)
+      return cuda_fail(e);
+  }
   return run_decode(a, B, Hq, Hkv, g, num_splits, nk, o, lse, static_cast<cudaStream_t>(stream));
 }
 

@@ -61,7 +61,11 @@ struct SplitKArgs {
   const int32_t* block_table;
   int page_size, max_pages, num_pages;
   // FP8 KV cache when k8 is non-null (k, v unused): E4M3 codes laid out like k, v; the value of
-  // element (head h, channel c) is e4m3(code) * k_scale[h * D + c] (v_scale for V)
+  // element (head h, channel c) is e4m3(code) * k_scale[h * D + c] (v_scale for V). tm_k8 and
+  // tm_v8 are 3-D uint8 maps with a 128-byte swizzle whose box is one 16-key step of one KV
+  // head: contiguous {128, cap, B * Hkv}, box {128, 16, 1}; paged {128, Hkv, pages * page_size},
+  // box {128, 1, 16}
+  CUtensorMap tm_k8, tm_v8;
   const uint8_t* k8;
   const uint8_t* v8;
   const float* k_scale;
@@ -71,6 +75,10 @@ struct SplitKArgs {
   unsigned int* tickets;
   uint16_t* o;
   float* lse;
+  // the FP8 instances' copies are waited for with a bounded wait (timeout_ns); one that gives up
+  // sets kStatusTimeoutBit in *status (the device status word)
+  unsigned int* status;
+  uint64_t timeout_ns;
 };
 cudaError_t launch_splitk(const SplitKArgs& a, cudaStream_t stream);
 

@@ -43,13 +43,14 @@ constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kRowsPerGroup = 16;
 constexpr int kKeysPerStep = 16;
-// FP8 cache: each thread's 16-byte chunks of a step (4 of K, 4 of V) go through a ring of
-// kFp8Stages shared-memory slots with cp.async, so that the bytes in flight are bounded by
-// shared memory rather than registers
+// FP8 cache: each warp's 16-key steps (2 KB of K codes, 2 KB of V codes) arrive by TMA in a ring
+// of kFp8Stages shared-memory stages per warp, one mbarrier per stage, so that the bytes in
+// flight are bounded by shared memory rather than registers and one lane issues a step's copies
 constexpr int kFp8Stages = 3;
-constexpr int kFp8Chunks = 8;
-constexpr uint32_t kFp8StageBytes = kWarps * kFp8Chunks * 32 * 16;
-constexpr uint32_t kFp8SmemBytes = kFp8Stages * kFp8StageBytes;
+constexpr uint32_t kFp8WarpStepBytes = 2 * kKeysPerStep * 128;  // K box + V box
+constexpr uint32_t kFp8StageBytes = kWarps * kFp8WarpStepBytes;
+constexpr uint32_t kFp8RingBytes = kFp8Stages * kFp8StageBytes;
+constexpr uint32_t kFp8SmemBytes = kFp8RingBytes + 1024;  // + slack to align the ring to 1024 B
 constexpr int kMergeThreads = 256;
 constexpr int kMergeMaxSplits = 1024;  // the entry points accept at most this many splits
 
@@ -59,17 +60,6 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(p));
   return r;
-}
-
-// 16-byte asynchronous copy global -> shared (L2 only); `bytes` = 0 writes zeros and reads
-// nothing from src.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -212,7 +202,7 @@ __device__ __forceinline__ void pair_sum(float4 (&slot)[2][32][NH], int half, in
 // window (a separate instance, so the plain causal and paged paths carry no window registers);
 // kFp8: FP8 E4M3 cache with per-channel scales (k8, v8, k_scale, v_scale).
 template <int D, int NH, bool kPaged, bool kWindow, bool kFp8>
-__global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(SplitKArgs a) {
+__global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(const __grid_constant__ SplitKArgs a) {
   static_assert(D == 64 || D == 128 || D == 256, "head dim");
   static_assert(!kFp8 || D == 128, "the FP8 cache layout is d = 128");
   // d = 256: the warps work in pairs on the same 16-key steps, each warp holding 128 of the
@@ -575,65 +565,82 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
       }
     }
   } else {
-    // FP8: the step's chunks are copied asynchronously into this thread's slots of a
-    // kFp8Stages-deep ring (slot = stage, chunk, lane), kFp8Stages - 1 steps ahead of the one
-    // being computed. Each thread reads back only what it copied, so no barrier is needed.
-    const uint32_t pipe = smem_u32(dsm) + static_cast<uint32_t>((warp * kFp8Chunks * 32 + lane) * 16);
-    auto slot = [&](int st, int c) { return pipe + st * kFp8StageBytes + c * 32 * 16; };
-    auto issue = [&](int kb, int64_t so, int st) {
-      if (kb < kend) {
-        // K: codes of chunks t and t + 4 of rows kb + nt*8 + gr; V: chunk gr of 4 key rows
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const int key = kb + nt * 8 + gr;
-          const uint8_t* kr = kbase8 + so + static_cast<int64_t>(nt * 8 + gr) * ks;
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf)
-            cp_async16(slot(st, 2 * nt + hf), (key < kend) ? kr + 16 * (t + 4 * hf) : kbase8,
-                       (key < kend) ? 16u : 0u);
-        }
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const int key = kb + 2 * t + (x & 1) + 8 * (x >> 1);
-          const uint8_t* vr = vbase8 + so + static_cast<int64_t>(key - kb) * ks;
-          cp_async16(slot(st, 4 + x), (key < kend) ? vr + 16 * gr : vbase8, (key < kend) ? 16u : 0u);
-        }
+    // FP8: each warp's steps arrive by TMA (one lane issues a K box and a V box, 16 key rows of
+    // 128 codes each, 128-byte swizzle) in a kFp8Stages-deep ring of this warp's own stages,
+    // kFp8Stages - 1 steps ahead of the one being computed; a stage is refilled only after the
+    // warp's reads of it, and each stage's barrier is waited for in step order.
+    __shared__ __align__(8) uint64_t fp8_full[kWarps][kFp8Stages];
+    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
+    if (lane == 0) {
+      for (int s2 = 0; s2 < kFp8Stages; ++s2) mbar_init(&fp8_full[warp][s2], 1);
+      fence_mbar_init();
+    }
+    __syncwarp();
+    auto stage_ptr = [&](int s2) { return ring + s2 * kFp8StageBytes + warp * kFp8WarpStepBytes; };
+    const int unit_row = seq * a.Hkv + hkv;  // contiguous map: (sequence, KV head) plane
+    auto issue = [&](int kb, int s2) {
+      if (kb >= kend) return;
+      uint8_t* dst = stage_ptr(s2);
+      mbar_arrive_expect_tx(&fp8_full[warp][s2], kFp8WarpStepBytes);
+      if constexpr (kPaged) {
+        int page = a.block_table[static_cast<int64_t>(seq) * a.max_pages + kb / a.page_size];
+        page = min(max(page, 0), a.num_pages - 1);  // a bad entry reads a wrong page, never outside the pool
+        const int tok = page * a.page_size + kb % a.page_size;
+        tma_load_3d(dst, &a.tm_k8, &fp8_full[warp][s2], 0, hkv, tok);
+        tma_load_3d(dst + kKeysPerStep * 128, &a.tm_v8, &fp8_full[warp][s2], 0, hkv, tok);
+      } else {
+        tma_load_3d(dst, &a.tm_k8, &fp8_full[warp][s2], 0, kb, unit_row);
+        tma_load_3d(dst + kKeysPerStep * 128, &a.tm_v8, &fp8_full[warp][s2], 0, kb, unit_row);
       }
-      cp_async_commit();  // one group per step, empty past the slice
     };
-    auto ld_slot = [&](int st, int c) {
-      uint4 r;
+    // 16 bytes at chunk c of row r of a 128-byte-swizzled box (chunk c ^ (r mod 8) holds it)
+    auto ld_box = [&](const uint8_t* box, int r, int c) {
+      uint4 v;
+      const uint32_t addr = smem_u32(box) + r * 128 + ((c ^ (r & 7)) << 4);
       asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                   : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                   : "r"(slot(st, c)));
-      return r;
+                   : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                   : "r"(addr));
+      return v;
     };
     constexpr int kStride = kWarps * kKeysPerStep;
+    const int no_abort = 0;
+    bool timed_out = false;
     int kb_next = kstart + warp * kKeysPerStep;
-    // paged: the block-table entry of the next step to issue is read one step before its copies
-    int64_t so_next = (kb_next < kend) ? step_offset<kPaged>(a, seq, kb_next) : 0;
-    auto advance = [&]() {
-      kb_next += kStride;
-      if (kb_next < kend) so_next = step_offset<kPaged>(a, seq, kb_next);
-    };
 #pragma unroll
-    for (int st = 0; st < kFp8Stages - 1; ++st) {
-      issue(kb_next, so_next, st);
-      advance();
+    for (int s2 = 0; s2 < kFp8Stages - 1; ++s2) {
+      issue(kb_next, s2);
+      kb_next += kStride;
     }
-    int st = 0;
-    for (int kb = kstart + warp * kKeysPerStep; kb < kend; kb += kStride) {
-      issue(kb_next, so_next, st == 0 ? kFp8Stages - 1 : st - 1);  // the slot read one step ago
-      advance();
-      cp_async_wait<kFp8Stages - 1>();  // this step's group has landed
+    int st = 0, n = 0;  // stage and index of this warp's current step
+    for (int kb = kstart + warp * kKeysPerStep; kb < kend; kb += kStride, ++n) {
+      // refill the stage read one step ago: every lane's reads of it are done (their values were
+      // used), and the fence orders them before the copy engine's writes
+      __syncwarp();
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(kb_next, st == 0 ? kFp8Stages - 1 : st - 1);
+      kb_next += kStride;
+      // bounded wait: a copy that never lands ends the warp's loop and sets the status word
+      if (!__all_sync(0xffffffffu, mbar_wait(&fp8_full[warp][st], (n / kFp8Stages) & 1, a.timeout_ns, &no_abort))) {
+        if (lane == 0 && a.status) atomicOr(a.status, kStatusTimeoutBit);
+        timed_out = true;
+        break;
+      }
+      const uint8_t* kbox = stage_ptr(st);
+      const uint8_t* vbox = kbox + kKeysPerStep * 128;
       uint4 kk[2][2], va[4];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        kk[nt][0] = ld_slot(st, 2 * nt);
-        kk[nt][1] = ld_slot(st, 2 * nt + 1);
+        kk[nt][0] = ld_box(kbox, nt * 8 + gr, t);
+        kk[nt][1] = ld_box(kbox, nt * 8 + gr, t + 4);
       }
 #pragma unroll
-      for (int x = 0; x < 4; ++x) va[x] = ld_slot(st, 4 + x);
+      for (int x = 0; x < 4; ++x) {
+        const int r = 2 * t + (x & 1) + 8 * (x >> 1);
+        va[x] = ld_box(vbox, r, gr);
+        // rows past the slice hold other keys' codes (possibly NaN): their P is 0, and 0 * NaN
+        // would still reach O, so their values are zeroed (their scores are masked)
+        if (kb + r >= kend) va[x] = make_uint4(0u, 0u, 0u, 0u);
+      }
       st = (st + 1 == kFp8Stages) ? 0 : st + 1;
       // k-step kst takes word kst & 3 of chunk kst >> 2: codes (c0, c1) -> k = 2t, 2t+1 and
       // (c2, c3) -> k = 2t+8, 2t+9, the channel order Q was packed in
@@ -697,7 +704,14 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(Split
         }
       }
     }
-    cp_async_wait<0>();  // nothing in flight once the ring is reused for the combine below
+    // after a timed-out wait, the copies this warp issued past it must still land (bounded)
+    // before the ring is reused for the combine below; otherwise every issued step was consumed
+    if (timed_out) {
+      for (int m = n; m < n + kFp8Stages; ++m) {
+        const int kbm = kstart + warp * kKeysPerStep + m * kStride;
+        if (kbm < kend) mbar_wait(&fp8_full[warp][m % kFp8Stages], (m / kFp8Stages) & 1, a.timeout_ns, &no_abort);
+      }
+    }
   }
 
   // ---- combine the key groups' states in shared memory, write this split's partials (d = 256:
