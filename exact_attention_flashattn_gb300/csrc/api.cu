@@ -443,6 +443,16 @@ int decode_contig(const void* q, const void* kcache, const void* vcache, const f
   a.kv_cap = nk_cap;
   a.total_q = a.total_k = 0;
   a.scale_log2 = scale * bw::kLog2e;
+  if (!fp8 && d == 128 && g > 8 && nk_cap > 0) {
+    // the 16-row form's K and V rows by TMA: {128 channels, key, sequence * KV head}, box {64, 16, 1}
+    cudaError_t e;
+    if ((e = make_map(&a.tm_k16, kcache, d, nk_cap, static_cast<int64_t>(B) * Hkv, d,
+                      static_cast<int64_t>(nk_cap) * d, 16, 1)) != cudaSuccess ||
+        (e = make_map(&a.tm_v16, vcache, d, nk_cap, static_cast<int64_t>(B) * Hkv, d,
+                      static_cast<int64_t>(nk_cap) * d, 16, 1)) != cudaSuccess)
+      return cuda_fail(e);
+    a.tma16 = 1;
+  }
   if (fp8 && nk_cap > 0) {
     // {128 codes, keys, sequence * KV head}: a box is one 16-key step of one KV head
     cudaError_t e;
@@ -648,6 +658,15 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
     return cuda_fail(e);
   s.o = static_cast<uint16_t*>(o);
   s.lse = lse;
+  if ((e = status_ptr(&s.status)) != cudaSuccess) return cuda_fail(e);
+  s.timeout_ns = g_timeout_ns.load();
+  if (d == 128 && window == 0 && total_k > 0) {
+    // the 16-row form's K and V rows by TMA: {128 channels, KV head, token}, box {64, 1, 16}
+    if ((e = make_map(&s.tm_k16, k, d, Hkv, total_k, d, static_cast<int64_t>(Hkv) * d, 1, 16)) != cudaSuccess ||
+        (e = make_map(&s.tm_v16, v, d, Hkv, total_k, d, static_cast<int64_t>(Hkv) * d, 1, 16)) != cudaSuccess)
+      return cuda_fail(e);
+    s.tma16 = 1;
+  }
   if ((e = bw::launch_splitk(s, st)) != cudaSuccess) return cuda_fail(e);
   g_launches.fetch_add(1);
   if (s.tickets) return BWATTN_OK;  // merged by the last CTA of each unit

@@ -66,6 +66,12 @@ struct SplitKArgs {
   // head: contiguous {128, cap, B * Hkv}, box {128, 16, 1}; paged {128, Hkv, pages * page_size},
   // box {128, 1, 16}
   CUtensorMap tm_k8, tm_v8;
+  // bf16 16-row form at d = 128 (contiguous or packed cache, no window) when tma16 is non-zero:
+  // K and V rows arrive by TMA through tm_k16 / tm_v16, 3-D bf16 maps with a 128-byte swizzle
+  // whose box is 16 keys x 64 channels of one KV head: contiguous {128, cap, B * Hkv}, box
+  // {64, 16, 1}; packed {128, Hkv, total_k}, box {64, 1, 16}
+  CUtensorMap tm_k16, tm_v16;
+  int tma16;
   const uint8_t* k8;
   const uint8_t* v8;
   const float* k_scale;

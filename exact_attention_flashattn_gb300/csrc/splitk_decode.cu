@@ -51,6 +51,12 @@ constexpr uint32_t kFp8WarpStepBytes = 2 * kKeysPerStep * 128;  // K box + V box
 constexpr uint32_t kFp8StageBytes = kWarps * kFp8WarpStepBytes;
 constexpr uint32_t kFp8RingBytes = kFp8Stages * kFp8StageBytes;
 constexpr uint32_t kFp8SmemBytes = kFp8RingBytes + 1024;  // + slack to align the ring to 1024 B
+// bf16 16-row form at d = 128 (varlen short-query sequences, decode with g > 8) with the TMA ring:
+// 8 KB per warp step, two stages
+constexpr int kT16Stages = 2;
+constexpr uint32_t kT16WarpStepBytes = 2 * 2 * kKeysPerStep * 128;
+constexpr uint32_t kT16StageBytes = kWarps * kT16WarpStepBytes;
+constexpr uint32_t kT16SmemBytes = kT16Stages * kT16StageBytes + 1024;  // + slack to align the ring
 constexpr int kMergeThreads = 256;
 constexpr int kMergeMaxSplits = 1024;  // the entry points accept at most this many splits
 
@@ -122,6 +128,7 @@ struct UnitGeom {
   int tok0;     // first query token of the sequence
   int nq;       // queries of the sequence
   int nk;       // keys of the sequence
+  int k0;       // varlen: token index of the sequence's first key (0 otherwise)
   int64_t kv0;  // element offset of key 0 of this KV head
   bool active;
 };
@@ -133,6 +140,7 @@ __device__ __forceinline__ UnitGeom unit_geom(const SplitKArgs& a, int seq, int 
     u.tok0 = min(max(a.cu_q[seq], 0), a.total_q);
     u.nq = min(max(a.cu_q[seq + 1] - u.tok0, 0), a.total_q - u.tok0);
     const int k0 = min(max(a.cu_k[seq], 0), a.total_k);
+    u.k0 = k0;
     u.nk = min(max(a.cu_k[seq + 1] - k0, 0), a.total_k - k0);
     u.kv0 = static_cast<int64_t>(k0) * a.kv_key_stride + static_cast<int64_t>(hkv) * a.kv_head_stride;
     u.active = u.nq > 0 && u.nq * a.g <= a.small_rows_limit;
@@ -140,12 +148,14 @@ __device__ __forceinline__ UnitGeom unit_geom(const SplitKArgs& a, int seq, int 
     // paged cache: kv0 is the head's offset inside a page row; pages come from the block table
     u.tok0 = seq;
     u.nq = 1;
+    u.k0 = 0;
     u.nk = min(max(a.nk[seq], 0), a.max_pages * a.page_size);
     u.kv0 = static_cast<int64_t>(hkv) * a.kv_head_stride;
     u.active = true;
   } else {
     u.tok0 = seq;
     u.nq = 1;
+    u.k0 = 0;
     u.nk = min(max(a.nk[seq], 0), a.kv_cap);
     u.kv0 = static_cast<int64_t>(seq) * a.kv_seq_stride + static_cast<int64_t>(hkv) * a.kv_head_stride;
     u.active = true;
@@ -201,10 +211,11 @@ __device__ __forceinline__ void pair_sum(float4 (&slot)[2][32][NH], int half, in
 // kPaged: keys are gathered page by page through the block table; kWindow: causal sliding
 // window (a separate instance, so the plain causal and paged paths carry no window registers);
 // kFp8: FP8 E4M3 cache with per-channel scales (k8, v8, k_scale, v_scale).
-template <int D, int NH, bool kPaged, bool kWindow, bool kFp8>
+template <int D, int NH, bool kPaged, bool kWindow, bool kFp8, bool kTma16 = false>
 __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(const __grid_constant__ SplitKArgs a) {
   static_assert(D == 64 || D == 128 || D == 256, "head dim");
   static_assert(!kFp8 || D == 128, "the FP8 cache layout is d = 128");
+  static_assert(!kTma16 || (D == 128 && NH == 2 && !kPaged && !kWindow && !kFp8), "TMA ring: 16-row form, d = 128");
   // d = 256: the warps work in pairs on the same 16-key steps, each warp holding 128 of the
   // channels of Q, K, V and O; the pair adds its two partial score tiles through shared memory,
   // so both warps take the same softmax and each accumulates its own half of O
@@ -477,27 +488,9 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(const
   if constexpr (!kFp8) {
     // d = 256: the pairs' exchange slots [key group][step parity][warp of the pair][lane]
     __shared__ float4 xch[kKG][2][2][32][NH];
-    int step = 0;
-    for (int kb = kstart + kg * kKeysPerStep; kb < kend; kb += kKG * kKeysPerStep, ++step) {
-      // ---- loads: K rows kb + nt*8 + gr (chunks t + 4s); V rows kb + {2t, 2t+1, 2t+8, 2t+9}
-      // (chunk gr into va; 128 channels per warp also chunk 8 + gr into vb); all from channel hoff
-      const int64_t so = step_offset<kPaged>(a, seq, kb) + hoff;
-      uint4 kk[2][DW / 32], va[4], vb[4];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const int key = kb + nt * 8 + gr;
-        const uint16_t* kr = kbase + so + static_cast<int64_t>(nt * 8 + gr) * ks;
-#pragma unroll
-        for (int s = 0; s < DW / 32; ++s)
-          kk[nt][s] = (key < kend) ? ld_stream(kr + 8 * (t + 4 * s)) : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const int key = kb + 2 * t + (x & 1) + 8 * (x >> 1);
-        const uint16_t* vr = vbase + so + static_cast<int64_t>(key - kb) * ks;
-        va[x] = (key < kend) ? ld_stream(vr + 8 * gr) : make_uint4(0, 0, 0, 0);
-        if constexpr (DW == 128) vb[x] = (key < kend) ? ld_stream(vr + 64 + 8 * gr) : make_uint4(0, 0, 0, 0);
-      }
+    // one 16-key step from its K and V fragments: the two contractions and the softmax update
+    auto compute_bf16 = [&](int kb, int step, const uint4 (&kk)[2][DW / 32], const uint4 (&va)[4],
+                            const uint4 (&vb)[4]) {
       if constexpr (NH == 1) {
         // ---- S^T = K Q^T: rows = keys gr / gr + 8 (the two K rows this thread loaded), DW/16
         // k16 steps over the warp's channels; Q is the B operand (row gr of the group)
@@ -562,6 +555,118 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(const
           float(&acc)[4] = *reinterpret_cast<float(*)[4]>(&oacc[nu][0]);
           mma_bf16(acc, pa, __byte_perm(w0, w1, sel), __byte_perm(w2, w3, sel));
         }
+      }
+    };
+    if constexpr (kTma16) {
+      // 16-row form at d = 128 over a contiguous or packed cache: each warp's steps arrive by TMA
+      // (one lane issues 4 boxes of 16 key rows x 64 channels: K and V, two channel halves each,
+      // 128-byte swizzle) in a kT16Stages-deep ring of the warp's own stages, so that a warp has
+      // the next step's 8 KB in flight while it computes this one, and the fragments live in
+      // registers only while they are used
+      __shared__ __align__(8) uint64_t t16_full[kWarps][kT16Stages];
+      uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
+      if (lane == 0) {
+        for (int s2 = 0; s2 < kT16Stages; ++s2) mbar_init(&t16_full[warp][s2], 1);
+        fence_mbar_init();
+      }
+      __syncwarp();
+      auto stage_ptr = [&](int s2) { return ring + s2 * kT16StageBytes + warp * kT16WarpStepBytes; };
+      const bool packed = a.cu_q != nullptr;
+      auto issue = [&](int kb, int s2) {
+        if (kb >= kend) return;
+        uint8_t* dst = stage_ptr(s2);
+        mbar_arrive_expect_tx(&t16_full[warp][s2], kT16WarpStepBytes);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          // boxes: K half 0, K half 1, V half 0, V half 1 (2 KB each)
+          if (packed) {
+            tma_load_3d(dst + h * 2048, &a.tm_k16, &t16_full[warp][s2], 64 * h, hkv, u.k0 + kb);
+            tma_load_3d(dst + 4096 + h * 2048, &a.tm_v16, &t16_full[warp][s2], 64 * h, hkv, u.k0 + kb);
+          } else {
+            tma_load_3d(dst + h * 2048, &a.tm_k16, &t16_full[warp][s2], 64 * h, kb, seq * a.Hkv + hkv);
+            tma_load_3d(dst + 4096 + h * 2048, &a.tm_v16, &t16_full[warp][s2], 64 * h, kb, seq * a.Hkv + hkv);
+          }
+        }
+      };
+      // 8 channels (16 bytes) at chunk c (0..15) of row r: box half c / 8, swizzled chunk c % 8
+      auto ld_row = [&](const uint8_t* box, int r, int c) {
+        uint4 v;
+        const uint32_t addr = smem_u32(box + (c >> 3) * 2048) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                     : "r"(addr));
+        return v;
+      };
+      constexpr int kStride = kWarps * kKeysPerStep;
+      const int no_abort = 0;
+      bool timed_out = false;
+      int kb_next = kstart + warp * kKeysPerStep;
+#pragma unroll
+      for (int s2 = 0; s2 < kT16Stages - 1; ++s2) {
+        issue(kb_next, s2);
+        kb_next += kStride;
+      }
+      int st = 0, n = 0;
+      for (int kb = kstart + warp * kKeysPerStep; kb < kend; kb += kStride, ++n) {
+        __syncwarp();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        issue(kb_next, st == 0 ? kT16Stages - 1 : st - 1);
+        kb_next += kStride;
+        if (!__all_sync(0xffffffffu, mbar_wait(&t16_full[warp][st], (n / kT16Stages) & 1, a.timeout_ns, &no_abort))) {
+          if (lane == 0 && a.status) atomicOr(a.status, kStatusTimeoutBit);
+          timed_out = true;
+          break;
+        }
+        const uint8_t* kbox = stage_ptr(st);
+        const uint8_t* vbox = kbox + 4096;
+        uint4 kk[2][DW / 32], va[4], vb[4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int s3 = 0; s3 < DW / 32; ++s3) kk[nt][s3] = ld_row(kbox, nt * 8 + gr, t + 4 * s3);
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const int r = 2 * t + (x & 1) + 8 * (x >> 1);
+          va[x] = ld_row(vbox, r, gr);
+          vb[x] = ld_row(vbox, r, 8 + gr);
+          // rows past the slice hold other keys (possibly NaN or inf): their P is 0, and 0 * NaN
+          // would still reach O, so their values are zeroed (their scores are masked)
+          if (kb + r >= kend) va[x] = vb[x] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        st = (st + 1 == kT16Stages) ? 0 : st + 1;
+        compute_bf16(kb, n, kk, va, vb);
+      }
+      // after a timed-out wait, the copies issued past it must land (bounded) before the ring is
+      // reused for the combine below; otherwise every issued step was consumed
+      if (timed_out) {
+        for (int m = n; m < n + kT16Stages; ++m) {
+          const int kbm = kstart + warp * kKeysPerStep + m * kStride;
+          if (kbm < kend) mbar_wait(&t16_full[warp][m % kT16Stages], (m / kT16Stages) & 1, a.timeout_ns, &no_abort);
+        }
+      }
+    } else {
+      int step = 0;
+      for (int kb = kstart + kg * kKeysPerStep; kb < kend; kb += kKG * kKeysPerStep, ++step) {
+        // ---- loads: K rows kb + nt*8 + gr (chunks t + 4s); V rows kb + {2t, 2t+1, 2t+8, 2t+9}
+        // (chunk gr into va; 128 channels per warp also chunk 8 + gr into vb); all from channel hoff
+        const int64_t so = step_offset<kPaged>(a, seq, kb) + hoff;
+        uint4 kk[2][DW / 32], va[4], vb[4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const int key = kb + nt * 8 + gr;
+          const uint16_t* kr = kbase + so + static_cast<int64_t>(nt * 8 + gr) * ks;
+#pragma unroll
+          for (int s = 0; s < DW / 32; ++s)
+            kk[nt][s] = (key < kend) ? ld_stream(kr + 8 * (t + 4 * s)) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const int key = kb + 2 * t + (x & 1) + 8 * (x >> 1);
+          const uint16_t* vr = vbase + so + static_cast<int64_t>(key - kb) * ks;
+          va[x] = (key < kend) ? ld_stream(vr + 8 * gr) : make_uint4(0, 0, 0, 0);
+          if constexpr (DW == 128) vb[x] = (key < kend) ? ld_stream(vr + 64 + 8 * gr) : make_uint4(0, 0, 0, 0);
+        }
+        compute_bf16(kb, step, kk, va, vb);
       }
     }
   } else {
@@ -719,8 +824,8 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(const
   __shared__ float sm_m[kKG][kRowsPerGroup];
   __shared__ float sm_l[kKG][kRowsPerGroup];
   float (*sm_o)[kRowsPerGroup][D + 4];
-  if constexpr (kFp8) {
-    // the FP8 ring is free now: every warp must be past its last read before it is reused
+  if constexpr (kFp8 || kTma16) {
+    // the TMA ring is free now: every warp must be past its last read before it is reused
     __syncthreads();
     sm_o = reinterpret_cast<float (*)[kRowsPerGroup][D + 4]>(dsm);
   } else {
@@ -1049,6 +1154,13 @@ cudaError_t launch_splitk_d(const SplitKArgs& a, cudaStream_t stream) {
   } else if (half) {
     paged ? splitk_kernel<D, 1, true, false, false><<<grid, kThreads, 0, stream>>>(a)
           : splitk_kernel<D, 1, false, false, false><<<grid, kThreads, 0, stream>>>(a);
+  } else if (D == 128 && !paged && a.tma16) {
+    static_assert(kT16SmemBytes >= sizeof(float) * kWarps * kRowsPerGroup * (128 + 4), "combine buffer");
+    auto k = splitk_kernel<D, 2, false, false, false, D == 128>;
+    const cudaError_t e =
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kT16SmemBytes));
+    if (e != cudaSuccess) return e;
+    k<<<grid, kThreads, kT16SmemBytes, stream>>>(a);
   } else {
     paged ? splitk_kernel<D, 2, true, false, false><<<grid, kThreads, 0, stream>>>(a)
           : splitk_kernel<D, 2, false, false, false><<<grid, kThreads, 0, stream>>>(a);
