@@ -23,12 +23,12 @@
 //               and V from shared memory, S_w(j+1) after P_w V_j. A tcgen05.mma issue blocks at
 //               about the tensor pipe's own rate (one M128 N128 K16 MMA per ~70 cycles, even
 //               with the pipe idle), so an issuer that waits for P leaves the pipe without work;
-//               with one issuer per tile the other tile's MMAs fill that time. The window and
-//               d = 64 instances keep one issuer for both tiles (warp 9; warp 10 idles), in the
-//               order PV0(j), S0(j+1), PV1(j), S1(j+1), which makes the two tiles' softmaxes
-//               alternate. Warps 8-10 each run their loop converged (waits voted across the
-//               warp) and one elected lane issues each copy, MMA and commit, which keeps their
-//               address arithmetic warp-uniform.
+//               with one issuer per tile the other tile's MMAs fill that time. The issuers take
+//               P.V turns in step order (PV0(j), PV1(j), PV0(j+1), ...), which keeps the two
+//               tiles' softmaxes alternating; their S MMAs and waits are not ordered. Warps 8-10
+//               each run their loop converged (waits voted across the warp) and one elected lane
+//               issues each copy, MMA and commit, which keeps their address arithmetic
+//               warp-uniform.
 //   warps 0-3,  softmax warpgroups, one per query tile, thread = row = TMEM lane: read the S
 //   4-7         row, apply the causal mask on diagonal tiles only ("Attention Computation in
 //               Practice", Masking variants: skip / full / diagonal), update m and l in
@@ -90,6 +90,7 @@ struct Barriers {
   uint64_t o_full[2];
   uint64_t o_empty[2];
   uint64_t mma_done[2];
+  uint64_t tok[2];  // PV turn tokens: tok[0] issuer 0 -> 1, tok[1] issuer 1 -> 0
   uint64_t kv_full[6];
   uint64_t kv_empty[6];
   uint64_t item_full[kItemSlots];
@@ -237,11 +238,7 @@ template <int D, bool kWindow>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ TcFwdArgs a,
                                                                  unsigned int* status, unsigned int* sched) {
   using C = Cfg<D>;
-  // MMA issuers: one per query tile, except in the window and d = 64 instances (one for both;
-  // there the tiles' softmaxes do better forced to alternate by a single issue order: short,
-  // window-bounded items, or MMA groups half as long as at d = 128)
-  constexpr int kIssuers = (kWindow || D == 64) ? 1 : 2;
-  constexpr int kItemConsumers = kIssuers + 8;  // one lane of each MMA warp and of each softmax warp
+  constexpr int kItemConsumers = 2 + 8;  // one lane of each MMA warp and of each softmax warp
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;                      // [2][halves][128 rows][128 B]
@@ -254,18 +251,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 
   if (threadIdx.x == 0) {
     mbar_init(&bar->q_full, 1);
-    mbar_init(&bar->q_empty, kIssuers);  // one commit per MMA warp
+    mbar_init(&bar->q_empty, 2);  // one commit per MMA warp
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar->s_full[i], 1);
       mbar_init(&bar->p_full[i], kBM);
       mbar_init(&bar->o_full[i], 1);
       mbar_init(&bar->o_empty[i], kBM);
     }
+    mbar_init(&bar->tok[0], 1);
+    mbar_init(&bar->tok[1], 1);
     mbar_init(&bar->mma_done[0], 1);
     mbar_init(&bar->mma_done[1], 1);
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&bar->kv_full[i], 1);
-      mbar_init(&bar->kv_empty[i], kIssuers);  // one commit per MMA warp
+      mbar_init(&bar->kv_empty[i], 2);  // one commit per MMA warp
     }
     for (int i = 0; i < kItemSlots; ++i) {
       mbar_init(&bar->item_full[i], 1);
@@ -372,140 +371,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       for (int i = max(0, nload - C::kStages); i < nload; ++i)
         mbar_wait(&bar->kv_full[i % C::kStages], (i / C::kStages) & 1, tmo, &no_abort);
     }
-  } else if (kIssuers == 1 && warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
-    // The whole warp runs this loop with identical values (waits are voted, so every lane takes
-    // the same path); the MMA and commit wrappers let one elected lane issue.
-    {
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, 0, 0);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, D, 0, 1);
-      // descriptor halves: K-major Q and K tiles (8-row groups 1024 B apart), MN-major V tiles
-      // (8-key groups 1024 B apart, the two 64-column halves kBN * 128 B apart)
-      const uint32_t hi = sdesc_hi(1024);
-      const uint32_t q_lo0 = sdesc_lo(smem_u32(sQ), 16);
-      const uint32_t q_lo1 = sdesc_lo(smem_u32(sQ) + C::kQBytes, 16);
-      const uint32_t k_lo = sdesc_lo(smem_u32(sRing), 16);
-      const uint32_t v_lo = sdesc_lo(smem_u32(sRing), kBN * 128);
-      const uint32_t slot_step = C::kTileBytes >> 4;
-      const uint32_t tS0 = tbase + C::kColS0, tS1 = tbase + C::kColS1;
-      const uint32_t tO0 = tbase + C::kColO0, tO1 = tbase + C::kColO1;
-      int nload = 0;      // K/V tiles consumed, over all items
-      int items = 0;      // active items
-      int pt0 = 0, pt1 = 0;  // p_full completions consumed per query tile
-      int ou0 = 0, ou1 = 0;  // items whose O accumulator of tile 0 / 1 was used
-      int s_left = 0;     // S MMAs still to issue in the current item
-      bool ok = true;
-
-      auto vote = [](bool x) { return __all_sync(0xffffffffu, x); };
-      auto wait_load = [&](int i) -> bool {
-        const bool r =
-            __all_sync(0xffffffffu, mbar_wait(&bar->kv_full[i % C::kStages], (i / C::kStages) & 1, tmo, abort));
-        tc_fence_after();
-        return r;
-      };
-      auto issue_s = [&](int t, int i) {  // S_t = Q_t K^T, K in load slot of load i
-        const uint32_t kl = k_lo + (i % C::kStages) * slot_step;
-        if constexpr (D == 128)
-          umma_ss_k128(t ? tS1 : tS0, t ? q_lo1 : q_lo0, hi, kl, hi, idesc_qk, 0);
-        else
-          umma_ss_k64(t ? tS1 : tS0, t ? q_lo1 : q_lo0, hi, kl, hi, idesc_qk, 0);
-        umma_commit(&bar->s_full[t]);
-        if (--s_left == 0) umma_commit(&bar->q_empty);  // last read of the Q tiles issued
-      };
-      // O_t += P_t V with V in the load slot of load i: 8 MMAs of K = 16 over the tile's keys
-      auto issue_pv = [&](int t, int i, bool accumulate) {
-        umma_ts_k128(t ? tO1 : tO0, t ? tS1 : tS0, v_lo + (i % C::kStages) * slot_step, hi, idesc_pv,
-                     accumulate ? 1u : 0u);
-      };
-
-      for (int k = 0; ok; ++k) {
-        const ItemRec* rp = wait_item(bar, k, tmo, abort);
-        if (!(ok = rp != nullptr)) break;
-        if (rp->idx < 0) {
-          release_item(bar, k);
-          break;
-        }
-        struct {
-          int nt_all, jmin, j0[2], j1[2], nt[2];
-        } w;
-        w.nt_all = rp->nt_all;
-        w.jmin = rp->jmin;
-        w.j0[0] = rp->j0[0];
-        w.j0[1] = rp->j0[1];
-        w.j1[0] = rp->j1[0];
-        w.j1[1] = rp->j1[1];
-        w.nt[0] = rp->nt[0];
-        w.nt[1] = rp->nt[1];
-        release_item(bar, k);
-        if (!(ok = vote(mbar_wait(&bar->q_full, items & 1, tmo, abort)))) break;
-        tc_fence_after();
-        ++items;
-        const int nt = w.nt_all;
-        const int base = nload;
-        // K/V tile jmin + j is used by query tile t iff j0[t] <= jmin + j < j1[t]
-        const int a0 = w.j0[0] - w.jmin, e0 = w.j1[0] - w.jmin;
-        const int a1 = w.j0[1] - w.jmin, e1 = w.j1[1] - w.jmin;
-        s_left = w.nt[0] + w.nt[1];
-        if (s_left == 0) umma_commit(&bar->q_empty);
-        if (nt > 0) {
-          if (!(ok = wait_load(base))) break;
-          if (a0 == 0 && e0 > 0) issue_s(0, base);
-          if (a1 == 0 && e1 > 0) issue_s(1, base);
-          umma_commit(&bar->kv_empty[base % C::kStages]);
-        }
-        for (int j = 0; j < nt; ++j) {
-          const int iv = base + 2 * j + 1, ik = base + 2 * j + 2;
-          if (!(ok = wait_load(iv))) break;
-          // tile 0: P0 V_j, then S0 for the next K tile
-          if (j >= a0 && j < e0) {
-            // the first P.V of an item overwrites O: the previous item's epilogue must be done
-            if (j == a0 && ou0 > 0 && !(ok = vote(mbar_wait(&bar->o_empty[0], (ou0 - 1) & 1, tmo, abort))))
-              break;
-            if (!(ok = vote(mbar_wait(&bar->p_full[0], pt0 & 1, tmo, abort)))) break;
-            ++pt0;
-            tc_fence_after();
-            issue_pv(0, iv, j > a0);
-            if (j == e0 - 1) {
-              umma_commit(&bar->o_full[0]);
-              ++ou0;
-            }
-          }
-          if (j + 1 < nt && !(ok = wait_load(ik))) break;
-          if (j + 1 >= a0 && j + 1 < e0) issue_s(0, ik);
-          // tile 1
-          if (j >= a1 && j < e1) {
-            if (j == a1 && ou1 > 0 && !(ok = vote(mbar_wait(&bar->o_empty[1], (ou1 - 1) & 1, tmo, abort))))
-              break;
-            if (!(ok = vote(mbar_wait(&bar->p_full[1], pt1 & 1, tmo, abort)))) break;
-            ++pt1;
-            tc_fence_after();
-            issue_pv(1, iv, j > a1);
-            if (j == e1 - 1) {
-              umma_commit(&bar->o_full[1]);
-              ++ou1;
-            }
-          }
-          if (j + 1 >= a1 && j + 1 < e1) issue_s(1, ik);
-          if (j + 1 < nt) umma_commit(&bar->kv_empty[ik % C::kStages]);
-          umma_commit(&bar->kv_empty[iv % C::kStages]);
-        }
-        if (!ok) break;
-        nload += 2 * nt;
-      }
-      if (!ok && lane == 0) raise_timeout(abort, status);
-      // all MMAs issued by this warp complete before TMEM is released
-      const int no_abort = 0;
-      umma_commit(&bar->mma_done[0]);
-      mbar_wait(&bar->mma_done[0], 0, tmo, &no_abort);
-    }
-  } else if (kIssuers == 2 && (warp == kMmaWarp || warp == kMmaWarp + 1)) {
+  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
     // ------------------------------------------------------------ MMA issuers, one per query tile
     // tcgen05.mma issue blocks at about the tensor pipe's own rate, so a single issuing warp that
     // waits (for P, a K/V tile or Q) leaves the pipe with nothing queued; with one issuer per
-    // query tile the other tile's MMAs keep it fed. Each warp runs its loop converged (waits
-    // are voted); the MMA and commit wrappers let one elected lane issue. Both warps release
-    // every K/V slot and the Q buffers (two-arrival barriers), each only after the slot's load
-    // has landed, so neither can arrive for a phase before the previous one has completed.
+    // query tile the other tile's MMAs keep it fed. The two warps take P.V turns in step order
+    // (PV0(j), PV1(j), PV0(j + 1), ...: a token barrier each way, arrived once per step whether
+    // or not the tile has a P.V there), which keeps the two tiles' softmaxes alternating on the
+    // SM's sub-partitions; their S MMAs and their waits are not ordered. Each warp runs its loop
+    // converged (waits are voted); the MMA and commit wrappers let one elected lane issue. Both
+    // warps release every K/V slot and the Q buffers (two-arrival barriers), each only after the
+    // slot's load has landed, so neither can arrive for a phase before the previous one has
+    // completed; the token barriers cannot run two phases ahead either (a warp's next arrival
+    // waits for the other's).
     {
       const int tt = warp - kMmaWarp;  // this warp's query tile
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, 0, 0);
@@ -523,6 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       int items = 0;  // active items
       int pt = 0;     // p_full completions consumed
       int ou = 0;     // items whose O accumulator was used
+      int gs = 0;     // steps of all items so far (both issuers count alike)
       bool ok = true;
 
       auto vote = [](bool x) { return __all_sync(0xffffffffu, x); };
@@ -574,6 +453,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           if ((j < ta || j >= te) && !(ok = wait_load(ik))) break;
           umma_commit(&bar->kv_empty[ik % C::kStages]);
           if (!(ok = wait_load(iv))) break;
+          // P.V turns alternate: PV0(gs), PV1(gs), PV0(gs + 1), ...
+          if (tt == 1) {
+            if (!(ok = vote(mbar_wait(&bar->tok[0], gs & 1, tmo, abort)))) break;
+          } else if (gs > 0) {
+            if (!(ok = vote(mbar_wait(&bar->tok[1], (gs - 1) & 1, tmo, abort)))) break;
+          }
+          bool passed = false;
           if (j >= ta && j < te) {
             // the first P.V of an item overwrites O: the previous item's epilogue must be done
             if (j == ta && ou > 0 && !(ok = vote(mbar_wait(&bar->o_empty[tt], (ou - 1) & 1, tmo, abort)))) break;
@@ -581,6 +467,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             ++pt;
             tc_fence_after();
             issue_pv(iv, j > ta);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar->tok[tt]);
+            passed = true;
             if (j == te - 1) {
               umma_commit(&bar->o_full[tt]);
               ++ou;
@@ -591,6 +480,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
               if (j + 2 == te) umma_commit(&bar->q_empty);  // the tile's last S
             }
           }
+          if (!ok) break;
+          if (!passed) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar->tok[tt]);
+          }
+          ++gs;
           umma_commit(&bar->kv_empty[iv % C::kStages]);
         }
         if (!ok) break;
