@@ -52,10 +52,10 @@ PROFILED_TRAFFIC = {
         "exact_attention_flashattn_gb300/csrc/ptx.cuh",
         "exact_attention_flashattn_gb300/csrc/api.cu",
     ],
-    "sha256": "d307c1e1cb3963cdf2bb7f059b1ef30f7f0b1578326dc1702402814512938388",
-    # (201.57 MB read + 46.59 MB written) at B=2, from the ncu capture summarised under profiles/,
+    "sha256": "8ba5d19cdbb5770e0970ad567c45207fcb54f35ad60bb2d2d346ade5d95278a2",
+    # (201.62 MB read + 45.76 MB written) at B=2, from the ncu capture summarised under profiles/,
     # scaled x2 to the B=4 launch: traffic grows with the number of (batch, head) units
-    "bytes_per_launch": 496326656,
+    "bytes_per_launch": 494776320,
 }
 PROFILED_TRAFFIC_D256 = {
     # the head-dim-256 prefill kernel, its PTX wrappers and the band sizing, hashed in this order
