@@ -14,8 +14,9 @@
 // to one or two bands, whose K/V stay in L2 while every query tile of those heads reads them.
 // The host sizes the band from the K/V bytes of a unit (16 to 64 units). 11 warps per CTA:
 //   warp 8      TMA producer: takes the next item and hands it to the other roles through a
-//               small shared-memory queue; per item, both Q tiles once (after the previous item's last
-//               S MMA freed them), then K_j, V_j tiles (128 keys x d, 128-byte swizzle) into a
+//               small shared-memory queue; per item, each Q tile once (its buffer is free when
+//               that tile's last S MMA of the previous item completed: each tile has its own
+//               full/empty pair), then K_j, V_j tiles (128 keys x d, 128-byte swizzle) into a
 //               ring of shared-memory slots guarded by full/empty mbarriers; the ring runs on
 //               across items.
 //   warps 9,10  MMA issuers, one per query tile w: S_w = Q_w K_j^T into TMEM (fp32, 128 columns
@@ -35,8 +36,9 @@
 //               registers (exp2 with log2(e) folded into the scale), write P as bf16 into TMEM,
 //               rescale O in TMEM when the running max grew by more than 2^8 (a lazily updated
 //               reference max: l and o always share it, so the final o / l is unchanged), and
-//               at the end of the item write O = o / l and the LSE. Tiles entirely above the
-//               diagonal are never loaded.
+//               at the end of the item write O = o / l and the LSE; O goes out through 4 KB of
+//               shared memory per warp so that the global stores write whole 128-byte rows.
+//               Tiles entirely above the diagonal are never loaded.
 // Every wait is bounded; a timed-out wait sets the device status word, the CTA stops
 // producing output, waits for its own copies and MMAs and frees its TMEM.
 #include <math.h>
@@ -63,7 +65,10 @@ struct Cfg {
   static constexpr uint32_t kQBytes = kBM * D * 2;
   static constexpr uint32_t kTileBytes = kBN * D * 2;
   static constexpr int kStages = (D == 128) ? 4 : 6;
-  static constexpr uint32_t kBarOffset = 2 * kQBytes + kStages * kTileBytes;
+  // epilogue staging: 4 KB per softmax warp (32 rows x 64 columns of bf16)
+  static constexpr uint32_t kStageOffset = 2 * kQBytes + kStages * kTileBytes;
+  static constexpr uint32_t kStageBytes = 8 * 4096;
+  static constexpr uint32_t kBarOffset = kStageOffset + kStageBytes;
   static constexpr uint32_t kSmemBytes = kBarOffset + 512 + 1024;  // + barriers, + alignment slack
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
@@ -84,7 +89,7 @@ struct ItemRec {
 };
 
 struct Barriers {
-  uint64_t q_full, q_empty;
+  uint64_t q_full[2], q_empty[2];  // per query tile
   uint64_t s_full[2];
   uint64_t p_full[2];  // P of the current K tile stored in TMEM
   uint64_t o_full[2];
@@ -250,8 +255,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   const int total_items = a.max_pairs * a.num_seqs * a.Hq;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bar->q_full, 1);
-    mbar_init(&bar->q_empty, 2);  // one commit per MMA warp
+    mbar_init(&bar->q_full[0], 1);
+    mbar_init(&bar->q_full[1], 1);
+    mbar_init(&bar->q_empty[0], 1);  // the tile's MMA warp
+    mbar_init(&bar->q_empty[1], 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar->s_full[i], 1);
       mbar_init(&bar->p_full[i], kBM);
@@ -298,6 +305,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       int nload = 0;  // K/V tiles issued by this CTA, over all items
       int items = 0;  // active items started by this CTA
       bool ok = true;
+      // query tile t of the item: its buffer is free once the tile's last S MMA of the previous
+      // item completed
+      auto load_q = [&](const Item& w, int t) -> bool {
+        if (items > 0 && !vote(mbar_wait(&bar->q_empty[t], (items - 1) & 1, tmo, abort))) return false;
+        mbar_arrive_expect_tx(&bar->q_full[t], C::kQBytes);
+        for (int hf = 0; hf < C::kHalves; ++hf)
+          tma_tile(&a.tm_q, w, sQ + t * C::kQBytes + hf * (kBM * 128), &bar->q_full[t], hf, w.q_lo[t], true);
+        return true;
+      };
       for (int k = 0; ok; ++k) {
         // take the next active item from the list and hand it to the consumers
         int idx;
@@ -339,11 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const int n_early = min(2 * w.nt_all, kEarlyLoads);
         for (int i = 0; i < 2 * w.nt_all; ++i, ++nload) {
           if (i == n_early) {
-            if (items > 0 && !(ok = vote(mbar_wait(&bar->q_empty, (items - 1) & 1, tmo, abort)))) break;
-            mbar_arrive_expect_tx(&bar->q_full, 2 * C::kQBytes);
-            for (int t = 0; t < 2; ++t)
-              for (int hf = 0; hf < C::kHalves; ++hf)
-                tma_tile(&a.tm_q, w, sQ + t * C::kQBytes + hf * (kBM * 128), &bar->q_full, hf, w.q_lo[t], true);
+            if (!(ok = load_q(w, 0) && load_q(w, 1))) break;
             ++items;
           }
           const int slot = nload % C::kStages;
@@ -355,11 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                      &bar->kv_full[slot], hf, (w.jmin + (i >> 1)) * kBN, false);
         }
         if (ok && n_early == 2 * w.nt_all) {  // items with no more than kEarlyLoads loads
-          if (items > 0 && !(ok = vote(mbar_wait(&bar->q_empty, (items - 1) & 1, tmo, abort)))) break;
-          mbar_arrive_expect_tx(&bar->q_full, 2 * C::kQBytes);
-          for (int t = 0; t < 2; ++t)
-            for (int hf = 0; hf < C::kHalves; ++hf)
-              tma_tile(&a.tm_q, w, sQ + t * C::kQBytes + hf * (kBM * 128), &bar->q_full, hf, w.q_lo[t], true);
+          if (!(ok = load_q(w, 0) && load_q(w, 1))) break;
           ++items;
         }
       }
@@ -367,7 +375,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       // every copy this CTA issued must have landed before the CTA may exit (bounded, and
       // not cut short by the abort flag)
       const int no_abort = 0;
-      if (items > 0) mbar_wait(&bar->q_full, (items - 1) & 1, tmo, &no_abort);
+      if (items > 0) {
+        mbar_wait(&bar->q_full[0], (items - 1) & 1, tmo, &no_abort);
+        mbar_wait(&bar->q_full[1], (items - 1) & 1, tmo, &no_abort);
+      }
       for (int i = max(0, nload - C::kStages); i < nload; ++i)
         mbar_wait(&bar->kv_full[i % C::kStages], (i / C::kStages) & 1, tmo, &no_abort);
     }
@@ -380,10 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     // or not the tile has a P.V there), which keeps the two tiles' softmaxes alternating on the
     // SM's sub-partitions; their S MMAs and their waits are not ordered. Each warp runs its loop
     // converged (waits are voted); the MMA and commit wrappers let one elected lane issue. Both
-    // warps release every K/V slot and the Q buffers (two-arrival barriers), each only after the
-    // slot's load has landed, so neither can arrive for a phase before the previous one has
-    // completed; the token barriers cannot run two phases ahead either (a warp's next arrival
-    // waits for the other's).
+    // warps release every K/V slot (two-arrival barriers), each only after the slot's load has
+    // landed, so neither can arrive for a phase before the previous one has completed; each warp
+    // releases its own tile's Q buffer. The token barriers cannot run two phases ahead either (a
+    // warp's next arrival waits for the other's).
     {
       const int tt = warp - kMmaWarp;  // this warp's query tile
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, 0, 0);
@@ -437,15 +448,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const int ta = rp->j0[tt] - rp->jmin;
         const int te = ta + rp->nt[tt];
         release_item(bar, k);
-        if (!(ok = vote(mbar_wait(&bar->q_full, items & 1, tmo, abort)))) break;
+        if (!(ok = vote(mbar_wait(&bar->q_full[tt], items & 1, tmo, abort)))) break;
         tc_fence_after();
         ++items;
         const int base = nload;
-        if (te == ta) umma_commit(&bar->q_empty);  // no S MMA reads this tile's Q
+        if (te == ta) umma_commit(&bar->q_empty[tt]);  // no S MMA reads this tile's Q
         if (te > ta) {
           if (!(ok = wait_load(base + 2 * ta))) break;
           issue_s(base + 2 * ta);
-          if (te == ta + 1) umma_commit(&bar->q_empty);
+          if (te == ta + 1) umma_commit(&bar->q_empty[tt]);
         }
         for (int j = 0; j < nt; ++j) {
           const int ik = base + 2 * j, iv = ik + 1;
@@ -477,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
               // S(j + 1) overwrites P(j): it follows this P.V in the warp's (in-order) stream
               if (!(ok = wait_load(ik + 2))) break;
               issue_s(ik + 2);
-              if (j + 2 == te) umma_commit(&bar->q_empty);  // the tile's last S
+              if (j + 2 == te) umma_commit(&bar->q_empty[tt]);  // the tile's last S
             }
           }
           if (!ok) break;
@@ -524,7 +535,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       const int lo = kWindow ? q_row + (wnk - wnq) + 1 - a.window : 0;
       const int ntile = rp->nt[t];
       const int jfirst = rp->j0[t];
-      const int64_t out_idx = rp->out_row0 + static_cast<int64_t>(q_row) * rp->out_row_stride;
+      const int64_t out_row0 = rp->out_row0;
+      const int out_stride = rp->out_row_stride;
+      const int row_w = rp->q_lo[t] + (warp & 3) * 32;  // this warp's first row
       release_item(bar, k);
       float m_ref = -INFINITY, l = 0.f;
       for (int j = 0; j < ntile; ++j) {
@@ -639,30 +652,47 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         tc_fence_after();
       }
       const float inv = (l > 0.f) ? 1.f / l : 0.f;
-      uint16_t* orow = a.o + out_idx * D;
+      // O leaves through this warp's 4 KB of shared memory, 64 columns at a time: each thread
+      // writes its row's 128 bytes (16-byte chunk c of row r at chunk c ^ (r & 7), so a warp's
+      // writes and reads spread over all banks), then each store instruction writes four rows'
+      // 128 contiguous bytes to global memory instead of 16 bytes of 32 rows
+      uint8_t* stg = smem + C::kStageOffset + warp * 4096;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t ov[32];
+      for (int hh = 0; hh < D / 64; ++hh) {
+        uint32_t oa[32], ob[32];
         if (ntile > 0) {
-          tmem_ld32(tO + c * 32, ov);
+          tmem_ld32(tO + hh * 64, oa);
+          tmem_ld32(tO + hh * 64 + 32, ob);
           tmem_wait_ld();
-          tmem_reg_fence(ov);
+          tmem_reg_fence(oa);
+          tmem_reg_fence(ob);
         } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) ov[e] = 0u;
+          for (int e = 0; e < 32; ++e) oa[e] = ob[e] = 0u;
         }
-        if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) {
-            uint4 pkt;
-            pkt.x = pack_bf16x2(__uint_as_float(ov[8 * v4 + 0]) * inv, __uint_as_float(ov[8 * v4 + 1]) * inv);
-            pkt.y = pack_bf16x2(__uint_as_float(ov[8 * v4 + 2]) * inv, __uint_as_float(ov[8 * v4 + 3]) * inv);
-            pkt.z = pack_bf16x2(__uint_as_float(ov[8 * v4 + 4]) * inv, __uint_as_float(ov[8 * v4 + 5]) * inv);
-            pkt.w = pack_bf16x2(__uint_as_float(ov[8 * v4 + 6]) * inv, __uint_as_float(ov[8 * v4 + 7]) * inv);
-            dst[v4] = pkt;
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t* src = (c < 4) ? oa + 8 * c : ob + 8 * (c - 4);
+          uint4 pkt;
+          pkt.x = pack_bf16x2(__uint_as_float(src[0]) * inv, __uint_as_float(src[1]) * inv);
+          pkt.y = pack_bf16x2(__uint_as_float(src[2]) * inv, __uint_as_float(src[3]) * inv);
+          pkt.z = pack_bf16x2(__uint_as_float(src[4]) * inv, __uint_as_float(src[5]) * inv);
+          pkt.w = pack_bf16x2(__uint_as_float(src[6]) * inv, __uint_as_float(src[7]) * inv);
+          *reinterpret_cast<uint4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) = pkt;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rr = i * 4 + (lane >> 3);  // row within the warp's 32
+          const int cc = lane & 7;             // 16-byte chunk of the row's 128 bytes
+          const uint4 v = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((cc ^ (rr & 7)) << 4));
+          const int r = row_w + rr;
+          if (r < wnq) {
+            uint16_t* dst = a.o + (out_row0 + static_cast<int64_t>(r) * out_stride) * D + hh * 64 + cc * 8;
+            *reinterpret_cast<uint4*>(dst) = v;
           }
         }
+        __syncwarp();
       }
       if (ntile > 0) {
         // O has been read: the next item's first P.V may overwrite it
@@ -670,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         mbar_arrive(&bar->o_empty[t]);
       }
       if (row_ok && a.lse)
-        a.lse[out_idx] = (l > 0.f) ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+        a.lse[out_row0 + static_cast<int64_t>(q_row) * out_stride] = (l > 0.f) ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
     }
     if (!ok && lane == 0) raise_timeout(abort, status);
     tc_fence_before();
