@@ -8,29 +8,33 @@
 //
 // GB300 mapping at d = 256. Tensor memory has 512 columns of 128 lanes; an fp32 O tile of 128
 // rows x 256 channels takes 256 of them, so one query tile is in flight per CTA (not two as at
-// d <= 128) and 192 of the other 256 columns hold three 64-column S buffers:
-//   TMEM columns   0..255  O (fp32)        256 + 64 b .. 319 + 64 b  S buffer b (b = 0, 1, 2)
-// K/V tiles are 64 keys x 256 channels (four 128-byte swizzle atoms, 32 KB) in a 5-stage ring;
-// with the 64 KB Q tile that is 224 KB of shared memory (a fourth stage fewer left the tensor
-// pipe waiting for K/V: 10-14 % slower). A work item is one 128-row query tile
+// d <= 128). Q itself sits in tensor memory as the S MMAs' A operand: read from shared memory,
+// an M128 K16 A operand costs the same 4 KB per MMA whatever N is, and with N = 64 (64-key
+// tiles) that made each S MMA take about 72 cycles instead of 32 (clock64 trace of the issuing
+// warp). From tensor memory only K's 2 KB per MMA are read (about 37 cycles per MMA traced).
+//   TMEM columns   0..255  O (fp32)   256..383  Q (bf16 pairs)   384 + 64 b .. 447 + 64 b  S buffer b
+// Shared memory is one ring of seven 32 KB slots (224 KB): an item's Q arrives in two slots (two
+// 128-row atoms each), then its K/V tiles of 64 keys x 256 channels (four 128-byte swizzle
+// atoms) follow in the order the MMA warp consumes them. A work item is one 128-row query tile
 // of a (sequence, head), taken from the same banded list as the d <= 128 kernel (persistent
 // CTAs, atomic counter, longest tiles of a band first). 6 warps per CTA:
-//   warp 4      TMA producer: Q once per item, then the K and V tiles into the ring in the
-//               order the MMA warp consumes them.
-//   warp 5      MMA issuer, in the order S(0), S(1), S(2), PV(0), S(3), PV(1), S(4), ...: S of
-//               the next two K tiles is computed into the other S buffers while the softmax
-//               works on S(j), and S(j+3) reuses S(j)'s buffer only after PV(j) (the tensor pipe
-//               runs in issue order). While the softmax of step j runs, PV(j-1), S(j+1) and
-//               S(j+2) are queued against the softmax of 64 keys per row (one S tile of
-//               lookahead measured 2 % slower).
+//   warp 4      TMA producer: per item the two Q slots, then the K and V tiles.
+//   warp 5      MMA issuer, in the order S(0), S(1), PV(0), S(2), PV(1), S(3), ...: S of the
+//               next K tile is computed into the other S buffer while the softmax works on
+//               S(j), and S(j+2) reuses S(j)'s buffer only after PV(j) (the tensor pipe runs in
+//               issue order). An item's Q slots go back to the producer once the softmax threads
+//               have copied Q into tensor memory.
 //   warps 0-3   softmax, thread = row = TMEM lane: S row (64 scores) from TMEM, mask on tiles
 //               that cross the causal limit or the window start, row max, lazy rescale (the
 //               reference max moves only when the max grows by more than 2^8), P as bf16 into
-//               the first 32 columns of the S buffer, then the item's epilogue O = o / l, LSE.
+//               the first 32 columns of the S buffer. After an item's last step every S MMA of
+//               it has completed, so the threads copy the next item's Q rows from its ring
+//               slots into tensor memory first (the MMA warp starts that item's S MMAs while
+//               they write this item's epilogue O = o / l, LSE).
 // Ordering of a rescale: o may be rescaled in TMEM at step j only after PV(j-1) has completed.
-// PV n commits to pv_done[n % 3]. When the softmax sees S(j), PV(j-3) and every PV before it have
-// completed (S(j) was issued after PV(j-3), and a commit tracks every earlier MMA), and PV(j+2)
-// cannot have been issued (P(j+2) does not exist yet); on pv_done[(j-1) % 3] the only phase that
+// PV n commits to pv_done[n % 2]. When the softmax sees S(j), PV(j-2) and every PV before it have
+// completed (S(j) was issued after PV(j-2), and a commit tracks every earlier MMA), and PV(j+1)
+// cannot have been issued (P(j+1) does not exist yet); on pv_done[(j-1) % 2] the only phase that
 // can still be open is PV(j-1)'s own, so a rescale waits for that parity without ambiguity and the
 // common step waits for no PV at all.
 // Every wait is bounded; a timed-out wait sets the device status word, the CTA stops producing
@@ -51,21 +55,19 @@ constexpr int kAtoms = kD / 64;  // 128-byte swizzle atoms across the head dim
 constexpr int kThreads = 192;
 constexpr int kTmaWarp = 4;
 constexpr int kMmaWarp = 5;
-constexpr int kStages = 5;
-constexpr int kLook = 3;  // S buffers: S(j+1) .. S(j+kLook-1) are issued before PV(j)
+constexpr int kStages = 7;
+constexpr int kLook = 2;  // S buffers: S(j+1) .. S(j+kLook-1) are issued before PV(j)
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kItemSlots = 2;
 constexpr int kItemConsumers = 1 + 4;  // one lane of the MMA warp and of each softmax warp
-constexpr int kEarlyLoads = 2;         // K/V loads of an item issued before its Q
-constexpr uint32_t kQBytes = kBM * kD * 2;     // 64 KB
 constexpr uint32_t kTileBytes = kBN * kD * 2;  // 32 KB
-constexpr uint32_t kBarOffset = kQBytes + kStages * kTileBytes;
+constexpr uint32_t kBarOffset = kStages * kTileBytes;
 constexpr uint32_t kSmemBytes = kBarOffset + 256 + 1024;  // + barriers, + alignment slack
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 0, kColS = 256;  // S buffer b: columns kColS + 64 b
+constexpr uint32_t kColO = 0, kColQ = 256, kColS = 384;  // S buffer b: columns kColS + 64 b
 
 struct Bars {
-  uint64_t q_full, q_empty;
+  uint64_t qt_full;          // Q is in tensor memory
   uint64_t s_full[kLook];
   uint64_t p_full[kLook];
   uint64_t pv_done[kLook];  // PV n completes a phase of pv_done[n % kLook]
@@ -170,17 +172,6 @@ __device__ __forceinline__ void tma_tile(const CUtensorMap* map, const Item& w, 
     tma_load_3d(dst, map, bar, c0, (is_q ? w.q_c1 : w.kv_c1) + row0, is_q ? w.q_c2 : w.kv_c2);
 }
 
-// One MMA D[tmem] (+)= A[smem] B[smem], issued by one elected lane of a converged warp.
-__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint32_t alo, uint32_t ahi, uint32_t blo, uint32_t bhi,
-                                        uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p, pe;\n\t.reg .b64 da, db;\n\telect.sync _|pe, 0xffffffff;\n\t"
-      "setp.ne.b32 p, %6, 0;\n\tmov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
-      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}\n" ::"r"(d_tmem),
-      "r"(alo), "r"(ahi), "r"(blo), "r"(bhi), "r"(idesc), "r"(acc)
-      : "memory");
-}
-
 // One MMA D[tmem] (+)= A[tmem] B[smem].
 __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t blo, uint32_t bhi, uint32_t idesc,
                                         uint32_t acc) {
@@ -192,15 +183,15 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint32
       : "memory");
 }
 
-// S = Q K^T over the 256 channels: 16 K=16 steps, 4 per swizzle atom (the start address moves
-// 32 B within an atom); the next atom is 128 rows x 128 B further for Q, 64 rows x 128 B for K.
-__device__ __forceinline__ void mma_s(uint32_t d_tmem, uint32_t q_lo, uint32_t k_lo, uint32_t hi, uint32_t idesc) {
+// S = Q K^T over the 256 channels: 16 K=16 steps, Q from tensor memory (8 columns = 16 channels
+// per step), K from shared memory 4 steps per swizzle atom (the start address moves 32 B within
+// an atom; the next atom is 64 rows x 128 B further).
+__device__ __forceinline__ void mma_s(uint32_t d_tmem, uint32_t q_tmem, uint32_t k_lo, uint32_t hi, uint32_t idesc) {
 #pragma unroll
   for (int at = 0; at < kAtoms; ++at)
 #pragma unroll
     for (int s = 0; s < 4; ++s)
-      umma_ss(d_tmem, q_lo + at * (kBM * 128 / 16) + 2 * s, hi, k_lo + at * (kBN * 128 / 16) + 2 * s, hi, idesc,
-              (at | s) ? 1u : 0u);
+      umma_ts(d_tmem, q_tmem + at * 32 + 8 * s, k_lo + at * (kBN * 128 / 16) + 2 * s, hi, idesc, (at | s) ? 1u : 0u);
 }
 
 // O (+)= P V over the tile's 64 keys: 4 K=16 steps; P advances 8 TMEM columns (16 bf16) per
@@ -217,8 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc256_kernel(const __grid
                                                                     unsigned int* status, unsigned int* sched) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem;               // [atoms][128 rows][128 B]
-  uint8_t* sRing = smem + kQBytes;  // [stages][atoms][64 rows][128 B]
+  uint8_t* sRing = smem;  // [stages][32 KB]: a K or V tile [atoms][64 rows][128 B], or half of Q [2 atoms][128 rows][128 B]
   Bars* bar = reinterpret_cast<Bars*>(smem + kBarOffset);
 
   const int warp = threadIdx.x >> 5;
@@ -226,8 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc256_kernel(const __grid
   const int total_items = a.max_pairs * a.num_seqs * a.Hq;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bar->q_full, 1);
-    mbar_init(&bar->q_empty, 1);
+    mbar_init(&bar->qt_full, kBM);
     for (int i = 0; i < kLook; ++i) {
       mbar_init(&bar->s_full[i], 1);
       mbar_init(&bar->p_full[i], kBM);
@@ -266,16 +255,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc256_kernel(const __grid
       prefetch_tmap(&a.tm_k);
       prefetch_tmap(&a.tm_v);
     }
-    int nload = 0;  // K/V tiles issued by this CTA, over all items
-    int items = 0;  // items whose Q this CTA loaded
+    int nload = 0;  // ring loads (Q halves and K/V tiles) issued by this CTA, over all items
     bool ok = true;
-    auto load_q = [&](const Item& w) -> bool {
-      if (items > 0 && !vote(mbar_wait(&bar->q_empty, (items - 1) & 1, tmo, abort))) return false;
-      mbar_arrive_expect_tx(&bar->q_full, kQBytes);
-      for (int at = 0; at < kAtoms; ++at) tma_tile(&a.tm_q, w, sQ + at * (kBM * 128), &bar->q_full, at, w.q_lo, true);
-      ++items;
-      return true;
-    };
     for (int k = 0; ok; ++k) {
       int idx;
       Item w;
@@ -294,16 +275,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc256_kernel(const __grid
         mbar_arrive(&bar->item_full[qs]);
       }
       if (idx < 0) break;
-      // the first K/V loads need only ring slots; Q waits until the previous item's last S MMA
-      const int n_early = min(2 * w.nt, kEarlyLoads);
+      // the item's Q in two ring slots (two atoms each), then its K/V tiles
       int kn = 0, vn = 0;  // K and V tiles of the item loaded so far, in the MMA warp's order
-      for (int i = 0; i < 2 * w.nt; ++i, ++nload) {
-        if (i == n_early && !(ok = load_q(w))) break;
-        const bool is_k = kn < w.nt && kn < vn + kLook;
+      for (int i = 0; i < 2 + 2 * w.nt; ++i, ++nload) {
         const int slot = nload % kStages;
         const int round = nload / kStages;
         if (round > 0 && !(ok = vote(mbar_wait(&bar->kv_empty[slot], (round - 1) & 1, tmo, abort)))) break;
         mbar_arrive_expect_tx(&bar->kv_full[slot], kTileBytes);
+        if (i < 2) {
+          for (int h = 0; h < 2; ++h)
+            tma_tile(&a.tm_q, w, sRing + slot * kTileBytes + h * (kBM * 128), &bar->kv_full[slot], 2 * i + h, w.q_lo,
+                     true);
+          continue;
+        }
+        const bool is_k = kn < w.nt && kn < vn + kLook;
         for (int at = 0; at < kAtoms; ++at)
           tma_tile(is_k ? &a.tm_k : &a.tm_v, w, sRing + slot * kTileBytes + at * (kBN * 128), &bar->kv_full[slot],
                    at, (w.j0 + (is_k ? kn : vn)) * kBN, false);
@@ -312,12 +297,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc256_kernel(const __grid
         else
           ++vn;
       }
-      if (ok && n_early == 2 * w.nt) ok = load_q(w);
     }
     if (!ok && lane == 0) raise_timeout(abort, status);
     // every copy this CTA issued lands before the CTA exits (bounded, not cut short by abort)
     const int no_abort = 0;
-    if (items > 0) mbar_wait(&bar->q_full, (items - 1) & 1, tmo, &no_abort);
     for (int i = max(0, nload - kStages); i < nload; ++i)
       mbar_wait(&bar->kv_full[i % kStages], (i / kStages) & 1, tmo, &no_abort);
   } else if (warp == kMmaWarp) {
@@ -325,17 +308,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc256_kernel(const __grid
     constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, 0, 0);
     constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, kD, 0, 1);
     const uint32_t hi = sdesc_hi(1024);
-    const uint32_t q_lo = sdesc_lo(smem_u32(sQ), 16);
     const uint32_t k_lo = sdesc_lo(smem_u32(sRing), 16);
     const uint32_t v_lo = sdesc_lo(smem_u32(sRing), kBN * 128);
     const uint32_t slot_step = kTileBytes >> 4;
     const uint32_t tO = tbase + kColO;
-    int nload = 0;   // K/V tiles consumed, over all items
-    int items = 0;   // items started
+    int nload = 0;   // ring loads consumed (Q halves and K/V tiles), over all items
+    int items = 0;   // items with K/V tiles started (tensor-memory Q copies consumed)
     int ns = 0;      // S MMAs issued, over all items (S buffer ns % kLook)
     int npv = 0;     // PV groups issued, over all items (P of PV n is in S buffer n % kLook)
     int ou = 0;      // items whose O accumulator was used
-    int s_left = 0;  // S MMAs still to issue in the current item
     bool ok = true;
     auto wait_load = [&](int i) -> bool {
       const bool r = vote(mbar_wait(&bar->kv_full[i % kStages], (i / kStages) & 1, tmo, abort));
@@ -343,10 +324,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc256_kernel(const __grid
       return r;
     };
     auto issue_s = [&](int i) {  // S into buffer ns % kLook from K in the slot of load i
-      mma_s(tbase + kColS + 64 * (ns % kLook), q_lo, k_lo + (i % kStages) * slot_step, hi, idesc_qk);
+      mma_s(tbase + kColS + 64 * (ns % kLook), tbase + kColQ, k_lo + (i % kStages) * slot_step, hi, idesc_qk);
       umma_commit(&bar->s_full[ns % kLook]);
       ++ns;
-      if (--s_left == 0) umma_commit(&bar->q_empty);  // last read of the Q tile issued
       umma_commit(&bar->kv_empty[i % kStages]);
     };
     for (int k = 0; ok; ++k) {
@@ -356,13 +336,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc256_kernel(const __grid
       if (lane == 0 && ok) mbar_arrive(&bar->item_empty[k % kItemSlots]);
       if (!ok || idx < 0) break;
       const Item w = make_item<kWindow>(a, idx);
-      if (!(ok = vote(mbar_wait(&bar->q_full, items & 1, tmo, abort)))) break;
-      tc_fence_after();
-      ++items;
       const int nt = w.nt;
-      const int base = nload;
-      s_left = nt;
-      if (nt == 0) umma_commit(&bar->q_empty);
+      // the item's two Q slots go back to the producer once their loads have landed and (items
+      // with tiles) the softmax threads have copied Q into tensor memory
+      if (!(ok = wait_load(nload) && wait_load(nload + 1))) break;
+      if (nt > 0) {
+        if (!(ok = vote(mbar_wait(&bar->qt_full, items & 1, tmo, abort)))) break;
+        tc_fence_after();
+        ++items;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bar->kv_empty[nload % kStages]);
+        mbar_arrive(&bar->kv_empty[(nload + 1) % kStages]);
+      }
+      const int base = nload + 2;
       // the item's 2 nt loads in the order the producer issued them: K tile kn while
       // kn < vn + kLook (S of the next kLook - 1 tiles ahead of each PV), else V tile vn
       int kn = 0, vn = 0;
@@ -389,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc256_kernel(const __grid
         ++vn;
       }
       if (!ok) break;
-      nload += 2 * nt;
+      nload += 2 + 2 * nt;
     }
     if (!ok && lane == 0) raise_timeout(abort, status);
     // all MMAs issued by this warp complete before TMEM is released
@@ -405,13 +393,56 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc256_kernel(const __grid
     int gs = 0;     // key steps done by this CTA, over all items: S buffer gs % kLook, PV index gs
     int oused = 0;  // items whose O accumulator was used
     bool ok = true;
-    for (int k = 0; ok; ++k) {
+    // the k-th item's index from the queue (-1: no more), the slot released
+    auto fetch = [&](int k) -> int {
       const int idx = next_item(bar, k, tmo, abort, &ok);
       ok = vote(ok);
       __syncwarp();
       if (lane == 0 && ok) mbar_arrive(&bar->item_empty[k % kItemSlots]);
-      if (!ok || idx < 0) break;
-      const Item w = make_item<kWindow>(a, idx);
+      return ok ? idx : -1;
+    };
+    // Item k's Q row of this thread goes from the shared-memory landing buffer (128-byte
+    // swizzle: 16-byte chunk c of row r at chunk c ^ (r & 7)) into tensor memory, columns kColQ
+    // on (bf16 pairs, the layout of an A operand read from tensor memory). Called once every S
+    // MMA of the previous item has completed; it frees the landing buffer for the next Q.
+    // Item k's Q row of this thread goes from its two ring slots (loads qb, qb + 1; 128-byte
+    // swizzle: 16-byte chunk c of row r at chunk c ^ (r & 7)) into tensor memory, columns kColQ
+    // on (bf16 pairs, the layout of an A operand read from tensor memory). Called once every S
+    // MMA of the previous item has completed. An item without K/V tiles has no S MMA: its Q is
+    // not copied, and the MMA warp hands its slots back without waiting for a copy.
+    auto q_to_tmem = [&](int qb, bool used) -> bool {
+      if (!used) return true;
+      for (int h = 0; h < 2; ++h)
+        if (!vote(mbar_wait(&bar->kv_full[(qb + h) % kStages], ((qb + h) / kStages) & 1, tmo, abort))) return false;
+      const uint32_t tq = tbase + lane_base + kColQ;
+#pragma unroll 1
+      for (int at = 0; at < kAtoms; ++at) {
+        uint32_t qv[32];
+        const uint8_t* src = sRing + ((qb + (at >> 1)) % kStages) * kTileBytes + (at & 1) * (kBM * 128) + row * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 x = *reinterpret_cast<const uint4*>(src + ((c ^ (row & 7)) << 4));
+          qv[4 * c] = x.x;
+          qv[4 * c + 1] = x.y;
+          qv[4 * c + 2] = x.z;
+          qv[4 * c + 3] = x.w;
+        }
+        tmem_st32(tq + at * 32, qv);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bar->qt_full);
+      return true;
+    };
+    int nl = 0;  // load index of the current item's first Q slot (2 + 2 nt loads per item)
+    int idx = fetch(0);
+    Item w_next;
+    if (ok && idx >= 0) {
+      w_next = make_item<kWindow>(a, idx);
+      ok = q_to_tmem(0, w_next.nt > 0);
+    }
+    for (int k = 0; ok && idx >= 0; ++k) {
+      const Item w = w_next;
       const int q_row = w.q_lo + row;
       const bool row_ok = q_row < w.nq;
       const int lim = a.causal ? min(w.nk, q_row + (w.nk - w.nq) + 1) : w.nk;
@@ -502,6 +533,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc256_kernel(const __grid
         ++gs;
       }
       if (!ok) break;
+      // every S MMA of this item has completed: the next item's Q may replace this one in tensor
+      // memory, and the MMA warp starts its first S while this item's epilogue runs
+      const int idx_next = fetch(k + 1);
+      if (!ok) break;
+      nl += 2 + 2 * w.nt;
+      if (idx_next >= 0) {
+        w_next = make_item<kWindow>(a, idx_next);
+        if (!(ok = q_to_tmem(nl, w_next.nt > 0))) break;
+      }
       // ---- epilogue: O = o / l (bf16), LSE = (m + log2 l) * ln 2
       if (w.nt > 0) {
         if (!(ok = vote(mbar_wait(&bar->o_full, oused & 1, tmo, abort)))) break;
@@ -542,6 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc256_kernel(const __grid
       if (row_ok && a.lse)
         a.lse[w.out_row0 + static_cast<int64_t>(q_row) * w.out_row_stride] =
             (l > 0.f) ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+      idx = idx_next;
     }
     if (!ok && lane == 0) raise_timeout(abort, status);
     tc_fence_before();
