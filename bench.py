@@ -52,10 +52,10 @@ PROFILED_TRAFFIC = {
         "exact_attention_flashattn_gb300/csrc/ptx.cuh",
         "exact_attention_flashattn_gb300/csrc/api.cu",
     ],
-    "sha256": "8ba5d19cdbb5770e0970ad567c45207fcb54f35ad60bb2d2d346ade5d95278a2",
-    # (201.62 MB read + 45.76 MB written) at B=2, from the ncu capture summarised under profiles/,
+    "sha256": "ddd89aa992d80de67a000eb94461ea9ac427d83818ecd1985562385dda54a22c",
+    # (201.67 MB read + 47.41 MB written) at B=2, from the ncu capture summarised under profiles/,
     # scaled x2 to the B=4 launch: traffic grows with the number of (batch, head) units
-    "bytes_per_launch": 494776320,
+    "bytes_per_launch": 498164736,
 }
 PROFILED_TRAFFIC_D256 = {
     # the head-dim-256 prefill kernel, its PTX wrappers and the band sizing, hashed in this order
@@ -64,10 +64,10 @@ PROFILED_TRAFFIC_D256 = {
         "exact_attention_flashattn_gb300/csrc/ptx.cuh",
         "exact_attention_flashattn_gb300/csrc/api.cu",
     ],
-    "sha256": "aeda8c1ebf803e5621be9b7ba4b614d5e988789da8d3417b2de2e8d642b00a52",
-    # (201.58 MB read + 44.71 MB written) at B=2, from the ncu capture summarised under profiles/,
+    "sha256": "1ac9730fd84634d20cecc423de20c1ae6f3af58714c07a899cdea45f6e35cae4",
+    # (201.53 MB read + 43.96 MB written) at B=2, from the ncu capture summarised under profiles/,
     # scaled x2 to the B=4 launch of prefill_causal_b4_h16_n4096_d256
-    "bytes_per_launch": 492587520,
+    "bytes_per_launch": 490985472,
 }
 METRIC = "prefill TFLOP/s and decode KV GB/s, 1×GB300, as fraction of roofline"
 # nominal GB300 figures, the second roofline basis: HBM3e bandwidth of about 8 TB/s and the dense
