@@ -227,9 +227,12 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(const
   extern __shared__ __align__(16) uint8_t dsm[];  // FP8: the load ring, then the combine buffer
   // a dependent merge launch may be scheduled from now on (it waits for this grid to complete)
   asm volatile("griddepcontrol.launch_dependents;");
-  const int split = blockIdx.x;
-  const int hkv = blockIdx.y % a.Hkv;
-  const int grp = blockIdx.y / a.Hkv;
+  // paged caches hold every KV head of a token in one row of a page: their grid runs the heads
+  // fastest, so the CTAs that read the same pages run at the same time
+  const int split = kPaged ? blockIdx.y : blockIdx.x;
+  const int hg = kPaged ? blockIdx.x : blockIdx.y;
+  const int hkv = hg % a.Hkv;
+  const int grp = hg / a.Hkv;
   const int seq = blockIdx.z;
   const UnitGeom u = unit_geom(a, seq, hkv);
   if (!u.active) return;
@@ -1125,10 +1128,11 @@ __global__ void __launch_bounds__(kMergeThreads, 1) merge_kernel(MergeArgs a) {
 
 template <int D>
 cudaError_t launch_splitk_d(const SplitKArgs& a, cudaStream_t stream) {
-  dim3 grid(a.num_splits, a.Hkv * a.row_groups, a.num_seqs);
   // 8-row groups take the transposed form
   const bool half = a.group_rows == 8;
   const bool paged = a.block_table != nullptr;
+  const dim3 grid = paged ? dim3(a.Hkv * a.row_groups, a.num_splits, a.num_seqs)
+                          : dim3(a.num_splits, a.Hkv * a.row_groups, a.num_seqs);
   const bool window = a.causal && a.window > 0;
   const bool fp8 = a.k8 != nullptr;
   if ((paged || fp8) && window) return cudaErrorInvalidValue;  // no entry point pairs them
