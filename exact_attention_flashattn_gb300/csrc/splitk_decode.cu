@@ -686,12 +686,24 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(const
     __syncwarp();
     auto stage_ptr = [&](int s2) { return ring + s2 * kFp8StageBytes + warp * kFp8WarpStepBytes; };
     const int unit_row = seq * a.Hkv + hkv;  // contiguous map: (sequence, KV head) plane
-    auto issue = [&](int kb, int s2) {
+    constexpr int kStride = kWarps * kKeysPerStep;
+    // paged: lane l holds the block-table entry of this warp's step 32 b + l, read once per 32
+    // steps, so a copy's page is a shuffle away instead of a dependent global load
+    int pg_batch = -1, pg_lane = 0;
+    auto page_of_step = [&](int ni) -> int {
+      if ((ni >> 5) != pg_batch) {
+        pg_batch = ni >> 5;
+        const int kbl = kstart + warp * kKeysPerStep + (pg_batch * 32 + lane) * kStride;
+        pg_lane = (kbl < kend) ? a.block_table[static_cast<int64_t>(seq) * a.max_pages + kbl / a.page_size] : 0;
+      }
+      return __shfl_sync(0xffffffffu, pg_lane, ni & 31);
+    };
+    auto issue = [&](int kb, int ni, int s2) {
       if (kb >= kend) return;
       uint8_t* dst = stage_ptr(s2);
       mbar_arrive_expect_tx(&fp8_full[warp][s2], kFp8WarpStepBytes);
       if constexpr (kPaged) {
-        int page = a.block_table[static_cast<int64_t>(seq) * a.max_pages + kb / a.page_size];
+        int page = page_of_step(ni);
         page = min(max(page, 0), a.num_pages - 1);  // a bad entry reads a wrong page, never outside the pool
         const int tok = page * a.page_size + kb % a.page_size;
         tma_load_3d(dst, &a.tm_k8, &fp8_full[warp][s2], 0, hkv, tok);
@@ -710,14 +722,15 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(const
                    : "r"(addr));
       return v;
     };
-    constexpr int kStride = kWarps * kKeysPerStep;
     const int no_abort = 0;
     bool timed_out = false;
     int kb_next = kstart + warp * kKeysPerStep;
+    int n_next = 0;  // this warp's step index of kb_next
 #pragma unroll
     for (int s2 = 0; s2 < kFp8Stages - 1; ++s2) {
-      issue(kb_next, s2);
+      issue(kb_next, n_next, s2);
       kb_next += kStride;
+      ++n_next;
     }
     int st = 0, n = 0;  // stage and index of this warp's current step
     for (int kb = kstart + warp * kKeysPerStep; kb < kend; kb += kStride, ++n) {
@@ -725,8 +738,9 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(const
       // used), and the fence orders them before the copy engine's writes
       __syncwarp();
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      issue(kb_next, st == 0 ? kFp8Stages - 1 : st - 1);
+      issue(kb_next, n_next, st == 0 ? kFp8Stages - 1 : st - 1);
       kb_next += kStride;
+      ++n_next;
       // bounded wait: a copy that never lands ends the warp's loop and sets the status word
       if (!__all_sync(0xffffffffu, mbar_wait(&fp8_full[warp][st], (n / kFp8Stages) & 1, a.timeout_ns, &no_abort))) {
         if (lane == 0 && a.status) atomicOr(a.status, kStatusTimeoutBit);
