@@ -52,7 +52,7 @@ PROFILED_TRAFFIC = {
         "exact_attention_flashattn_gb300/csrc/ptx.cuh",
         "exact_attention_flashattn_gb300/csrc/api.cu",
     ],
-    "sha256": "ddd89aa992d80de67a000eb94461ea9ac427d83818ecd1985562385dda54a22c",
+    "sha256": "96d6f640814efa02f0ed7621d263c6d50250bce88054a3be556c98d0509494a4",
     # (201.67 MB read + 47.41 MB written) at B=2, from the ncu capture summarised under profiles/,
     # scaled x2 to the B=4 launch: traffic grows with the number of (batch, head) units
     "bytes_per_launch": 498164736,

@@ -58,7 +58,7 @@ constexpr int kBM = 128;  // rows per query tile
 constexpr int kBN = 128;  // keys per K/V tile
 constexpr int kThreads = 352;
 constexpr int kTmaWarp = 8;
-constexpr int kMmaWarp = 9;  // warps 9 (query tile 0, or both) and 10 (query tile 1)
+constexpr int kMmaWarp = 9;  // warps 9 (query tile 0) and 10 (query tile 1)
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
 constexpr int kItemSlots = 2;              // depth of the item queue from producer to consumers
 constexpr int kEarlyLoads = 2;             // K/V loads of an item issued before its Q
