@@ -106,6 +106,32 @@ def test_bf16_prefill(B, Hq, Hkv, Nq, Nk, d, causal):
     check_bf16(o, o_ref, lse, lse_ref, what=(B, Hq, Hkv, Nq, Nk, d, causal))
 
 
+@pytest.mark.parametrize("d,H", [(64, 32), (128, 32), (256, 16)])
+def test_prefill_runs_of_items_without_keys(d, H):
+    # causal with 64 keys and 4096 queries: only rows i >= 4032 see a key, so nearly every work
+    # item has no K/V tile; 512 items over at most 152 persistent CTAs put runs of such items on
+    # one CTA (the Q buffers, the d = 256 tensor-memory Q and its barrier phases are still
+    # handed on for them)
+    q, k, v = wl.prefill_inputs(1, H, H, 4096, 64, d, torch.bfloat16, seed=17 + d)
+    o_ref, lse_ref = oracle.attention(f64(q), f64(k), f64(v), True, method="tiled", block=128)
+    o, lse = bw.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True)
+    torch.cuda.synchronize()
+    assert torch.all(o[:, :, :4032] == 0) and torch.all(torch.isneginf(lse[:, :, :4032]))
+    check_bf16(o, o_ref, lse, lse_ref, what=("items without keys", d, H))
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_varlen_long_queries_without_keys(d):
+    # long-query sequences (the tcgen05 path) whose first rows see no key, one with no keys at all
+    nq = [2000, 1500, 700, 1]
+    nk = [10, 0, 600, 5]
+    q, k, v, cq, ck = wl.varlen_inputs(nq, nk, 8, 2, d, torch.bfloat16, seed=23 + d)
+    o_ref, lse_ref = oracle.varlen(f64(q), f64(k), f64(v), cq.numpy(), ck.numpy(), True, method="tiled", block=128)
+    o, lse = bw.attn_varlen(q.cuda(), k.cuda(), v.cuda(), cq.cuda(), ck.cuda(), max(nq), max(nk), causal=True)
+    torch.cuda.synchronize()
+    check_bf16(o, o_ref, lse, lse_ref, what=("varlen without keys", d))
+
+
 def test_bf16_prefill_no_keys():
     q, k, v = wl.prefill_inputs(1, 2, 2, 64, 0, 128, torch.bfloat16, seed=5)
     o, lse = bw.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=False)
