@@ -115,6 +115,8 @@ struct TcFwdArgs {
   int max_pairs;         // work items per (sequence, head): pairs of 128-row query tiles (d = 256: tiles)
   int window;            // > 0: sliding window of that many keys ending at the causal limit
   int band_units;        // (sequence, head) units per band of the item list (at least 1)
+  int head_pair;         // d = 128, even g: a work item is one query tile of two heads that share
+                         // a KV head (units are head pairs, max_pairs counts query tiles)
   float scale_log2;
   uint64_t timeout_ns;
 };

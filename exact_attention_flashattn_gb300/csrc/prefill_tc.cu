@@ -94,7 +94,8 @@ struct ItemRec {
   int nt[2];         // j1 - j0
   int jmin, nt_all;  // K/V tiles the item loads: jmin .. jmin + nt_all - 1
   int out_row_stride;
-  int64_t out_row0;  // output row index of the sequence's first query for this head
+  int out_head_step;  // output rows between the two tiles' heads (head pairs; else 0)
+  int64_t out_row0;  // output row index of the sequence's first query for tile 0's head
 };
 
 struct Barriers {
@@ -129,26 +130,30 @@ struct Item {
   // TMA coordinates: dense maps are {d, rows, seq*heads}, packed maps {d, heads, tokens}
   int q_c1, q_c2, kv_c1, kv_c2;
   bool packed;
-  int64_t out_row0;  // output row index of the sequence's first query for this head
+  int q_dh;          // head pairs: the tiles' Q (and O) heads differ by this (else 0)
+  int64_t out_row0;  // output row index of the sequence's first query for tile 0's head
   int64_t out_row_stride;
+  int64_t out_head_step;
 };
 
 // Item numbering: bands of a.band_units (sequence, head) units; inside a band all units of the
 // last query-tile pair come first, then those of the pair before, and so on (with a causal
 // mask later pairs see more keys).
-template <bool kWindow>
+template <bool kWindow, bool kHeadPair>
 __device__ __forceinline__ Item make_item(const TcFwdArgs& a, int idx) {
   Item w;
-  const int units = a.num_seqs * a.Hq;
+  // a unit is a (sequence, head), or with head pairs a (sequence, head pair)
+  const int hpu = kHeadPair ? a.Hq / 2 : a.Hq;  // units per sequence
+  const int units = a.num_seqs * hpu;
   const int bu = a.band_units;
   const int per_band = bu * a.max_pairs;
   const int band = idx / per_band;
   const int within = idx % per_band;
   const int band_units = min(bu, units - band * bu);
-  const int pair = a.max_pairs - 1 - within / band_units;
+  const int pair = a.max_pairs - 1 - within / band_units;  // query-tile pair, or the query tile
   const int unit = band * bu + within % band_units;
-  const int s = unit / a.Hq;
-  const int h = unit % a.Hq;
+  const int s = unit / hpu;
+  const int h = (unit % hpu) * (kHeadPair ? 2 : 1);  // tile 0's head
   const int g = a.Hq / a.Hkv;
   const int hkv = h / g;
   w.packed = a.cu_q != nullptr;
@@ -163,7 +168,7 @@ __device__ __forceinline__ Item make_item(const TcFwdArgs& a, int idx) {
     w.nq = a.Nq;
     w.nk = a.Nk;
   }
-  w.active = w.nq > 0 && pair * 2 * kBM < w.nq;
+  w.active = w.nq > 0 && pair * (kHeadPair ? 1 : 2) * kBM < w.nq;
   if (w.packed && w.nq * g <= a.small_rows_limit) w.active = false;
   const int shift = w.nk - w.nq;
   if constexpr (!kWindow) {
@@ -171,7 +176,7 @@ __device__ __forceinline__ Item make_item(const TcFwdArgs& a, int idx) {
     w.jmin = 0;
     w.nt_all = 0;
     for (int t = 0; t < 2; ++t) {
-      w.q_lo[t] = pair * 2 * kBM + t * kBM;
+      w.q_lo[t] = kHeadPair ? pair * kBM : pair * 2 * kBM + t * kBM;
       int nt = 0;
       if (w.active && w.q_lo[t] < w.nq) {
         const int q_hi = min(w.q_lo[t] + kBM - 1, w.nq - 1);
@@ -188,7 +193,7 @@ __device__ __forceinline__ Item make_item(const TcFwdArgs& a, int idx) {
     int jmax = 0;
     w.jmin = 0x7fffffff;
     for (int t = 0; t < 2; ++t) {
-      w.q_lo[t] = pair * 2 * kBM + t * kBM;
+      w.q_lo[t] = kHeadPair ? pair * kBM : pair * 2 * kBM + t * kBM;
       int j0 = 0, j1 = 0;
       if (w.active && w.q_lo[t] < w.nq) {
         const int q_hi = min(w.q_lo[t] + kBM - 1, w.nq - 1);
@@ -209,6 +214,7 @@ __device__ __forceinline__ Item make_item(const TcFwdArgs& a, int idx) {
     if (w.jmin > jmax) w.jmin = 0;
     w.nt_all = jmax - w.jmin;
   }
+  w.q_dh = kHeadPair ? 1 : 0;
   if (w.packed) {
     w.q_c1 = h;
     w.q_c2 = tok_q0;  // + row
@@ -216,6 +222,7 @@ __device__ __forceinline__ Item make_item(const TcFwdArgs& a, int idx) {
     w.kv_c2 = tok_k0;  // + key
     w.out_row0 = static_cast<int64_t>(tok_q0) * a.Hq + h;
     w.out_row_stride = a.Hq;
+    w.out_head_step = w.q_dh;
   } else {
     w.q_c1 = 0;  // + row
     w.q_c2 = s * a.Hq + h;
@@ -223,6 +230,7 @@ __device__ __forceinline__ Item make_item(const TcFwdArgs& a, int idx) {
     w.kv_c2 = s * a.Hkv + hkv;
     w.out_row0 = (static_cast<int64_t>(s) * a.Hq + h) * a.Nq;
     w.out_row_stride = 1;
+    w.out_head_step = static_cast<int64_t>(w.q_dh) * a.Nq;
   }
   return w;
 }
@@ -240,17 +248,17 @@ __device__ __forceinline__ void release_item(Barriers* bar, int k) {
 }
 
 __device__ __forceinline__ void tma_tile(const CUtensorMap* map, const Item& w, uint8_t* dst, uint64_t* bar,
-                                         int half, int row0, bool is_q) {
+                                         int half, int row0, bool is_q, int dh = 0) {
   const int c0 = half * 64;
   if (w.packed) {
-    tma_load_3d(dst, map, bar, c0, is_q ? w.q_c1 : w.kv_c1, (is_q ? w.q_c2 : w.kv_c2) + row0);
+    tma_load_3d(dst, map, bar, c0, (is_q ? w.q_c1 : w.kv_c1) + dh, (is_q ? w.q_c2 : w.kv_c2) + row0);
   } else {
-    tma_load_3d(dst, map, bar, c0, (is_q ? w.q_c1 : w.kv_c1) + row0, is_q ? w.q_c2 : w.kv_c2);
+    tma_load_3d(dst, map, bar, c0, (is_q ? w.q_c1 : w.kv_c1) + row0, (is_q ? w.q_c2 : w.kv_c2) + dh);
   }
 }
 
 // kWindow: causal sliding window (its own instance; the plain path keeps K/V tile 0 as start)
-template <int D, bool kWindow>
+template <int D, bool kWindow, bool kHeadPair>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ TcFwdArgs a,
                                                                  unsigned int* status, unsigned int* sched) {
   using C = Cfg<D>;
@@ -263,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int total_items = a.max_pairs * a.num_seqs * a.Hq;
+  const int total_items = a.max_pairs * a.num_seqs * (kHeadPair ? a.Hq / 2 : a.Hq);
 
   if (threadIdx.x == 0) {
     mbar_init(&bar->q_full[0], 1);
@@ -324,7 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         if (items > 0 && !vote(mbar_wait(&bar->q_empty[t], (items - 1) & 1, tmo, abort))) return false;
         mbar_arrive_expect_tx(&bar->q_full[t], C::kQBytes);
         for (int hf = 0; hf < C::kHalves; ++hf)
-          tma_tile(&a.tm_q, w, sQ + t * C::kQBytes + hf * (kBM * 128), &bar->q_full[t], hf, w.q_lo[t], true);
+          tma_tile(&a.tm_q, w, sQ + t * C::kQBytes + hf * (kBM * 128), &bar->q_full[t], hf, w.q_lo[t], true,
+                   kHeadPair ? t : 0);
         return true;
       };
       for (int k = 0; ok; ++k) {
@@ -335,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           int got = 0;
           if (lane == 0) got = static_cast<int>(atomicAdd(&sched[0], 1u));
           idx = __shfl_sync(0xffffffffu, got, 0);
-          if (idx < total_items) w = make_item<kWindow>(a, idx);
+          if (idx < total_items) w = make_item<kWindow, kHeadPair>(a, idx);
         } while (idx < total_items && !w.active);
         if (idx >= total_items) idx = -1;
         const int qs = k % kItemSlots;
@@ -359,6 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             r.nt_all = w.nt_all;
             r.out_row_stride = static_cast<int>(w.out_row_stride);
             r.out_row0 = w.out_row0;
+            if (kHeadPair) r.out_head_step = static_cast<int>(w.out_head_step);
           }
           mbar_arrive(&bar->item_full[qs]);
         }
@@ -573,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       const int lo = kWindow ? q_row + (wnk - wnq) + 1 - a.window : 0;
       const int ntile = rp->nt[t];
       const int jfirst = rp->j0[t];
-      const int64_t out_row0 = rp->out_row0;
+      const int64_t out_row0 = kHeadPair ? rp->out_row0 + static_cast<int64_t>(t) * rp->out_head_step : rp->out_row0;
       const int out_stride = rp->out_row_stride;
       const int row_w = rp->q_lo[t] + (warp & 3) * 32;  // this warp's first row
       release_item(bar, k);
@@ -793,10 +803,10 @@ __global__ void wait_timeout_probe_kernel(uint64_t timeout_ns, unsigned int* sta
 
 int g_num_sms[64] = {};
 
-template <int D, bool kWindow>
+template <int D, bool kWindow, bool kHeadPair>
 cudaError_t launch_d(const TcFwdArgs& a, unsigned int* status, unsigned int* sched, cudaStream_t stream) {
   using C = Cfg<D>;
-  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, kWindow>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, kWindow, kHeadPair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(C::kSmemBytes));
   if (e != cudaSuccess) return e;
   int dev = 0;
@@ -806,10 +816,10 @@ cudaError_t launch_d(const TcFwdArgs& a, unsigned int* status, unsigned int* sch
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) g_num_sms[dev] = sms;
   }
-  const long items = static_cast<long>(a.max_pairs) * a.num_seqs * a.Hq;
+  const long items = static_cast<long>(a.max_pairs) * a.num_seqs * (kHeadPair ? a.Hq / 2 : a.Hq);
   const int grid = static_cast<int>(items < sms ? items : sms);
   if (grid <= 0) return cudaSuccess;
-  prefill_tc_kernel<D, kWindow><<<grid, kThreads, C::kSmemBytes, stream>>>(a, status, sched);
+  prefill_tc_kernel<D, kWindow, kHeadPair><<<grid, kThreads, C::kSmemBytes, stream>>>(a, status, sched);
   return cudaGetLastError();
 }
 
@@ -818,8 +828,10 @@ cudaError_t launch_d(const TcFwdArgs& a, unsigned int* status, unsigned int* sch
 cudaError_t launch_prefill_tc(const TcFwdArgs& a, unsigned int* status, unsigned int* sched, cudaStream_t stream) {
   const bool window = a.causal && a.window > 0;
   if (a.d == 64)
-    return window ? launch_d<64, true>(a, status, sched, stream) : launch_d<64, false>(a, status, sched, stream);
-  return window ? launch_d<128, true>(a, status, sched, stream) : launch_d<128, false>(a, status, sched, stream);
+    return window ? launch_d<64, true, false>(a, status, sched, stream) : launch_d<64, false, false>(a, status, sched, stream);
+  if (a.head_pair)  // two heads of one KV group per item (the host sets it at d = 128 for even g only)
+    return window ? launch_d<128, true, true>(a, status, sched, stream) : launch_d<128, false, true>(a, status, sched, stream);
+  return window ? launch_d<128, true, false>(a, status, sched, stream) : launch_d<128, false, false>(a, status, sched, stream);
 }
 
 cudaError_t launch_wait_timeout_probe(uint64_t timeout_ns, unsigned int* status, cudaStream_t stream) {
