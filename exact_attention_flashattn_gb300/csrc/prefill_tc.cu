@@ -6,7 +6,9 @@
 // exist only on chip, each row keeps a running max m and sum l, the unnormalised output o is
 // rescaled by exp(m - m_new) when the max grows, and O = o / l is written once.
 //
-// GB300 mapping. A work item is two 128-row query tiles of one (sequence, head). The kernel is
+// GB300 mapping. A work item is two 128-row query tiles of one (sequence, head), or (kHeadPair:
+// d = 128 with an even number of query heads per KV head) one query tile of two heads that share
+// a KV head, whose K/V ranges are then identical, so no step runs one tile alone. The kernel is
 // persistent: one CTA per SM takes items from a list in order through an atomic counter
 // (dynamic, so long and short items balance); the producer warp publishes each item with the
 // fields its consumers need already worked out. The list is cut into bands of (sequence, head)
