@@ -52,10 +52,10 @@ PROFILED_TRAFFIC = {
         "exact_attention_flashattn_gb300/csrc/ptx.cuh",
         "exact_attention_flashattn_gb300/csrc/api.cu",
     ],
-    "sha256": "96d6f640814efa02f0ed7621d263c6d50250bce88054a3be556c98d0509494a4",
-    # (201.67 MB read + 47.41 MB written) at B=2, from the ncu capture summarised under profiles/,
+    "sha256": "74eef19d772b4f399c7d07812ae7c90fd210fcf92ad288db08b59fd736befb4b",
+    # (201.60 MB read + 47.01 MB written) at B=2, from the ncu capture summarised under profiles/,
     # scaled x2 to the B=4 launch: traffic grows with the number of (batch, head) units
-    "bytes_per_launch": 498164736,
+    "bytes_per_launch": 497211392,
 }
 PROFILED_TRAFFIC_D256 = {
     # the head-dim-256 prefill kernel, its PTX wrappers and the band sizing, hashed in this order
@@ -64,7 +64,7 @@ PROFILED_TRAFFIC_D256 = {
         "exact_attention_flashattn_gb300/csrc/ptx.cuh",
         "exact_attention_flashattn_gb300/csrc/api.cu",
     ],
-    "sha256": "1ac9730fd84634d20cecc423de20c1ae6f3af58714c07a899cdea45f6e35cae4",
+    "sha256": "b3fac1ead49b3a92c5bf95225c41b0a901fcfa4700841c8076cf7d301235b8ad",
     # (201.53 MB read + 43.96 MB written) at B=2, from the ncu capture summarised under profiles/,
     # scaled x2 to the B=4 launch of prefill_causal_b4_h16_n4096_d256
     "bytes_per_launch": 490985472,
@@ -542,7 +542,7 @@ def main():
     breakdown = {}
     if not args.no_breakdown:
         for name in ("prefill_causal_b4_h16_n4096_d256", "prefill_window_b4_h32_n4096_w1024_d128",
-                     "prefill_causal_b4_h32_n4096_d64"):
+                     "prefill_causal_b4_h32_n4096_d64", "prefill_causal_b4_h32x8_n4096_d128"):
             breakdown[name] = bench_prefill(name, args, world, stream, dev, peaks)
         breakdown["decode_gqa_b8_h32x8_n16384_d256"] = bench_decode("decode_gqa_b8_h32x8_n16384_d256", args, world,
                                                                     stream, dev, peaks)

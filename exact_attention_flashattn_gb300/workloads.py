@@ -30,6 +30,8 @@ Workloads (names give their sizes):
   each, as the d = 128 decode does.
 * ``prefill_causal_b4_h32_n4096_d64``: the causal prefill workload at head dim 64 (the pages'
   smallest fast head dim), same B, heads and lengths.
+* ``prefill_causal_b4_h32x8_n4096_d128``: the causal prefill workload with grouped-query heads
+  (32 query heads over 8 KV heads, the grouping of the decode and varlen workloads).
 """
 from __future__ import annotations
 
@@ -46,6 +48,7 @@ SEED_FP8_GQA = 1006
 SEED_FP8_LONG = 1007
 SEED_D256 = 1008
 SEED_D64 = 1009
+SEED_GQA_PREFILL = 1010
 # FP8 caches: N(0, 1) draws are quantised with 448 / 4.5 codes per unit, so |z| up to 4.5 is
 # representable and larger draws saturate at the largest code
 FP8_SIGMAS = 4.5
@@ -122,6 +125,9 @@ WORKLOADS = {
     "prefill_causal_b4_h32_n4096_d64": Workload("prefill_causal_b4_h32_n4096_d64", "fwd", torch.bfloat16,
                                                 B=4, Hq=32, Hkv=32, Nq=4096, Nk=4096, d=64, causal=True,
                                                 seed=SEED_D64),
+    "prefill_causal_b4_h32x8_n4096_d128": Workload("prefill_causal_b4_h32x8_n4096_d128", "fwd", torch.bfloat16,
+                                                   B=4, Hq=32, Hkv=8, Nq=4096, Nk=4096, d=128, causal=True,
+                                                   seed=SEED_GQA_PREFILL),
     "decode_gqa_b8_h32x8_n16384_d256": Workload("decode_gqa_b8_h32x8_n16384_d256", "decode", torch.bfloat16,
                                                 B=8, Hq=32, Hkv=8, Nq=1, Nk=16384, d=256, causal=False,
                                                 num_splits=8, seed=SEED_D256),

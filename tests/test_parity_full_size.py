@@ -82,7 +82,8 @@ class Acc:
 
 
 @pytest.mark.parametrize("name", ["prefill_causal_b4_h32_n4096_d128", "prefill_window_b4_h32_n4096_w1024_d128",
-                                  "prefill_causal_b4_h16_n4096_d256", "prefill_causal_b4_h32_n4096_d64"])
+                                  "prefill_causal_b4_h16_n4096_d256", "prefill_causal_b4_h32_n4096_d64",
+                                  "prefill_causal_b4_h32x8_n4096_d128"])
 def test_prefill_workload_every_row(name):
     x = wl.make(name, device="cuda")
     w = x["w"]
