@@ -97,6 +97,9 @@ def test_single_head_workload_fp32():
     (1, 2, 2, 200, 90, 128, True),     # more queries than keys
     (2, 2, 1, 384, 384, 64, True),     # head dim 64
     (1, 1, 1, 1, 1, 128, True),        # one query, one key
+    (1, 6, 2, 300, 500, 128, True),    # odd group size 3: tile pairs, not head pairs
+    (1, 12, 2, 260, 260, 128, True),   # group size 6: three head pairs per KV head
+    (2, 4, 2, 300, 300, 128, False),   # head pairs, non-causal, ragged
 ])
 def test_bf16_prefill(B, Hq, Hkv, Nq, Nk, d, causal):
     q, k, v = wl.prefill_inputs(B, Hq, Hkv, Nq, Nk, d, torch.bfloat16, seed=11 + Nq + Nk)
@@ -130,6 +133,18 @@ def test_varlen_long_queries_without_keys(d):
     o, lse = bw.attn_varlen(q.cuda(), k.cuda(), v.cuda(), cq.cuda(), ck.cuda(), max(nq), max(nk), causal=True)
     torch.cuda.synchronize()
     check_bf16(o, o_ref, lse, lse_ref, what=("varlen without keys", d))
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(6, 2), (12, 2)])
+def test_varlen_group_sizes(Hq, Hkv):
+    # long-query sequences at group sizes 3 (tile pairs) and 6 (head pairs), causal
+    nq = [300, 129, 2, 600]
+    nk = [700, 129, 50, 900]
+    q, k, v, cq, ck = wl.varlen_inputs(nq, nk, Hq, Hkv, 128, torch.bfloat16, seed=29 + Hq)
+    o_ref, lse_ref = oracle.varlen(f64(q), f64(k), f64(v), cq.numpy(), ck.numpy(), True, method="tiled", block=128)
+    o, lse = bw.attn_varlen(q.cuda(), k.cuda(), v.cuda(), cq.cuda(), ck.cuda(), max(nq), max(nk), causal=True)
+    torch.cuda.synchronize()
+    check_bf16(o, o_ref, lse, lse_ref, what=("varlen group sizes", Hq, Hkv))
 
 
 def test_bf16_prefill_no_keys():
