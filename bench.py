@@ -52,7 +52,7 @@ PROFILED_TRAFFIC = {
         "exact_attention_flashattn_gb300/csrc/ptx.cuh",
         "exact_attention_flashattn_gb300/csrc/api.cu",
     ],
-    "sha256": "74eef19d772b4f399c7d07812ae7c90fd210fcf92ad288db08b59fd736befb4b",
+    "sha256": "ebfdbdd46bf6f7da7498bd645de40e0ddba3c3b6cc38026d489731331b6c44ea",
     # (201.60 MB read + 47.01 MB written) at B=2, from the ncu capture summarised under profiles/,
     # scaled x2 to the B=4 launch: traffic grows with the number of (batch, head) units
     "bytes_per_launch": 497211392,
@@ -64,7 +64,7 @@ PROFILED_TRAFFIC_D256 = {
         "exact_attention_flashattn_gb300/csrc/ptx.cuh",
         "exact_attention_flashattn_gb300/csrc/api.cu",
     ],
-    "sha256": "b3fac1ead49b3a92c5bf95225c41b0a901fcfa4700841c8076cf7d301235b8ad",
+    "sha256": "5566316b0f9657c6a7d6ce50c4871df68f0ba5e0cfc1e2c17907b76c890f9cf6",
     # (201.53 MB read + 43.96 MB written) at B=2, from the ncu capture summarised under profiles/,
     # scaled x2 to the B=4 launch of prefill_causal_b4_h16_n4096_d256
     "bytes_per_launch": 490985472,

@@ -32,9 +32,15 @@ std::atomic<uint32_t> g_sched_next[kMaxDevices];
 // Launches still in flight by then (other streams, a captured graph replayed alongside) would
 // share it; the header states the limit.
 constexpr uint32_t kTicketSlots = 1u << 16;
-// With more splits than this the separate merge kernel (one CTA per output row) is faster than
-// letting one CTA per unit walk all the splits.
+// Varlen short-query pass: with more splits than this the separate merge kernel (one CTA per
+// output row) is faster than letting one CTA per unit walk all the splits. Below it the fused
+// merge also saves the merge launch's CTAs for every inactive (sequence, row) of the batch
+// (separate merge at 8 splits: 1.000 against 0.949 ms on the 64-sequence append workload).
 constexpr int kFusedMergeMaxSplits = 32;
+// Dense and paged decode: the separate merge, a programmatic dependent launch, is faster from a
+// few splits on (16 splits: bf16 GQA +0.6 %, paged +1.2 %, FP8 GQA +2.5 %, FP8 paged +1.7 %;
+// 8 splits, d = 256: +0.5 %); with this many or fewer the fused merge saves the second launch.
+constexpr int kFusedMergeMaxSplitsDecode = 4;
 __device__ unsigned int g_merge_tickets[kTicketSlots];
 uint32_t g_ticket_next[kMaxDevices] = {};
 
@@ -379,7 +385,7 @@ int run_decode(bw::SplitKArgs& a, int B, int Hq, int Hkv, int g, int num_splits,
   a.small_rows_limit = g;
   a.ws_o_offset = bw::splitk_o_offset(B * Hkv, num_splits, g);
   cudaError_t e;
-  if (num_splits <= kFusedMergeMaxSplits &&
+  if (num_splits <= kFusedMergeMaxSplitsDecode &&
       (e = bw::merge_tickets(B * Hkv * a.row_groups, &a.tickets)) != cudaSuccess)
     return cuda_fail(e);
   a.o = static_cast<uint16_t*>(o);
