@@ -52,7 +52,7 @@ PROFILED_TRAFFIC = {
         "exact_attention_flashattn_gb300/csrc/ptx.cuh",
         "exact_attention_flashattn_gb300/csrc/api.cu",
     ],
-    "sha256": "ebfdbdd46bf6f7da7498bd645de40e0ddba3c3b6cc38026d489731331b6c44ea",
+    "sha256": "5097486066fe23679cddd07f1a0db9e22ec333f13e697b36a987314fc02f8038",
     # (201.60 MB read + 47.01 MB written) at B=2, from the ncu capture summarised under profiles/,
     # scaled x2 to the B=4 launch: traffic grows with the number of (batch, head) units
     "bytes_per_launch": 497211392,
@@ -64,7 +64,7 @@ PROFILED_TRAFFIC_D256 = {
         "exact_attention_flashattn_gb300/csrc/ptx.cuh",
         "exact_attention_flashattn_gb300/csrc/api.cu",
     ],
-    "sha256": "5566316b0f9657c6a7d6ce50c4871df68f0ba5e0cfc1e2c17907b76c890f9cf6",
+    "sha256": "cd5f9e163341ce5d8bba32578c7cbc34a779d9a3a4d16ba1b2c1d72960b9d4c0",
     # (201.53 MB read + 43.96 MB written) at B=2, from the ncu capture summarised under profiles/,
     # scaled x2 to the B=4 launch of prefill_causal_b4_h16_n4096_d256
     "bytes_per_launch": 490985472,

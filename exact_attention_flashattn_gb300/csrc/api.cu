@@ -175,7 +175,10 @@ constexpr int kSmallRowsLimit = 32;  // varlen: n_q * g at or below this takes t
 // more rows takes several row-group CTAs, which read its K/V from L2 after the first) measured
 // 1.194 against 1.093 ms on the 64-sequence append workload.
 constexpr int kVarlenGroupRows = 16;
-constexpr int kVarlenKeysPerSplit = 2048;
+// Keys per split of the short-query pass, which is also the least a split takes (min_chunk):
+// 4096 measured 0.937 ms on the 64-sequence append workload against 0.945 for 2048, 0.984 for
+// 1024 and 0.986 for 8192.
+constexpr int kVarlenKeysPerSplit = 4096;
 constexpr int kVarlenMaxSplits = 64;
 
 int varlen_splits(int max_seqlen_k) {

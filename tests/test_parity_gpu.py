@@ -950,10 +950,10 @@ def test_varlen_with_empty_and_single_token_sequences():
 
 def test_varlen_short_queries_around_the_minimum_split():
     # the longest sequence asks for 5 splits, and every split takes at least 2048 keys: the
-    # short-query sequences (1 .. 4100 keys) leave their later splits empty, and the 2047 / 2048 /
-    # 2049-key ones sit on a split boundary
-    nq = [1, 4, 8, 1, 4, 8, 2, 300]
-    nk = [1, 17, 2047, 2048, 2049, 4100, 700, 10000]
+    # short-query sequences (1 .. 8200 keys) leave their later splits empty, and the ones of 2047 /
+    # 2048 / 2049 and 4095 / 4096 / 4097 keys sit on or next to a split boundary
+    nq = [1, 4, 8, 1, 4, 8, 2, 300, 1, 4, 8]
+    nk = [1, 17, 2047, 2048, 2049, 4100, 700, 10000, 4095, 4096, 8200]
     q, k, v, cq, ck = wl.varlen_inputs(nq, nk, 8, 2, 128, torch.bfloat16, seed=83)
     o_ref, lse_ref = oracle.varlen(f64(q), f64(k), f64(v), cq.numpy(), ck.numpy(), True, method="tiled", block=128)
     o, lse = bw.attn_varlen(q.cuda(), k.cuda(), v.cuda(), cq.cuda(), ck.cuda(), max(nq), max(nk), causal=True)
