@@ -722,19 +722,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       // writes and reads spread over all banks), then each store instruction writes four rows'
       // 128 contiguous bytes to global memory instead of 16 bytes of 32 rows
       uint8_t* stg = smem + C::kStageOffset + warp * 4096;
+      // all of O's columns are requested before one wait
+      uint32_t ov[D / 32][32];
+      if (ntile > 0) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) tmem_ld32(tO + c * 32, ov[c]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) tmem_reg_fence(ov[c]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[c][e] = 0u;
+      }
 #pragma unroll
       for (int hh = 0; hh < D / 64; ++hh) {
-        uint32_t oa[32], ob[32];
-        if (ntile > 0) {
-          tmem_ld32(tO + hh * 64, oa);
-          tmem_ld32(tO + hh * 64 + 32, ob);
-          tmem_wait_ld();
-          tmem_reg_fence(oa);
-          tmem_reg_fence(ob);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) oa[e] = ob[e] = 0u;
-        }
+        const uint32_t (&oa)[32] = ov[2 * hh];
+        const uint32_t (&ob)[32] = ov[2 * hh + 1];
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           const uint32_t* src = (c < 4) ? oa + 8 * c : ob + 8 * (c - 4);
