@@ -52,10 +52,10 @@ PROFILED_TRAFFIC = {
         "exact_attention_flashattn_gb300/csrc/ptx.cuh",
         "exact_attention_flashattn_gb300/csrc/api.cu",
     ],
-    "sha256": "5097486066fe23679cddd07f1a0db9e22ec333f13e697b36a987314fc02f8038",
-    # (201.60 MB read + 47.01 MB written) at B=2, from the ncu capture summarised under profiles/,
+    "sha256": "bdaa55e2d02c9877b03b0f14917a4d7ed1437e1424cf90b2b5744f22fec0bebc",
+    # (201.68 MB read + 47.12 MB written) at B=2, from the ncu capture summarised under profiles/,
     # scaled x2 to the B=4 launch: traffic grows with the number of (batch, head) units
-    "bytes_per_launch": 497211392,
+    "bytes_per_launch": 497586688,
 }
 PROFILED_TRAFFIC_D256 = {
     # the head-dim-256 prefill kernel, its PTX wrappers and the band sizing, hashed in this order
