@@ -1140,6 +1140,140 @@ __global__ void __launch_bounds__(kMergeThreads, 1) merge_kernel(MergeArgs a) {
   if (a.lse && lane == 0) a.lse[orow] = (L > 0.f) ? (M + log2f(L)) * kLn2 : -INFINITY;
 }
 
+// Merge for many splits: the channels of an output row are shared by kMergeGroups CTAs (one
+// per (unit, row, channel group)), so four times as many CTAs each read a quarter of the row's
+// o partials. Every CTA takes the global max and the merged l from all splits' (m, l); its warp
+// lanes are laid out as (split, channel quad), and the lanes of one quad add their splits' sums
+// by shuffles, the warps theirs in shared memory.
+constexpr int kMergeGroups = 4;
+constexpr int kMergeGroupsMinSplits = 64;
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads, 1) merge_cg_kernel(MergeArgs a) {
+  // the split-K pass (the grid this launch depends on) has completed from here on
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int cg = blockIdx.x % kMergeGroups;
+  const int row_id = blockIdx.x / kMergeGroups;
+  const int unit = row_id / a.rows_max;
+  const int r = row_id % a.rows_max;
+  const int seq = unit / a.Hkv, hkv = unit % a.Hkv;
+  int tok0, nq;
+  if (a.cu_q) {
+    tok0 = min(max(a.cu_q[seq], 0), a.total_q);
+    nq = min(max(a.cu_q[seq + 1] - tok0, 0), a.total_q - tok0);
+    if (nq <= 0 || nq * a.g > a.small_rows_limit) return;
+  } else {
+    tok0 = seq;
+    nq = 1;
+  }
+  if (r >= nq * a.g) return;
+  const int i = r / a.g, hh = r % a.g;
+  const int S = a.num_splits;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int kMW = kMergeThreads / 32;
+  constexpr int kQ = (D / 4) / kMergeGroups;  // channel quads of this CTA
+  constexpr int kSL = 32 / kQ;                 // splits side by side in a warp
+  constexpr int kSP = kMW * kSL;               // splits per pass of the CTA
+  constexpr int kUnroll = 8;
+  const int q = lane % kQ, ssub = lane / kQ;
+  const int c4 = cg * kQ + q;
+  const float* ml = a.ws + (static_cast<size_t>(unit) * S * a.rows_max + r) * 2;
+  const float* wo = a.ws + a.ws_o_offset + (static_cast<size_t>(unit) * S * a.rows_max + r) * D + 4 * c4;
+  const size_t ml_stride = static_cast<size_t>(a.rows_max) * 2;
+  const size_t o_stride = static_cast<size_t>(a.rows_max) * D;
+  __shared__ float sh_f[kMergeMaxSplits];
+  __shared__ float sh_red[kMW];
+  __shared__ float4 sh_o[kMW][kQ];
+  __shared__ float sh_l[kMW];
+
+  // this lane's splits: warp * kSL + ssub + p * kSP; the first kUnroll of them are loaded before
+  // the weights are known (every split's o row is written, zeros for an empty split)
+  const int s_lane = warp * kSL + ssub;
+  auto load_rows = [&](int p0, float4 (&x)[kUnroll]) {
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int s = min(s_lane + (p0 + u) * kSP, S - 1);
+      x[u] = *reinterpret_cast<const float4*>(wo + s * o_stride);
+    }
+  };
+  float4 x[kUnroll];
+  load_rows(0, x);
+
+  constexpr int kPT = kMergeMaxSplits / kMergeThreads;
+  float2 v[kPT];
+  float M = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < kPT; ++u) {
+    const int s = threadIdx.x + u * kMergeThreads;
+    v[u] = s < S ? *reinterpret_cast<const float2*>(ml + s * ml_stride) : make_float2(-INFINITY, 0.f);
+    if (v[u].y > 0.f) M = fmaxf(M, v[u].x);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  if (lane == 0) sh_red[warp] = M;
+  __syncthreads();
+  M = sh_red[0];
+#pragma unroll
+  for (int w = 1; w < kMW; ++w) M = fmaxf(M, sh_red[w]);
+  float L = 0.f;
+#pragma unroll
+  for (int u = 0; u < kPT; ++u) {
+    const int s = threadIdx.x + u * kMergeThreads;
+    const float f = v[u].y > 0.f ? ex2(v[u].x - M) : 0.f;
+    L += f * v[u].y;
+    if (s < S) sh_f[s] = f;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  if (lane == 0) sh_l[warp] = L;
+  __syncthreads();
+
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int p0 = 0;;) {
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int s = s_lane + (p0 + u) * kSP;
+      const float f = s < S ? sh_f[s] : 0.f;
+      o.x += f * x[u].x;
+      o.y += f * x[u].y;
+      o.z += f * x[u].z;
+      o.w += f * x[u].w;
+    }
+    p0 += kUnroll;
+    if (p0 * kSP >= S) break;
+    load_rows(p0, x);
+  }
+  // the lanes of one quad: ssub = 0 .. kSL - 1, kQ lanes apart
+#pragma unroll
+  for (int off = kQ; off < 32; off <<= 1) {
+    o.x += __shfl_xor_sync(0xffffffffu, o.x, off);
+    o.y += __shfl_xor_sync(0xffffffffu, o.y, off);
+    o.z += __shfl_xor_sync(0xffffffffu, o.z, off);
+    o.w += __shfl_xor_sync(0xffffffffu, o.w, off);
+  }
+  if (lane < kQ) sh_o[warp][lane] = o;
+  __syncthreads();
+  if (warp != 0 || lane >= kQ) return;
+  L = 0.f;
+#pragma unroll
+  for (int w = 0; w < kMW; ++w) L += sh_l[w];
+  const float inv = (L > 0.f) ? 1.f / L : 0.f;
+  const int64_t orow = (static_cast<int64_t>(tok0 + i) * a.Hq + hkv * a.g + hh);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int w = 0; w < kMW; ++w) {
+    const float4 y = sh_o[w][lane];
+    acc.x += y.x;
+    acc.y += y.y;
+    acc.z += y.z;
+    acc.w += y.w;
+  }
+  uint2 packed;
+  packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+  packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+  *reinterpret_cast<uint2*>(a.o + orow * D + 4 * c4) = packed;
+  if (a.lse && cg == 0 && lane == 0) a.lse[orow] = (L > 0.f) ? (M + log2f(L)) * kLn2 : -INFINITY;
+}
+
 template <int D>
 cudaError_t launch_splitk_d(const SplitKArgs& a, cudaStream_t stream) {
   // 8-row groups take the transposed form
@@ -1199,7 +1333,8 @@ cudaError_t launch_splitk(const SplitKArgs& a, cudaStream_t stream) {
 // pass finishes (the split kernel signals this at its start) and wait for that grid to complete,
 // with its writes visible, before reading any partial.
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
-  const long blocks = static_cast<long>(a.num_seqs) * a.Hkv * a.rows_max;
+  const bool groups = a.num_splits >= kMergeGroupsMinSplits;  // channels over kMergeGroups CTAs
+  const long blocks = static_cast<long>(a.num_seqs) * a.Hkv * a.rows_max * (groups ? kMergeGroups : 1);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(blocks));
   cfg.blockDim = dim3(kMergeThreads);
@@ -1210,9 +1345,9 @@ cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (a.d == 64) return cudaLaunchKernelEx(&cfg, merge_kernel<64>, a);
-  if (a.d == 128) return cudaLaunchKernelEx(&cfg, merge_kernel<128>, a);
-  if (a.d == 256) return cudaLaunchKernelEx(&cfg, merge_kernel<256>, a);
+  if (a.d == 64) return cudaLaunchKernelEx(&cfg, groups ? merge_cg_kernel<64> : merge_kernel<64>, a);
+  if (a.d == 128) return cudaLaunchKernelEx(&cfg, groups ? merge_cg_kernel<128> : merge_kernel<128>, a);
+  if (a.d == 256) return cudaLaunchKernelEx(&cfg, groups ? merge_cg_kernel<256> : merge_kernel<256>, a);
   return cudaErrorInvalidValue;
 }
 

@@ -221,6 +221,21 @@ def test_decode(B, Hq, Hkv, cap, nk, S):
     check_bf16(o, o_ref, lse, lse_ref, what=(B, Hq, Hkv, cap, nk, S))
 
 
+@pytest.mark.parametrize("d,B,Hq,Hkv,cap,nk,S", [
+    (64, 2, 8, 2, 3000, [3000, 0], 64),       # the merge's channel groups at d = 64; an empty sequence
+    (128, 2, 16, 2, 5000, [5000, 1777], 200),  # g = 8, 200 splits (25 keys each, some empty)
+    (256, 1, 8, 2, 4100, [4100], 128),         # d = 256
+    (128, 1, 32, 1, 2000, [2000], 96),         # g = 32: two row groups
+])
+def test_decode_many_splits(d, B, Hq, Hkv, cap, nk, S):
+    # 64 splits and more: the merge kernel spreads each output row's channels over four CTAs
+    q, kc, vc, nkt = wl.decode_inputs(B, Hq, Hkv, cap, d, torch.bfloat16, seed=33 + cap + d, nk=nk)
+    o_ref, lse_ref = oracle.decode(f64(q), f64(kc), f64(vc), nkt.numpy(), method="splitk", workers=S)
+    o, lse = bw.attn_decode(q.cuda(), kc.cuda(), vc.cuda(), nkt.cuda(), num_splits=S)
+    torch.cuda.synchronize()
+    check_bf16(o, o_ref, lse, lse_ref, what=("many splits", d, B, Hq, Hkv, nk, S))
+
+
 def test_decode_ignores_cache_tail_exactly():
     q, kc, vc, nkt = wl.decode_inputs(2, 8, 2, 700, 128, torch.bfloat16, seed=41, nk=[650, 333])
     q, kc, vc, nkt = q.cuda(), kc.cuda(), vc.cuda(), nkt.cuda()
