@@ -52,10 +52,10 @@ PROFILED_TRAFFIC = {
         "exact_attention_flashattn_gb300/csrc/ptx.cuh",
         "exact_attention_flashattn_gb300/csrc/api.cu",
     ],
-    "sha256": "bdaa55e2d02c9877b03b0f14917a4d7ed1437e1424cf90b2b5744f22fec0bebc",
-    # (201.68 MB read + 47.12 MB written) at B=2, from the ncu capture summarised under profiles/,
+    "sha256": "4a42f06d2f3ffa639d3a5c8d525fda36bf81f8de4a32581b7c382824f6e3ded8",
+    # (201.63 MB read + 46.83 MB written) at B=2, from the ncu capture summarised under profiles/,
     # scaled x2 to the B=4 launch: traffic grows with the number of (batch, head) units
-    "bytes_per_launch": 497586688,
+    "bytes_per_launch": 496902144,
 }
 PROFILED_TRAFFIC_D256 = {
     # the head-dim-256 prefill kernel, its PTX wrappers and the band sizing, hashed in this order
@@ -64,10 +64,10 @@ PROFILED_TRAFFIC_D256 = {
         "exact_attention_flashattn_gb300/csrc/ptx.cuh",
         "exact_attention_flashattn_gb300/csrc/api.cu",
     ],
-    "sha256": "cd5f9e163341ce5d8bba32578c7cbc34a779d9a3a4d16ba1b2c1d72960b9d4c0",
-    # (201.53 MB read + 43.96 MB written) at B=2, from the ncu capture summarised under profiles/,
+    "sha256": "ed382ad63bcd39cc126497cffc6c9355df4525849c2c11fe00c560ba319a12cf",
+    # (201.60 MB read + 43.77 MB written) at B=2, from the ncu capture summarised under profiles/,
     # scaled x2 to the B=4 launch of prefill_causal_b4_h16_n4096_d256
-    "bytes_per_launch": 490985472,
+    "bytes_per_launch": 490757120,
 }
 METRIC = "prefill TFLOP/s and decode KV GB/s, 1×GB300, as fraction of roofline"
 # nominal GB300 figures, the second roofline basis: HBM3e bandwidth of about 8 TB/s and the dense

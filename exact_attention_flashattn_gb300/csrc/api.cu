@@ -595,7 +595,8 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
   const float sl2 = scale * bw::kLog2e;
   cudaError_t e;
   // 1) sequences with many queries: tcgen05 prefill kernel over the packed layout
-  if (static_cast<int64_t>(max_seqlen_q) * g > kSmallRowsLimit) {
+  const bool prefill = static_cast<int64_t>(max_seqlen_q) * g > kSmallRowsLimit;
+  if (prefill) {
     bw::TcFwdArgs a{};
     // with no keys at all the K/V maps are never used; they point at q so they stay valid
     const void* kp = total_k > 0 ? k : q;
@@ -669,6 +670,7 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
   s.min_chunk = kVarlenKeysPerSplit;  // 1.6 % faster on the varlen workload than slices sized by the longest sequence
   s.ws_o_offset = bw::splitk_o_offset(units, splits, kSmallRowsLimit);
   s.scale_log2 = sl2;
+  s.after_prefill = prefill ? 1 : 0;  // runs beside the prefill's last items
   if (splits <= kFusedMergeMaxSplits && (e = bw::merge_tickets(units * s.row_groups, &s.tickets)) != cudaSuccess)
     return cuda_fail(e);
   s.o = static_cast<uint16_t*>(o);

@@ -85,6 +85,11 @@ struct SplitKArgs {
   // sets kStatusTimeoutBit in *status (the device status word)
   unsigned int* status;
   uint64_t timeout_ns;
+  // varlen: non-zero when the call's prefill kernel was launched just before on the same stream.
+  // The pass reads nothing that kernel writes, so it is then a programmatic dependent launch whose
+  // CTAs take the SMs the prefill's persistent CTAs leave; its last CTA waits for the prefill grid
+  // to complete, so that this grid (and the work queued after it) completes after the prefill
+  int after_prefill;
 };
 cudaError_t launch_splitk(const SplitKArgs& a, cudaStream_t stream);
 

@@ -276,6 +276,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   const int total_items = a.max_pairs * a.num_seqs * (kHeadPair ? a.Hq / 2 : a.Hq);
 
   if (threadIdx.x == 0) {
+    // packed (varlen) calls: the call's short-query pass, queued after this grid as a
+    // programmatic dependent launch, may be scheduled from now on; its CTAs take the SMs that
+    // these persistent CTAs leave once the item list runs out
+    if (a.cu_q) asm volatile("griddepcontrol.launch_dependents;");
     mbar_init(&bar->q_full[0], 1);
     mbar_init(&bar->q_full[1], 1);
     mbar_init(&bar->q_empty[0], 1);  // the tile's MMA warp

@@ -216,6 +216,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc256_kernel(const __grid
   const int total_items = a.max_pairs * a.num_seqs * a.Hq;
 
   if (threadIdx.x == 0) {
+    // packed (varlen) calls: the call's short-query pass, queued after this grid as a
+    // programmatic dependent launch, may be scheduled from now on; its CTAs take the SMs that
+    // these persistent CTAs leave once the item list runs out
+    if (a.cu_q) asm volatile("griddepcontrol.launch_dependents;");
     mbar_init(&bar->qt_full, kBM);
     for (int i = 0; i < kLook; ++i) {
       mbar_init(&bar->s_full[i], 1);

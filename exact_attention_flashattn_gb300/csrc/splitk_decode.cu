@@ -227,6 +227,10 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 4 : 3) splitk_kernel(const
   extern __shared__ __align__(16) uint8_t dsm[];  // FP8: the load ring, then the combine buffer
   // a dependent merge launch may be scheduled from now on (it waits for this grid to complete)
   asm volatile("griddepcontrol.launch_dependents;");
+  // after a prefill launch this grid may start before that one completes (it reads nothing the
+  // prefill writes); its last CTA waits for it, so that this grid completes after the prefill
+  if (a.after_prefill && blockIdx.x == gridDim.x - 1 && blockIdx.y == gridDim.y - 1 && blockIdx.z == gridDim.z - 1)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
   // paged caches hold every KV head of a token in one row of a page: their grid runs the heads
   // fastest, so the CTAs that read the same pages run at the same time
   const int split = kPaged ? blockIdx.y : blockIdx.x;
@@ -1274,6 +1278,26 @@ __global__ void __launch_bounds__(kMergeThreads, 1) merge_cg_kernel(MergeArgs a)
   if (a.lse && cg == 0 && lane == 0) a.lse[orow] = (L > 0.f) ? (M + log2f(L)) * kLn2 : -INFINITY;
 }
 
+// One split-K launch; after a prefill launch (varlen) a programmatic dependent one.
+template <typename Kernel>
+cudaError_t launch_one(Kernel kernel, dim3 grid, unsigned smem, cudaStream_t stream, const SplitKArgs& a) {
+  if (!a.after_prefill) {
+    kernel<<<grid, kThreads, smem, stream>>>(a);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
 template <int D>
 cudaError_t launch_splitk_d(const SplitKArgs& a, cudaStream_t stream) {
   // 8-row groups take the transposed form
@@ -1292,32 +1316,27 @@ cudaError_t launch_splitk_d(const SplitKArgs& a, cudaStream_t stream) {
       const cudaError_t e =
           cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kFp8SmemBytes));
       if (e != cudaSuccess) return e;
-      k<<<grid, kThreads, kFp8SmemBytes, stream>>>(a);
-      return cudaGetLastError();
+      return launch_one(k, grid, kFp8SmemBytes, stream, a);
     }
   } else if (fp8) {
     return cudaErrorInvalidValue;  // the FP8 cache is d = 128 only
   }
-  if (window) {
-    if (half)
-      splitk_kernel<D, 1, false, true, false><<<grid, kThreads, 0, stream>>>(a);
-    else
-      splitk_kernel<D, 2, false, true, false><<<grid, kThreads, 0, stream>>>(a);
-  } else if (half) {
-    paged ? splitk_kernel<D, 1, true, false, false><<<grid, kThreads, 0, stream>>>(a)
-          : splitk_kernel<D, 1, false, false, false><<<grid, kThreads, 0, stream>>>(a);
-  } else if (D == 128 && !paged && a.tma16) {
+  if (window)
+    return half ? launch_one(splitk_kernel<D, 1, false, true, false>, grid, 0, stream, a)
+                : launch_one(splitk_kernel<D, 2, false, true, false>, grid, 0, stream, a);
+  if (half)
+    return paged ? launch_one(splitk_kernel<D, 1, true, false, false>, grid, 0, stream, a)
+                 : launch_one(splitk_kernel<D, 1, false, false, false>, grid, 0, stream, a);
+  if (D == 128 && !paged && a.tma16) {
     static_assert(kT16SmemBytes >= sizeof(float) * kWarps * kRowsPerGroup * (128 + 4), "combine buffer");
     auto k = splitk_kernel<D, 2, false, false, false, D == 128>;
     const cudaError_t e =
         cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kT16SmemBytes));
     if (e != cudaSuccess) return e;
-    k<<<grid, kThreads, kT16SmemBytes, stream>>>(a);
-  } else {
-    paged ? splitk_kernel<D, 2, true, false, false><<<grid, kThreads, 0, stream>>>(a)
-          : splitk_kernel<D, 2, false, false, false><<<grid, kThreads, 0, stream>>>(a);
+    return launch_one(k, grid, kT16SmemBytes, stream, a);
   }
-  return cudaGetLastError();
+  return paged ? launch_one(splitk_kernel<D, 2, true, false, false>, grid, 0, stream, a)
+               : launch_one(splitk_kernel<D, 2, false, false, false>, grid, 0, stream, a);
 }
 
 }  // namespace

@@ -256,7 +256,10 @@ size_t attn_varlen_workspace_size(int num_seqs, int max_seqlen_k, int Hq, int Hk
  *   causal       : 1 = causal aligned to each sequence's end, 0 = none
  *   workspace    : device buffer of at least attn_varlen_workspace_size(...) bytes
  * Sequences whose n_q * (Hq / Hkv) <= 32 run on the split-K decode kernel (all query heads
- * of a KV group packed in one tile); the others run on the tcgen05 prefill kernel.
+ * of a KV group packed in one tile); the others run on the tcgen05 prefill kernel. When both
+ * run, the split-K pass is a programmatic dependent launch that starts on the SMs the prefill
+ * leaves; it still completes after the prefill, so work queued on `stream` after the call sees
+ * the whole output.
  * Supported: d in {64, 128, 256}, 1 <= g <= 32. Errors as for attn_decode.
  */
 int attn_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens_q,

@@ -1051,6 +1051,64 @@ def test_graph_capture_and_replay_matches_eager():
         assert torch.equal(od, od_e) and torch.equal(ldd, ld_e)
 
 
+def _varlen_prefill_and_short_pass(seed):
+    # one sequence long enough that its prefill items run for a while, beside 40 short-query
+    # sequences for the split-K pass (a programmatic dependent launch after the prefill)
+    nq = [4096] + [(1, 4, 8)[i % 3] for i in range(40)]
+    nk = [8192] + [1000 + 97 * i for i in range(40)]
+    q, k, v, cq, ck = wl.varlen_inputs(nq, nk, 32, 8, 128, torch.bfloat16, seed=seed)
+    return nq, nk, q.cuda(), k.cuda(), v.cuda(), cq.cuda(), ck.cuda()
+
+
+def test_varlen_output_complete_for_the_next_kernel_on_the_stream():
+    # the short-query pass may start before the prefill kernel ends; work queued after the call
+    # must still see every row of both (a copy taken right after the call, without a host sync)
+    nq, nk, q, k, v, cq, ck = _varlen_prefill_and_short_pass(75)
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device="cuda")
+    for _ in range(3):
+        o.fill_(float("nan"))
+        lse.fill_(float("nan"))
+        bw.attn_varlen(q, k, v, cq, ck, max(nq), max(nk), causal=True, out=o, lse=lse)
+        o_next, lse_next = o.clone(), lse.clone()
+        torch.cuda.synchronize()
+        assert torch.isfinite(o_next).all() and torch.isfinite(lse_next).all()
+        assert torch.equal(o_next, o) and torch.equal(lse_next, lse)
+    # rows of the prefill sequence (first, middle, last query) and of short sequences, against
+    # the oracle row by row
+    cql, ckl = cq.tolist(), ck.tolist()
+    for s, i, h in ((0, 0, 0), (0, 2047, 17), (0, 4095, 31), (1, 0, 5), (3, 7, 30), (40, 0, 30)):
+        vis = nk[s] - nq[s] + i + 1
+        qi = f64(q[cql[s] + i, h])[None, None, None]
+        ki = f64(k[ckl[s]:ckl[s] + vis, h // 4])[None, None]
+        vi = f64(v[ckl[s]:ckl[s] + vis, h // 4])[None, None]
+        o_ref, lse_ref = oracle.attention(qi, ki, vi, False, method="naive")
+        assert np.abs(f64(o[cql[s] + i, h]) - o_ref[0, 0, 0]).max() <= TOL_BF16_MAX, (s, i, h)
+        assert abs(float(lse[cql[s] + i, h]) - lse_ref[0, 0, 0]) <= TOL_LSE
+
+
+def test_varlen_graph_capture_and_replay_matches_eager():
+    nq, nk, q, k, v, cq, ck = _varlen_prefill_and_short_pass(76)
+    o_e, l_e = bw.attn_varlen(q, k, v, cq, ck, max(nq), max(nk), causal=True)
+    o, lse = torch.empty_like(o_e), torch.empty_like(l_e)
+    ws = torch.empty(bw.varlen_workspace_size(len(nq), max(nk), 32, 8, 128), dtype=torch.uint8, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        bw.attn_varlen(q, k, v, cq, ck, max(nq), max(nk), causal=True, workspace=ws, out=o, lse=lse)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        bw.attn_varlen(q, k, v, cq, ck, max(nq), max(nk), causal=True, workspace=ws, out=o, lse=lse)
+    for _ in range(3):
+        o.zero_()
+        lse.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(o, o_e) and torch.equal(lse, l_e)
+
+
 def test_concurrent_calls_on_two_streams():
     qd, kc, vc, nk = wl.decode_inputs(4, 16, 4, 1000, 128, torch.bfloat16, seed=73, nk=[1000, 999, 17, 512])
     qd, kc, vc, nk = (t.cuda() for t in (qd, kc, vc, nk))
