@@ -286,11 +286,16 @@ def r4(x):
 
 def roofline_entry(bound, achieved, peaks, unit, **extra):
     """Roofline object on both bases: the measured peak (MEASURED_PEAKS.json, else the fallback)
-    and the nominal one (8 TB/s HBM3e; 2.25 PFLOP/s dense bf16)."""
+    and the nominal one (8 TB/s HBM3e; 2.25 PFLOP/s dense bf16). A tensor-bound entry also
+    carries the measured sustained bf16 figure (cuBLAS looped for seconds under the power cap),
+    the fair denominator when many timed steps run the GPU into that cap."""
     key = "hbm_gbs" if bound == "hbm" else "bf16_tflops"
     out = {"bound": bound, "achieved": r4(achieved), "peak": peaks[key], "unit": unit,
            "frac": r4(achieved / peaks[key]), "peak_nominal": NOMINAL[key],
            "frac_nominal": r4(achieved / NOMINAL[key])}
+    if bound == "tensor":
+        out["peak_sustained"] = peaks["bf16_tflops_sustained"]
+        out["frac_sustained"] = r4(achieved / peaks["bf16_tflops_sustained"])
     out.update(extra)
     return out
 
